@@ -1,0 +1,11 @@
+"""Float64 CPU oracle for the GPT-2 Pre-LN forward (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never does, and this
+package imports nothing from it.
+"""
+from .gpt2_ref import (  # noqa: F401
+    argmax_lowest, block_forward, causal_attention, causal_probs, conv1d, decode_step, embed,
+    forward_hidden, forward_logits, gelu_new, layer_norm, lm_head, merge_heads, mlp_forward,
+    prefill_cache, split_qkv_heads,
+)
