@@ -1,0 +1,395 @@
+"""Benchmark: GPT-2 small forward (B=8, T=1024, bf16 weights and activations,
+fp32 accumulation, fp32 logits) on one GB300, through the libgpt2gb C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  A step is one whole forward (embedding, 12
+blocks, ln_f, tied lm_head) over the [8, 1024] batch of synthetic token ids
+with random-init weights of the GPT-2 small architecture.
+
+* value: tokens / s over K timed steps with inputs resident in HBM; the
+  working set of a step (0.25 GB of weights, 0.16 GB of activations, 1.65 GB
+  of fp32 logits written) is far larger than the 129 MB L2, so no flush is
+  needed between steps.  Every kernel launch inside the timed region is
+  bracketed by CUDA events on its stream (the library's profiler), which
+  gives each kernel's time for the roofline entry and the launch count.
+* e2e: the same step through the same C call, but from pinned host memory:
+  the token ids are copied host -> device and the logits device -> host
+  inside the timed region, every step.
+* roofline: the tcgen05 GEMM (the dominant kernel) -- algorithmic flops
+  (2 M N K per launch) over its event-timed duration, against the measured
+  sustained bf16 peak.
+* cpu_baseline: the float64 oracle on the host cores, on a bounded sample
+  (whole sequences of the same batch, until about 10 s of work).
+* decode: the KV-cache decode step of the same model at B=64 with 1023
+  cached positions, 64 greedy steps, as achieved HBM GB/s.
+* --impl reference: the oracle alone, timed as the reference arm.
+Multi-GPU (torchrun): each rank runs an independent replica on its own GPU
+(the forward has no exchange step); value sums the tokens of all ranks over
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "gpt2_small_fwd_b8_t1024"
+METRIC = "tokens/s GPT-2 small fwd B=8 T=1024 bf16; % tensor-core peak; decode % HBM BW"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _cpu_oracle_time(inp, budget_s=10.0, max_seqs=None):
+    """Time the float64 oracle on whole sequences of the batch until the
+    budget is spent; returns (tokens, seconds, sequences)."""
+    import oracle as O
+    dims, params, tokens = inp["dims"], inp["params"], inp["tokens"]
+    n = tokens.shape[0] if max_seqs is None else min(max_seqs, tokens.shape[0])
+    done, t0 = 0, time.perf_counter()
+    while done < n:
+        O.forward_logits(tokens[done:done + 1], params, dims)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return done * tokens.shape[1], time.perf_counter() - t0, done
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import synth
+    inp = synth.workload_inputs(WORKLOAD)
+    T = inp["tokens"].shape[1]
+    for _ in range(args.warmup):
+        _cpu_oracle_time(inp, budget_s=0.0, max_seqs=1)
+    t0 = time.perf_counter()
+    toks = 0
+    for _ in range(args.steps):
+        n, _, _ = _cpu_oracle_time(inp, budget_s=0.0, max_seqs=1)
+        toks += n
+    dt = time.perf_counter() - t0
+    v = toks / dt
+    sample = f"each step: the float64 oracle forward of 1 of the 8 sequences (T={T}) of the workload"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": 8, "seq_len": T, "sample": "1 sequence per step"},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": _cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def _decode_measure(G, torch, steps=64):
+    """64 greedy decode steps at B=64 over a 1023-long cache; achieved GB/s."""
+    import synth
+    dims = synth.GPT2_SMALL_DECODE
+    B, cache_len = 64, 1023
+    T_max = cache_len + steps
+    params, d = synth.draw_model(dims, "bf16", synth.WORKLOADS["gpt2_small_decode_b64"].seed)
+    dev = G.to_device(params, G.BF16)
+    mw, keep = G.model_weights(dev)
+    cd = G.make_dims(dims.n_layer, dims.d_model, dims.n_head, dims.d_ff, dims.vocab, dims.n_pos, dims.eps, G.BF16)
+    L, H = dims.n_layer, dims.n_head
+    g = torch.Generator(device="cuda").manual_seed(1238)
+    kv = torch.zeros(L, 2, B, H, T_max, 64, device="cuda", dtype=torch.bfloat16)
+    kv[..., :cache_len, :] = torch.randn(L, 2, B, H, cache_len, 64, device="cuda", generator=g).to(torch.bfloat16)
+    tokens0 = torch.from_numpy(synth.draw_tokens(d, B, 1, dims.vocab)[:, 0].copy()).cuda()
+    past = torch.full((B,), cache_len, dtype=torch.int32, device="cuda")
+    tok = tokens0.clone()
+    wsb = G.gpt2_decode_workspace_bytes(cd, B)
+    ws = torch.empty(wsb, device="cuda", dtype=torch.uint8)
+    # warm-up (does not advance the measured state)
+    for _ in range(3):
+        p2 = past.clone()
+        t2 = tok.clone()
+        G.gpt2_decode_step(cd, mw, kv, B, T_max, p2, t2, t2, None, 0, ws, wsb)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    G.gpt2_profile_begin(200 * steps)
+    s.record()
+    for _ in range(steps):
+        G.gpt2_decode_step(cd, mw, kv, B, T_max, past, tok, tok, None, 0, ws, wsb)
+    e.record()
+    torch.cuda.synchronize()
+    G.gpt2_profile_end()
+    prof = G.gpt2_profile_read()
+    ms = s.elapsed_time(e)
+    st, site = G.gpt2_last_error()
+    # algorithmic bytes: every step reads the cached K, V of all layers for
+    # positions 0..p (p = 1023 .. 1086) plus every weight once
+    per_layer_pos = 2 * H * 64 * 2  # K and V, bf16
+    kv_bytes = sum(B * L * (cache_len + s_ + 1) * per_layer_pos for s_ in range(steps))
+    w_bytes = steps * 2 * (dims.vocab * dims.d_model + L * (dims.d_model * 3 * dims.d_model + dims.d_model ** 2 +
+                                                           2 * dims.d_model * dims.d_ff))
+    attn = prof.get("decode_attn", (0, 0.0, 0.0, 0.0))
+    attn_kv = kv_bytes
+    del keep
+    return {
+        "workload": "gpt2_small_decode_b64", "batch": B, "cached": cache_len, "steps": steps,
+        "tokens_per_s": B * steps / (ms / 1e3), "ms_per_step": ms / steps,
+        "algorithmic_gb_per_step": (kv_bytes + w_bytes) / steps / 1e9,
+        "achieved_gbs": (kv_bytes + w_bytes) / (ms / 1e3) / 1e9,
+        "attn_kernel_gbs": attn_kv / (attn[1] / 1e3) / 1e9 if attn[1] > 0 else None,
+        "attn_share": attn[1] / ms if ms > 0 else None,
+        "device_status": st, "launches": sum(v[0] for v in prof.values()),
+    }
+
+
+def _traffic_from_profile():
+    """DRAM bytes per launch of the GEMM, from the committed ncu summary, if
+    it was taken on the current kernel source."""
+    import hashlib
+    summ = os.path.join(ROOT, "profiles", "gemm_bf16_tcgen05_gpt2_small_fwd.md")
+    src = os.path.join(ROOT, "gpt_pre_ln_gb300", "csrc", "gemm_tcgen05.cu")
+    if not os.path.exists(summ):
+        return None
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    for line in open(summ):
+        if line.startswith("traffic_bytes_per_launch:"):
+            parts = line.split()
+            if len(parts) >= 4 and parts[3] == sha:
+                return float(parts[1])
+    return None
+
+
+def run_ours(args):
+    world, rank, local = _dist()
+    import numpy as np
+    import torch
+
+    import gpt_pre_ln_gb300 as G
+    import synth
+    from gpt_pre_ln_gb300 import build as _b
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0 or not os.path.exists(G.library_path):
+        _b.build()
+    if world > 1:
+        dist.barrier()
+    G.lib()
+
+    inp = synth.workload_inputs(WORKLOAD)
+    dims, params, tokens_np = inp["dims"], inp["params"], inp["tokens"]
+    B, T = tokens_np.shape
+    V = dims.vocab
+    dev = G.to_device(params, G.BF16)
+    mw, keep = G.model_weights(dev)
+    cd = G.make_dims(dims.n_layer, dims.d_model, dims.n_head, dims.d_ff, V, dims.n_pos, dims.eps, G.BF16)
+    ld = (V + 7) // 8 * 8
+    logits = torch.empty(B, T, ld, device="cuda", dtype=torch.float32)
+    wsb = G.gpt2_workspace_bytes(cd, B, T)
+    ws = torch.empty(wsb, device="cuda", dtype=torch.uint8)
+    tokens = torch.from_numpy(tokens_np).cuda()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        G.gpt2_forward_logits(cd, mw, tokens, logits, ld, G.F32, B, T, ws, wsb, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    st, site = G.gpt2_last_error()
+    if st != 0:
+        raise RuntimeError(f"device error {st} at site {site} during warm-up")
+
+    # ------------------------------------------------ timed region (device)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    G.gpt2_profile_begin(200 * args.steps)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    G.gpt2_profile_end()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    prof = G.gpt2_profile_read()
+    st, site = G.gpt2_last_error()
+    if st != 0:
+        raise RuntimeError(f"device error {st} at site {site} in the timed region")
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens_all = B * T * args.steps * world
+    value = tokens_all / (ms / 1e3)
+    launches = sum(v[0] for v in prof.values())
+
+    # ---------------------------------------------------------- e2e (host)
+    h_tok = torch.from_numpy(tokens_np.copy()).pin_memory()
+    h_log = torch.empty(B, T, ld, dtype=torch.float32).pin_memory()
+    e2e_steps = max(1, min(args.steps, 5))
+    for _ in range(2):
+        tokens.copy_(h_tok, non_blocking=True)
+        step()
+        h_log.copy_(logits, non_blocking=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        tokens.copy_(h_tok, non_blocking=True)
+        step()
+        h_log.copy_(logits, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = B * T * e2e_steps * world / (e2e_ms / 1e3)
+    assert np.isfinite(h_log[0, 0, :V].numpy()).all()
+
+    # -------------------------------------------------------- roofline etc.
+    peaks = _peaks()
+    gemm = prof.get("gemm_bf16_tcgen05")
+    g_launch_ms = gemm[1] / gemm[0]
+    g_flops_launch = gemm[2] / gemm[0]
+    achieved = g_flops_launch / (g_launch_ms / 1e3) / 1e12
+    total_flops_step = sum(v[2] for v in prof.values()) / args.steps
+    kernels = {k: {"launches_per_step": v[0] / args.steps, "ms_per_step": v[1] / args.steps,
+                   "share": v[1] / sum(x[1] for x in prof.values())} for k, v in prof.items()}
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": B, "seq_len": T, "parallelism": f"replicas x{world}",
+                   "logits": "fp32", "l2": "working set per step > 2 GB, larger than L2 (no flush)"},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": int(B * T * 4),
+                "d2h_bytes_per_step": int(B * T * ld * 4), "steps": e2e_steps},
+        "gpu_launches": launches,
+        "roofline": {"bound": "tensor", "kernel": "gemm_bf16_tcgen05", "achieved": achieved,
+                     "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops_sustained"],
+                     "frac_of_burst": achieved / peaks["bf16_tflops"], "peak_source": peaks["source"],
+                     "traffic": _traffic_from_profile()},
+        "end_to_end_tflops": total_flops_step / (ms / args.steps / 1e3) / 1e12 / world * world,
+        "end_to_end_frac": total_flops_step / (ms / args.steps / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
+        "kernels": kernels,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_decode:
+        dec = _decode_measure(G, torch)
+        dec["frac_of_hbm"] = dec["achieved_gbs"] / peaks["hbm_gbs"]
+        out["decode"] = dec
+    if rank == 0 and world == 1 and not args.no_cpu:
+        toks, secs, seqs = _cpu_oracle_time(inp, budget_s=10.0)
+        out["cpu_baseline"] = {"value": toks / secs, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+                               "sample": f"{seqs} of the 8 sequences (T={T}), float64 oracle, numpy BLAS threads"}
+    del keep
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

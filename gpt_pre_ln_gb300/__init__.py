@@ -1,0 +1,248 @@
+"""Python binding of libgpt2gb, the GB300 (sm_103a) GPT-2 Pre-LN forward library.
+
+Thin ctypes marshalling over the C ABI of ``include/gpt2gb.h``: every
+function here has the name of the C entry point it calls, takes device
+tensors (or raw integer pointers) and sizes, and raises ``GPT2Error`` on a
+non-zero status.  All arithmetic runs in the CUDA library; if the library is
+missing the calls raise instead of falling back to anything else.
+PyTorch is used only for device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "GPT2Error", "F32", "BF16", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_GELU", "EPI_BIAS_RESIDUAL", "W_IN_OUT",
+    "W_OUT_IN", "Dims", "BlockWeights", "ModelWeights", "lib", "library_path", "gpt2_abi_version",
+    "gpt2_status_string", "gpt2_last_error", "gpt2_layernorm", "gpt2_linear", "gpt2_attention_causal",
+    "gpt2_mlp_workspace_bytes", "gpt2_mlp", "gpt2_workspace_bytes", "gpt2_block_forward", "gpt2_forward_logits",
+    "gpt2_kv_cache_bytes", "gpt2_decode_workspace_bytes", "gpt2_decode_step", "gpt2_profile_begin",
+    "gpt2_profile_end", "gpt2_profile_read", "ProfileEntry",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_PKG, "libgpt2gb.so")
+
+F32, BF16 = 0, 1
+EPI_NONE, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESIDUAL = 0, 1, 2, 3
+W_IN_OUT, W_OUT_IN = 0, 1
+
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or type", 3: "workspace too small",
+           4: "CUDA error", 5: "device wait timed out", 6: "token id or position out of range"}
+
+
+class GPT2Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({_STATUS.get(status, 'unknown')})")
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("n_layer", ctypes.c_int), ("d_model", ctypes.c_int), ("n_head", ctypes.c_int),
+                ("d_ff", ctypes.c_int), ("vocab", ctypes.c_int), ("n_pos", ctypes.c_int), ("eps", ctypes.c_float),
+                ("dtype", ctypes.c_int)]
+
+
+_BLOCK_FIELDS = ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_g", "ln2_b", "w_fc", "b_fc", "w_proj",
+                 "b_proj")
+
+
+class BlockWeights(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_void_p) for k in _BLOCK_FIELDS]
+
+
+class ModelWeights(ctypes.Structure):
+    _fields_ = [("wte", ctypes.c_void_p), ("wpe", ctypes.c_void_p), ("lnf_g", ctypes.c_void_p),
+                ("lnf_b", ctypes.c_void_p), ("blocks", ctypes.POINTER(BlockWeights))]
+
+
+class ProfileEntry(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int), ("ms", ctypes.c_double),
+                ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
+
+
+_lib = None
+_VP, _I64, _I32, _SZ, _F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+_SIGS = {
+    "gpt2_abi_version": (_I32, []),
+    "gpt2_status_string": (ctypes.c_char_p, [_I32]),
+    "gpt2_last_error": (_I32, [ctypes.POINTER(ctypes.c_int)]),
+    "gpt2_layernorm": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _F, _I32, _I32, _VP]),
+    "gpt2_linear": (_I32, [_VP, _VP, _VP, _VP, _VP, _I64, _I32, _I32, _I64, _I32, _I32, _I32, _I32, _VP]),
+    "gpt2_attention_causal": (_I32, [_VP, _VP, _I32, _I32, _I32, _I32, _I32, _VP]),
+    "gpt2_mlp_workspace_bytes": (_SZ, [_I64, _I32, _I32]),
+    "gpt2_mlp": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I32, _I32, _VP, _SZ, _I32, _VP]),
+    "gpt2_workspace_bytes": (_SZ, [ctypes.POINTER(Dims), _I32, _I32]),
+    "gpt2_block_forward": (_I32, [ctypes.POINTER(Dims), ctypes.POINTER(BlockWeights), _VP, _VP, _I32, _I32, _VP, _SZ,
+                                  _VP]),
+    "gpt2_forward_logits": (_I32, [ctypes.POINTER(Dims), ctypes.POINTER(ModelWeights), _VP, _VP, _I64, _I32, _I32,
+                                   _I32, _VP, _SZ, _VP]),
+    "gpt2_kv_cache_bytes": (_SZ, [ctypes.POINTER(Dims), _I32, _I32]),
+    "gpt2_decode_workspace_bytes": (_SZ, [ctypes.POINTER(Dims), _I32]),
+    "gpt2_decode_step": (_I32, [ctypes.POINTER(Dims), ctypes.POINTER(ModelWeights), _VP, _I32, _I32, _VP, _VP, _VP,
+                                _VP, _I64, _VP, _SZ, _VP]),
+    "gpt2_profile_begin": (_I32, [_I32]),
+    "gpt2_profile_end": (_I32, []),
+    "gpt2_profile_read": (_I32, [ctypes.POINTER(ProfileEntry), _I32, ctypes.POINTER(ctypes.c_int)]),
+}
+
+
+def lib():
+    """Load libgpt2gb.so (built by ``gpt_pre_ln_gb300.build``); raises if absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(f"{library_path} is missing: run `python -m gpt_pre_ln_gb300.build` first")
+        L = ctypes.CDLL(library_path)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise GPT2Error(status, where)
+
+
+# ------------------------------------------------------------- entry points
+def gpt2_abi_version() -> int:
+    return lib().gpt2_abi_version()
+
+
+def gpt2_status_string(status: int) -> str:
+    return lib().gpt2_status_string(status).decode()
+
+
+def gpt2_last_error():
+    """(status, site) of the first device-side fault since the last call."""
+    site = ctypes.c_int(0)
+    st = lib().gpt2_last_error(ctypes.byref(site))
+    return st, site.value
+
+
+def gpt2_layernorm(x, gamma, beta, y, rows, D, eps, x_t, y_t, stream=None):
+    _check(lib().gpt2_layernorm(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), rows, D, eps, x_t, y_t, _stream(stream)),
+           "gpt2_layernorm")
+
+
+def gpt2_linear(x, w, bias, residual, y, M, N, K, ldy, w_layout, epilogue, dtype, y_t, stream=None):
+    _check(lib().gpt2_linear(_ptr(x), _ptr(w), _ptr(bias), _ptr(residual), _ptr(y), M, N, K, ldy, w_layout, epilogue,
+                             dtype, y_t, _stream(stream)), "gpt2_linear")
+
+
+def gpt2_attention_causal(qkv, out, B, T, n_head, head_dim, dtype, stream=None):
+    _check(lib().gpt2_attention_causal(_ptr(qkv), _ptr(out), B, T, n_head, head_dim, dtype, _stream(stream)),
+           "gpt2_attention_causal")
+
+
+def gpt2_mlp_workspace_bytes(M, F, dtype) -> int:
+    return lib().gpt2_mlp_workspace_bytes(M, F, dtype)
+
+
+def gpt2_mlp(x, w_fc, b_fc, w_proj, b_proj, residual, out, M, D, F, ws, ws_bytes, dtype, stream=None):
+    _check(lib().gpt2_mlp(_ptr(x), _ptr(w_fc), _ptr(b_fc), _ptr(w_proj), _ptr(b_proj), _ptr(residual), _ptr(out), M,
+                          D, F, _ptr(ws), ws_bytes, dtype, _stream(stream)), "gpt2_mlp")
+
+
+def gpt2_workspace_bytes(dims: Dims, B: int, T: int) -> int:
+    return lib().gpt2_workspace_bytes(ctypes.byref(dims), B, T)
+
+
+def gpt2_block_forward(dims: Dims, w: BlockWeights, x_in, x_out, B, T, ws, ws_bytes, stream=None):
+    _check(lib().gpt2_block_forward(ctypes.byref(dims), ctypes.byref(w), _ptr(x_in), _ptr(x_out), B, T, _ptr(ws),
+                                    ws_bytes, _stream(stream)), "gpt2_block_forward")
+
+
+def gpt2_forward_logits(dims: Dims, w: ModelWeights, tokens, logits, ld, logits_t, B, T, ws, ws_bytes, stream=None):
+    _check(lib().gpt2_forward_logits(ctypes.byref(dims), ctypes.byref(w), _ptr(tokens), _ptr(logits), ld, logits_t,
+                                     B, T, _ptr(ws), ws_bytes, _stream(stream)), "gpt2_forward_logits")
+
+
+def gpt2_kv_cache_bytes(dims: Dims, B: int, T_max: int) -> int:
+    return lib().gpt2_kv_cache_bytes(ctypes.byref(dims), B, T_max)
+
+
+def gpt2_decode_workspace_bytes(dims: Dims, B: int) -> int:
+    return lib().gpt2_decode_workspace_bytes(ctypes.byref(dims), B)
+
+
+def gpt2_decode_step(dims: Dims, w: ModelWeights, kv_cache, B, T_max, past_len, tokens, next_tokens, logits_opt, ld,
+                     ws, ws_bytes, stream=None):
+    _check(lib().gpt2_decode_step(ctypes.byref(dims), ctypes.byref(w), _ptr(kv_cache), B, T_max, _ptr(past_len),
+                                  _ptr(tokens), _ptr(next_tokens), _ptr(logits_opt), ld, _ptr(ws), ws_bytes,
+                                  _stream(stream)), "gpt2_decode_step")
+
+
+def gpt2_profile_begin(max_launches: int):
+    _check(lib().gpt2_profile_begin(max_launches), "gpt2_profile_begin")
+
+
+def gpt2_profile_end():
+    _check(lib().gpt2_profile_end(), "gpt2_profile_end")
+
+
+def gpt2_profile_read(max_entries: int = 64):
+    """{kernel name: (launches, ms, flops, bytes)} of the last profiled span."""
+    arr = (ProfileEntry * max_entries)()
+    n = ctypes.c_int(0)
+    _check(lib().gpt2_profile_read(arr, max_entries, ctypes.byref(n)), "gpt2_profile_read")
+    return {arr[i].name.decode(): (arr[i].launches, arr[i].ms, arr[i].flops, arr[i].bytes)
+            for i in range(min(n.value, max_entries))}
+
+
+# ------------------------------------------------------ weight marshalling
+def make_dims(n_layer, d_model, n_head, d_ff, vocab, n_pos, eps=1e-5, dtype=BF16) -> Dims:
+    return Dims(n_layer, d_model, n_head, d_ff, vocab, n_pos, eps, dtype)
+
+
+def block_weights(tensors: dict) -> BlockWeights:
+    """BlockWeights from a dict of device tensors keyed like the C struct."""
+    return BlockWeights(*[_ptr(tensors[k]) for k in _BLOCK_FIELDS])
+
+
+def model_weights(tensors: dict):
+    """(ModelWeights, keep-alive) from {wte, wpe, lnf_g, lnf_b, blocks: [dict]}."""
+    blocks = (BlockWeights * len(tensors["blocks"]))(*[block_weights(b) for b in tensors["blocks"]])
+    mw = ModelWeights(_ptr(tensors["wte"]), _ptr(tensors["wpe"]), _ptr(tensors["lnf_g"]), _ptr(tensors["lnf_b"]),
+                      ctypes.cast(blocks, ctypes.POINTER(BlockWeights)))
+    return mw, blocks
+
+
+def to_device(params: dict, dtype: int, device="cuda"):
+    """Copy a parameter dict of float32 numpy arrays to device tensors.
+
+    Arrays are converted to bf16 (``dtype == BF16``) or kept fp32; the values
+    are expected to be exactly representable already.  Returns the same
+    nesting ({..., "blocks": [dict]}) with torch tensors.
+    """
+    import numpy as np
+    import torch
+    tdt = torch.bfloat16 if dtype == BF16 else torch.float32
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device=device).to(tdt).contiguous()
+
+    out = {k: up(v) for k, v in params.items() if k != "blocks"}
+    out["blocks"] = [{k: up(v) for k, v in b.items()} for b in params["blocks"]]
+    return out

@@ -1,0 +1,552 @@
+// C-ABI entry points of libgpt2gb (declared in include/gpt2gb.h): argument
+// validation, workspace carving, and the order of kernel launches of the
+// GPT-2 Pre-LN forward, block, MLP and decode step.
+//
+// Block dataflow ("Hidden State 如何流过 GPT-2 Block", section "GPT-2 Block";
+// "逐行拆GPT-2源码", GPT2Block.forward):
+//   a   = LN_1(x)                          layernorm (fused with the
+//                                          embedding for the first block)
+//   qkv = a W_qkv + b_qkv                  GEMM, epilogue + bias
+//   o   = causal attention(qkv)            attention kernel
+//   h   = x + o W_o + b_o                  GEMM, epilogue + bias + residual
+//   a   = LN_2(h)                          layernorm
+//   g   = gelu_new(a W_fc + b_fc)          GEMM, epilogue gelu_new(+ bias)
+//   x'  = h + g W_proj + b_proj            GEMM, epilogue + bias + residual
+// then LN_f and the tied lm_head (GEMM against wte [V, D], no bias).
+#include <climits>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gpt2 {
+
+__device__ unsigned g_error_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+unsigned* g_err_ptr[kMaxDevices] = {nullptr};
+int g_sms[kMaxDevices] = {0};
+std::mutex g_mu;
+
+int current_device() {
+  int d = 0;
+  cudaGetDevice(&d);
+  return d;
+}
+
+}  // namespace
+
+unsigned* device_error_word() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return nullptr;
+  if (!g_err_ptr[d]) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[d]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_error_word) == cudaSuccess) g_err_ptr[d] = static_cast<unsigned*>(p);
+    }
+  }
+  return g_err_ptr[d];
+}
+
+int num_sms() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return 1;
+  if (!g_sms[d]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
+    g_sms[d] = n > 0 ? n : 1;
+  }
+  return g_sms[d];
+}
+
+}  // namespace gpt2
+
+using namespace gpt2;
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+
+// ------------------------------------------------------------- profiler
+struct ProfRec {
+  int name_id;
+  int ev0;  // events ev0 (start) and ev0 + 1 (end)
+  double flops, bytes;
+};
+
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  std::vector<cudaEvent_t> ev;
+  int next_ev = 0;
+  std::vector<ProfRec> recs;
+  std::vector<std::string> names;
+
+  void release() {
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    ev.clear();
+    recs.clear();
+    names.clear();
+    next_ev = 0;
+  }
+  int name_id(const char* n) {
+    for (size_t i = 0; i < names.size(); ++i)
+      if (names[i] == n) return static_cast<int>(i);
+    names.emplace_back(n);
+    return static_cast<int>(names.size() - 1);
+  }
+};
+Profiler g_prof;
+
+// Brackets one kernel launch with events on its stream while profiling is on.
+class ProfScope {
+ public:
+  ProfScope(const char* name, double flops, double bytes, cudaStream_t s) : s_(s) {
+    if (!g_prof.on) return;
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    if (!g_prof.on || g_prof.next_ev + 2 > static_cast<int>(g_prof.ev.size())) return;
+    idx_ = g_prof.next_ev;
+    g_prof.next_ev += 2;
+    g_prof.recs.push_back({g_prof.name_id(name), idx_, flops, bytes});
+    cudaEventRecord(g_prof.ev[idx_], s_);
+  }
+  ~ProfScope() {
+    if (idx_ >= 0) cudaEventRecord(g_prof.ev[idx_ + 1], s_);
+  }
+  ProfScope(const ProfScope&) = delete;
+  ProfScope& operator=(const ProfScope&) = delete;
+
+ private:
+  cudaStream_t s_;
+  int idx_ = -1;
+};
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+inline size_t esize(gpt2_dtype t) { return t == GPT2_BF16 ? 2 : 4; }
+inline bool valid_dtype(int t) { return t == GPT2_F32 || t == GPT2_BF16; }
+inline cudaStream_t cs(gpt2_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+struct Carve {
+  char* base;
+  size_t off = 0;
+  explicit Carve(void* p) : base(static_cast<char*>(p)) {}
+  template <typename T>
+  T* take(size_t count, size_t elem) {
+    T* r = reinterpret_cast<T*>(base + off);
+    off += align256(count * elem);
+    return r;
+  }
+};
+
+// Checks the shape fields of a dims struct; `need_model` adds n_layer,
+// vocab and n_pos.
+int check_dims(const gpt2_dims* d, bool need_model) {
+  if (!d) return GPT2_ERR_ARG;
+  if (!valid_dtype(d->dtype)) return GPT2_ERR_ARG;
+  if (d->d_model <= 0 || d->n_head <= 0 || d->d_ff <= 0) return GPT2_ERR_ARG;
+  if (!(d->eps > 0.f) || !std::isfinite(d->eps)) return GPT2_ERR_ARG;
+  if (d->d_model % d->n_head != 0 || d->d_model / d->n_head != 64) return GPT2_ERR_UNSUPPORTED;
+  if (d->d_model > 4096 || d->d_ff % 64 != 0 || d->d_ff > 65536) return GPT2_ERR_UNSUPPORTED;
+  if (need_model) {
+    if (d->n_layer <= 0 || d->vocab <= 0 || d->n_pos <= 0) return GPT2_ERR_ARG;
+  }
+  return GPT2_OK;
+}
+
+int check_block_ptrs(const gpt2_block_weights* w) {
+  if (!w) return GPT2_ERR_ARG;
+  const void* ps[12] = {w->ln1_g, w->ln1_b, w->w_qkv, w->b_qkv, w->w_o,  w->b_o,
+                        w->ln2_g, w->ln2_b, w->w_fc,  w->b_fc,  w->w_proj, w->b_proj};
+  for (const void* p : ps)
+    if (!p || !aligned16(p)) return GPT2_ERR_ARG;
+  return GPT2_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA; }
+
+#define GPT2_TRY(expr)                 \
+  do {                                 \
+    int _s = (expr);                   \
+    if (_s != GPT2_OK) return _s;      \
+  } while (0)
+#define GPT2_CUDA(expr) GPT2_TRY(cuda_status(expr))
+
+// One linear layer on the path of dims.dtype (no argument checks).
+cudaError_t linear(gpt2_dtype dt, const void* x, const void* w, const void* bias, const float* res, void* y,
+                   int64_t M, int N, int K, int64_t ldy, bool w_out_in, int epi, gpt2_dtype y_t, cudaStream_t s) {
+  const double e = static_cast<double>(esize(dt));
+  const double bytes = (static_cast<double>(M) * K + static_cast<double>(K) * N) * e +
+                       (epi != GPT2_EPI_NONE ? N * e : 0.0) +
+                       (epi == GPT2_EPI_BIAS_RESIDUAL ? 4.0 * M * N : 0.0) + static_cast<double>(M) * N * esize(y_t);
+  ProfScope prof(dt == GPT2_BF16 ? "gemm_bf16_tcgen05" : "gemm_f32_simt", 2.0 * M * N * K, bytes, s);
+  if (dt == GPT2_BF16)
+    return launch_gemm_bf16(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w),
+                            static_cast<const __nv_bfloat16*>(bias), res, y, M, N, K, ldy, w_out_in, epi, y_t, s);
+  return launch_gemm_f32(static_cast<const float*>(x), static_cast<const float*>(w), static_cast<const float*>(bias),
+                         res, static_cast<float*>(y), M, N, K, ldy, w_out_in, epi, s);
+}
+
+cudaError_t attention(gpt2_dtype dt, const void* qkv, void* out, int B, int T, int H, cudaStream_t s) {
+  // causal algorithmic work: q.k and p.v over the j <= i pairs only
+  const double pairs = static_cast<double>(B) * H * T * (T + 1.0) / 2.0;
+  const double D = 64.0 * H;
+  ProfScope prof(dt == GPT2_BF16 ? "attn_causal_bf16_mma" : "attn_causal_f32", 4.0 * 64.0 * pairs,
+                 static_cast<double>(B) * T * 4.0 * D * esize(dt), s);
+  if (dt == GPT2_BF16)
+    return launch_attention_bf16(static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out), B, T, H,
+                                 s);
+  return launch_attention_f32(static_cast<const float*>(qkv), static_cast<float*>(out), B, T, H, s);
+}
+
+cudaError_t layernorm(const void* x, const void* g, const void* b, void* y, int64_t rows, int D, float eps,
+                      gpt2_dtype x_t, gpt2_dtype y_t, cudaStream_t s) {
+  ProfScope prof("layernorm", 8.0 * rows * D,
+                 static_cast<double>(rows) * D * (esize(x_t) + esize(y_t)) + 2.0 * D * esize(y_t), s);
+  return launch_layernorm(x, g, b, y, rows, D, eps, x_t, y_t, s);
+}
+
+struct Acts {
+  float* x;
+  float* h;
+  void* a;
+  void* qkv;
+  void* o;
+  void* g;
+};
+
+size_t acts_bytes(const gpt2_dims* d, int64_t M) {
+  const size_t e = esize(d->dtype);
+  const size_t D = d->d_model, F = d->d_ff;
+  return align256(M * D * 4) * 2 + align256(M * D * e) * 2 + align256(M * 3 * D * e) + align256(M * F * e);
+}
+
+Acts carve_acts(void* ws, const gpt2_dims* d, int64_t M) {
+  Carve c(ws);
+  const size_t e = esize(d->dtype);
+  const size_t D = d->d_model, F = d->d_ff;
+  Acts a;
+  a.x = c.take<float>(M * D, 4);
+  a.h = c.take<float>(M * D, 4);
+  a.a = c.take<char>(M * D, e);
+  a.qkv = c.take<char>(M * 3 * D, e);
+  a.o = c.take<char>(M * D, e);
+  a.g = c.take<char>(M * F, e);
+  return a;
+}
+
+// The block body from `a = LN_1(x)` already computed; x -> x_out.
+int block_body(const gpt2_dims* d, const gpt2_block_weights* w, const float* x, float* x_out, int B, int T,
+               const Acts& A, cudaStream_t s) {
+  const gpt2_dtype dt = d->dtype;
+  const int64_t M = static_cast<int64_t>(B) * T;
+  const int D = d->d_model, F = d->d_ff, H = d->n_head;
+  GPT2_CUDA(linear(dt, A.a, w->w_qkv, w->b_qkv, nullptr, A.qkv, M, 3 * D, D, 3 * D, false, GPT2_EPI_BIAS, dt, s));
+  GPT2_CUDA(attention(dt, A.qkv, A.o, B, T, H, s));
+  GPT2_CUDA(linear(dt, A.o, w->w_o, w->b_o, x, A.h, M, D, D, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32, s));
+  GPT2_CUDA(layernorm(A.h, w->ln2_g, w->ln2_b, A.a, M, D, d->eps, GPT2_F32, dt, s));
+  GPT2_CUDA(linear(dt, A.a, w->w_fc, w->b_fc, nullptr, A.g, M, F, D, F, false, GPT2_EPI_BIAS_GELU, dt, s));
+  GPT2_CUDA(linear(dt, A.g, w->w_proj, w->b_proj, A.h, x_out, M, D, F, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32, s));
+  return GPT2_OK;
+}
+
+int check_model(const gpt2_dims* dims, const gpt2_model_weights* w) {
+  GPT2_TRY(check_dims(dims, true));
+  if (!w || !w->blocks) return GPT2_ERR_ARG;
+  const void* ps[4] = {w->wte, w->wpe, w->lnf_g, w->lnf_b};
+  for (const void* p : ps)
+    if (!p || !aligned16(p)) return GPT2_ERR_ARG;
+  for (int l = 0; l < dims->n_layer; ++l) GPT2_TRY(check_block_ptrs(&w->blocks[l]));
+  return GPT2_OK;
+}
+
+size_t decode_ws_bytes(const gpt2_dims* d, int B) {
+  const size_t M = static_cast<size_t>(B);
+  const size_t Vp = (static_cast<size_t>(d->vocab) + 3) & ~static_cast<size_t>(3);
+  return acts_bytes(d, static_cast<int64_t>(M)) + align256(M * Vp * 4) + align256(M * 4);
+}
+
+}  // namespace
+
+extern "C" {
+
+int gpt2_abi_version(void) { return kAbiVersion; }
+
+const char* gpt2_status_string(int status) {
+  switch (status) {
+    case GPT2_OK: return "ok";
+    case GPT2_ERR_ARG: return "invalid argument";
+    case GPT2_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case GPT2_ERR_WORKSPACE: return "workspace too small";
+    case GPT2_ERR_CUDA: return "CUDA error";
+    case GPT2_ERR_TIMEOUT: return "device wait timed out";
+    case GPT2_ERR_RANGE: return "token id or position out of range";
+    default: return "unknown status";
+  }
+}
+
+int gpt2_last_error(int* site) {
+  if (site) *site = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return GPT2_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v)) != cudaSuccess) return GPT2_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return GPT2_ERR_CUDA;
+  }
+  if (site) *site = static_cast<int>(v >> 8);
+  return static_cast<int>(v & 0xFFu);
+}
+
+int gpt2_layernorm(const void* x, const void* gamma, const void* beta, void* y, int64_t rows, int D, float eps,
+                   gpt2_dtype x_t, gpt2_dtype y_t, gpt2_stream_t stream) {
+  if (!valid_dtype(x_t) || !valid_dtype(y_t)) return GPT2_ERR_ARG;
+  if (rows < 0 || D <= 0 || !(eps > 0.f) || !std::isfinite(eps)) return GPT2_ERR_ARG;
+  if (D % 4 != 0 || D > 4096) return GPT2_ERR_UNSUPPORTED;
+  if (rows == 0) return GPT2_OK;
+  if (!x || !gamma || !beta || !y) return GPT2_ERR_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(gamma) || !aligned16(beta)) return GPT2_ERR_ARG;
+  return cuda_status(layernorm(x, gamma, beta, y, rows, D, eps, x_t, y_t, cs(stream)));
+}
+
+int gpt2_linear(const void* x, const void* w, const void* bias, const float* residual, void* y, int64_t M, int N,
+                int K, int64_t ldy, gpt2_weight_layout w_layout, gpt2_epilogue epilogue, gpt2_dtype dtype,
+                gpt2_dtype y_t, gpt2_stream_t stream) {
+  if (!valid_dtype(dtype) || !valid_dtype(y_t)) return GPT2_ERR_ARG;
+  if (w_layout != GPT2_W_IN_OUT && w_layout != GPT2_W_OUT_IN) return GPT2_ERR_ARG;
+  if (epilogue < GPT2_EPI_NONE || epilogue > GPT2_EPI_BIAS_RESIDUAL) return GPT2_ERR_ARG;
+  if (M < 0 || M > INT_MAX || N <= 0 || K <= 0 || ldy < N) return GPT2_ERR_ARG;
+  if (K % 64 != 0) return GPT2_ERR_UNSUPPORTED;
+  if (epilogue == GPT2_EPI_BIAS_RESIDUAL && y_t != GPT2_F32) return GPT2_ERR_UNSUPPORTED;
+  if (dtype == GPT2_F32 && y_t != GPT2_F32) return GPT2_ERR_UNSUPPORTED;
+  if (dtype == GPT2_BF16 && w_layout == GPT2_W_IN_OUT && N % 8 != 0) return GPT2_ERR_UNSUPPORTED;
+  if (M == 0) return GPT2_OK;
+  if (!x || !w || !y || !aligned16(x) || !aligned16(w) || !aligned16(y)) return GPT2_ERR_ARG;
+  if (epilogue != GPT2_EPI_NONE && (!bias || !aligned16(bias))) return GPT2_ERR_ARG;
+  if (epilogue == GPT2_EPI_BIAS_RESIDUAL && (!residual || !aligned16(residual))) return GPT2_ERR_ARG;
+  return cuda_status(linear(dtype, x, w, bias, residual, y, M, N, K, ldy, w_layout == GPT2_W_OUT_IN, epilogue, y_t,
+                            cs(stream)));
+}
+
+int gpt2_attention_causal(const void* qkv, void* out, int B, int T, int n_head, int head_dim, gpt2_dtype dtype,
+                          gpt2_stream_t stream) {
+  if (!valid_dtype(dtype) || B < 0 || T < 0 || n_head <= 0 || head_dim <= 0) return GPT2_ERR_ARG;
+  if (head_dim != 64) return GPT2_ERR_UNSUPPORTED;
+  if (dtype == GPT2_F32 && T > 8192) return GPT2_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * n_head > INT_MAX || T > 65535 * 64) return GPT2_ERR_UNSUPPORTED;
+  if (B == 0 || T == 0) return GPT2_OK;
+  if (!qkv || !out || !aligned16(qkv) || !aligned16(out)) return GPT2_ERR_ARG;
+  return cuda_status(attention(dtype, qkv, out, B, T, n_head, cs(stream)));
+}
+
+size_t gpt2_mlp_workspace_bytes(int64_t M, int F, gpt2_dtype dtype) {
+  if (M < 0 || F <= 0 || !valid_dtype(dtype)) return 0;
+  return align256(static_cast<size_t>(M) * F * esize(dtype));
+}
+
+int gpt2_mlp(const void* x, const void* w_fc, const void* b_fc, const void* w_proj, const void* b_proj,
+             const float* residual, float* out, int64_t M, int D, int F, void* ws, size_t ws_bytes,
+             gpt2_dtype dtype, gpt2_stream_t stream) {
+  if (!valid_dtype(dtype) || M < 0 || M > INT_MAX || D <= 0 || F <= 0) return GPT2_ERR_ARG;
+  if (D % 64 != 0 || F % 64 != 0) return GPT2_ERR_UNSUPPORTED;
+  if (M == 0) return GPT2_OK;
+  const void* ps[6] = {x, w_fc, b_fc, w_proj, b_proj, out};
+  for (const void* p : ps)
+    if (!p || !aligned16(p)) return GPT2_ERR_ARG;
+  if (residual && !aligned16(residual)) return GPT2_ERR_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return GPT2_ERR_ARG;
+  if (ws_bytes < gpt2_mlp_workspace_bytes(M, F, dtype)) return GPT2_ERR_WORKSPACE;
+  cudaStream_t s = cs(stream);
+  GPT2_CUDA(linear(dtype, x, w_fc, b_fc, nullptr, ws, M, F, D, F, false, GPT2_EPI_BIAS_GELU, dtype, s));
+  if (residual)
+    GPT2_CUDA(linear(dtype, ws, w_proj, b_proj, residual, out, M, D, F, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32, s));
+  else
+    GPT2_CUDA(linear(dtype, ws, w_proj, b_proj, nullptr, out, M, D, F, D, false, GPT2_EPI_BIAS, GPT2_F32, s));
+  return GPT2_OK;
+}
+
+size_t gpt2_workspace_bytes(const gpt2_dims* dims, int B, int T) {
+  if (check_dims(dims, false) != GPT2_OK || B < 0 || T < 0) return 0;
+  return acts_bytes(dims, static_cast<int64_t>(B) * T);
+}
+
+int gpt2_block_forward(const gpt2_dims* dims, const gpt2_block_weights* w, const float* x_in, float* x_out, int B,
+                       int T, void* ws, size_t ws_bytes, gpt2_stream_t stream) {
+  GPT2_TRY(check_dims(dims, false));
+  GPT2_TRY(check_block_ptrs(w));
+  if (B < 0 || T < 0 || static_cast<int64_t>(B) * T > INT_MAX) return GPT2_ERR_ARG;
+  if (B == 0 || T == 0) return GPT2_OK;
+  if (!x_in || !x_out || !aligned16(x_in) || !aligned16(x_out)) return GPT2_ERR_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return GPT2_ERR_ARG;
+  if (ws_bytes < gpt2_workspace_bytes(dims, B, T)) return GPT2_ERR_WORKSPACE;
+  const int64_t M = static_cast<int64_t>(B) * T;
+  Acts A = carve_acts(ws, dims, M);
+  cudaStream_t s = cs(stream);
+  GPT2_CUDA(layernorm(x_in, w->ln1_g, w->ln1_b, A.a, M, dims->d_model, dims->eps, GPT2_F32, dims->dtype, s));
+  return block_body(dims, w, x_in, x_out, B, T, A, s);
+}
+
+int gpt2_forward_logits(const gpt2_dims* dims, const gpt2_model_weights* w, const int32_t* tokens, void* logits,
+                        int64_t ld, gpt2_dtype logits_t, int B, int T, void* ws, size_t ws_bytes,
+                        gpt2_stream_t stream) {
+  GPT2_TRY(check_model(dims, w));
+  if (!valid_dtype(logits_t)) return GPT2_ERR_ARG;
+  if (dims->dtype == GPT2_F32 && logits_t != GPT2_F32) return GPT2_ERR_UNSUPPORTED;
+  if (B < 0 || T < 0 || static_cast<int64_t>(B) * T > INT_MAX || ld < dims->vocab) return GPT2_ERR_ARG;
+  if (T > dims->n_pos) return GPT2_ERR_ARG;
+  if (B == 0 || T == 0) return GPT2_OK;
+  if (!tokens || !logits || !aligned16(logits)) return GPT2_ERR_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return GPT2_ERR_ARG;
+  if (ws_bytes < gpt2_workspace_bytes(dims, B, T)) return GPT2_ERR_WORKSPACE;
+  const int64_t M = static_cast<int64_t>(B) * T;
+  const gpt2_dtype dt = dims->dtype;
+  const int D = dims->d_model;
+  Acts A = carve_acts(ws, dims, M);
+  cudaStream_t s = cs(stream);
+  {
+    ProfScope prof("embed_layernorm", 8.0 * M * D, static_cast<double>(M) * (4.0 + D * (2.0 * esize(dt) + 4.0 + esize(dt))),
+                   s);
+    GPT2_CUDA(launch_embed_ln(tokens, w->wte, w->wpe, w->blocks[0].ln1_g, w->blocks[0].ln1_b, A.x, A.a, B, T, D,
+                              dims->vocab, dims->eps, dt, s));
+  }
+  for (int l = 0; l < dims->n_layer; ++l) {
+    const gpt2_block_weights* bw = &w->blocks[l];
+    if (l > 0) GPT2_CUDA(layernorm(A.x, bw->ln1_g, bw->ln1_b, A.a, M, D, dims->eps, GPT2_F32, dt, s));
+    GPT2_TRY(block_body(dims, bw, A.x, A.x, B, T, A, s));
+  }
+  GPT2_CUDA(layernorm(A.x, w->lnf_g, w->lnf_b, A.a, M, D, dims->eps, GPT2_F32, dt, s));
+  GPT2_CUDA(linear(dt, A.a, w->wte, nullptr, nullptr, logits, M, dims->vocab, D, ld, true, GPT2_EPI_NONE, logits_t, s));
+  return GPT2_OK;
+}
+
+size_t gpt2_kv_cache_bytes(const gpt2_dims* dims, int B, int T_max) {
+  if (check_dims(dims, true) != GPT2_OK || B < 0 || T_max < 0) return 0;
+  return static_cast<size_t>(dims->n_layer) * 2 * B * dims->n_head * static_cast<size_t>(T_max) * 64 *
+         esize(dims->dtype);
+}
+
+size_t gpt2_decode_workspace_bytes(const gpt2_dims* dims, int B) {
+  if (check_dims(dims, true) != GPT2_OK || B < 0) return 0;
+  return decode_ws_bytes(dims, B);
+}
+
+int gpt2_decode_step(const gpt2_dims* dims, const gpt2_model_weights* w, void* kv_cache, int B, int T_max,
+                     int32_t* past_len, const int32_t* tokens, int32_t* next_tokens, float* logits_opt, int64_t ld,
+                     void* ws, size_t ws_bytes, gpt2_stream_t stream) {
+  GPT2_TRY(check_model(dims, w));
+  if (dims->dtype != GPT2_BF16) return GPT2_ERR_UNSUPPORTED;
+  if (B < 0 || T_max <= 0) return GPT2_ERR_ARG;
+  if (B == 0) return GPT2_OK;
+  if (!kv_cache || !past_len || !tokens || !next_tokens || !aligned16(kv_cache)) return GPT2_ERR_ARG;
+  if (logits_opt && (ld < dims->vocab || !aligned16(logits_opt))) return GPT2_ERR_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return GPT2_ERR_ARG;
+  if (ws_bytes < decode_ws_bytes(dims, B)) return GPT2_ERR_WORKSPACE;
+  const int D = dims->d_model, F = dims->d_ff, H = dims->n_head, V = dims->vocab;
+  Carve c(ws);
+  Acts A;
+  A.x = c.take<float>(static_cast<size_t>(B) * D, 4);
+  A.h = c.take<float>(static_cast<size_t>(B) * D, 4);
+  A.a = c.take<char>(static_cast<size_t>(B) * D, 2);
+  A.qkv = c.take<char>(static_cast<size_t>(B) * 3 * D, 2);
+  A.o = c.take<char>(static_cast<size_t>(B) * D, 2);
+  A.g = c.take<char>(static_cast<size_t>(B) * F, 2);
+  const int64_t Vp = (static_cast<int64_t>(V) + 3) & ~static_cast<int64_t>(3);
+  float* lg = c.take<float>(static_cast<size_t>(B) * Vp, 4);
+  int* valid = c.take<int>(static_cast<size_t>(B), 4);
+  float* logits = logits_opt ? logits_opt : lg;
+  const int64_t lld = logits_opt ? ld : Vp;
+  cudaStream_t s = cs(stream);
+  using bf = __nv_bfloat16;
+  const size_t layer_elems = static_cast<size_t>(2) * B * H * static_cast<size_t>(T_max) * 64;
+  {
+    ProfScope prof("decode_embed_layernorm", 8.0 * B * D, static_cast<double>(B) * D * 10.0, s);
+    GPT2_CUDA(launch_decode_embed_ln(tokens, past_len, static_cast<const bf*>(w->wte), static_cast<const bf*>(w->wpe),
+                                   static_cast<const bf*>(w->blocks[0].ln1_g),
+                                   static_cast<const bf*>(w->blocks[0].ln1_b), A.x, static_cast<bf*>(A.a), B, D, V,
+                                     dims->n_pos, T_max, dims->eps, valid, s));
+  }
+  for (int l = 0; l < dims->n_layer; ++l) {
+    const gpt2_block_weights* bw = &w->blocks[l];
+    if (l > 0) GPT2_CUDA(layernorm(A.x, bw->ln1_g, bw->ln1_b, A.a, B, D, dims->eps, GPT2_F32, GPT2_BF16, s));
+    GPT2_CUDA(linear(GPT2_BF16, A.a, bw->w_qkv, bw->b_qkv, nullptr, A.qkv, B, 3 * D, D, 3 * D, false, GPT2_EPI_BIAS,
+                     GPT2_BF16, s));
+    bf* kv_layer = static_cast<bf*>(kv_cache) + l * layer_elems;
+    {
+      // the cached lengths live on the device: the bytes of this kernel are
+      // left to the caller, who knows them
+      ProfScope prof("decode_attn", 0.0, 0.0, s);
+      GPT2_CUDA(launch_decode_attention(static_cast<const bf*>(A.qkv), kv_layer, static_cast<bf*>(A.o), past_len,
+                                        valid, B, H, T_max, s));
+    }
+    GPT2_CUDA(linear(GPT2_BF16, A.o, bw->w_o, bw->b_o, A.x, A.h, B, D, D, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32,
+                     s));
+    GPT2_CUDA(layernorm(A.h, bw->ln2_g, bw->ln2_b, A.a, B, D, dims->eps, GPT2_F32, GPT2_BF16, s));
+    GPT2_CUDA(linear(GPT2_BF16, A.a, bw->w_fc, bw->b_fc, nullptr, A.g, B, F, D, F, false, GPT2_EPI_BIAS_GELU,
+                     GPT2_BF16, s));
+    GPT2_CUDA(linear(GPT2_BF16, A.g, bw->w_proj, bw->b_proj, A.h, A.x, B, D, F, D, false, GPT2_EPI_BIAS_RESIDUAL,
+                     GPT2_F32, s));
+  }
+  GPT2_CUDA(layernorm(A.x, w->lnf_g, w->lnf_b, A.a, B, D, dims->eps, GPT2_F32, GPT2_BF16, s));
+  GPT2_CUDA(linear(GPT2_BF16, A.a, w->wte, nullptr, nullptr, logits, B, V, D, lld, true, GPT2_EPI_NONE, GPT2_F32, s));
+  {
+    ProfScope prof("argmax_rows", static_cast<double>(B) * V, static_cast<double>(B) * V * 4.0, s);
+    GPT2_CUDA(launch_argmax_rows(logits, lld, B, V, valid, next_tokens, past_len, s));
+  }
+  return GPT2_OK;
+}
+
+int gpt2_profile_begin(int max_launches) {
+  if (max_launches <= 0 || max_launches > (1 << 20)) return GPT2_ERR_ARG;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  g_prof.on = false;
+  g_prof.release();
+  g_prof.ev.resize(static_cast<size_t>(2) * max_launches);
+  for (auto& e : g_prof.ev) {
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      e = nullptr;
+      g_prof.release();
+      return GPT2_ERR_CUDA;
+    }
+  }
+  g_prof.on = true;
+  return GPT2_OK;
+}
+
+int gpt2_profile_end(void) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  g_prof.on = false;
+  return GPT2_OK;
+}
+
+int gpt2_profile_read(gpt2_profile_entry* out, int max_entries, int* n_entries) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (g_prof.on || max_entries < 0 || (!out && max_entries > 0)) return GPT2_ERR_ARG;
+  const int n = static_cast<int>(g_prof.names.size());
+  if (n_entries) *n_entries = n;
+  for (int i = 0; i < n && i < max_entries; ++i) {
+    std::memset(&out[i], 0, sizeof(out[i]));
+    std::strncpy(out[i].name, g_prof.names[i].c_str(), sizeof(out[i].name) - 1);
+  }
+  for (const ProfRec& r : g_prof.recs) {
+    if (cudaEventSynchronize(g_prof.ev[r.ev0 + 1]) != cudaSuccess) return GPT2_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, g_prof.ev[r.ev0], g_prof.ev[r.ev0 + 1]) != cudaSuccess) return GPT2_ERR_CUDA;
+    if (r.name_id < max_entries) {
+      gpt2_profile_entry& e = out[r.name_id];
+      e.launches += 1;
+      e.ms += ms;
+      e.flops += r.flops;
+      e.bytes += r.bytes;
+    }
+  }
+  return GPT2_OK;
+}
+
+}  // extern "C"

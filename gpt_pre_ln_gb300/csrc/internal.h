@@ -1,0 +1,52 @@
+// Host-side declarations shared by the translation units of libgpt2gb.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gpt2gb.h"
+
+namespace gpt2 {
+
+// Device error word of the current device (see gpt2_last_error).
+unsigned* device_error_word();
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+// Each launcher validates nothing beyond what its kernel needs (the C-ABI
+// layer has checked the arguments) and returns the launch status.
+cudaError_t launch_layernorm(const void* x, const void* gamma, const void* beta, void* y, int64_t rows, int D,
+                             float eps, gpt2_dtype x_t, gpt2_dtype y_t, cudaStream_t stream);
+
+// x[m] = wte[tokens[m]] + wpe[pos0 + m % T] (fp32), y = LN(x) (type dt).
+cudaError_t launch_embed_ln(const int32_t* tokens, const void* wte, const void* wpe, const void* gamma,
+                            const void* beta, float* x, void* y, int B, int T, int D, int V, float eps, gpt2_dtype dt,
+                            cudaStream_t stream);
+
+// bf16 tensor-core GEMM with a fused epilogue (tcgen05 + TMA).
+cudaError_t launch_gemm_bf16(const __nv_bfloat16* x, const __nv_bfloat16* w, const __nv_bfloat16* bias,
+                             const float* residual, void* y, int64_t M, int N, int K, int64_t ldy, bool w_out_in,
+                             int epilogue, gpt2_dtype y_t, cudaStream_t stream);
+
+// fp32 CUDA-core GEMM with the same epilogues.
+cudaError_t launch_gemm_f32(const float* x, const float* w, const float* bias, const float* residual, float* y,
+                            int64_t M, int N, int K, int64_t ldy, bool w_out_in, int epilogue, cudaStream_t stream);
+
+cudaError_t launch_attention_bf16(const __nv_bfloat16* qkv, __nv_bfloat16* out, int B, int T, int n_head,
+                                  cudaStream_t stream);
+cudaError_t launch_attention_f32(const float* qkv, float* out, int B, int T, int n_head, cudaStream_t stream);
+
+// Decode-step kernels (bf16 path).
+cudaError_t launch_decode_embed_ln(const int32_t* tokens, const int32_t* past_len, const __nv_bfloat16* wte,
+                                   const __nv_bfloat16* wpe, const __nv_bfloat16* gamma, const __nv_bfloat16* beta,
+                                   float* x, __nv_bfloat16* y, int B, int D, int V, int n_pos, int T_max, float eps,
+                                   int* valid, cudaStream_t stream);
+cudaError_t launch_decode_attention(const __nv_bfloat16* qkv, __nv_bfloat16* kv_layer, __nv_bfloat16* out,
+                                    const int32_t* past_len, const int* valid, int B, int n_head, int T_max,
+                                    cudaStream_t stream);
+cudaError_t launch_argmax_rows(const float* logits, int64_t ld, int B, int V, const int* valid, int32_t* next_tokens,
+                               int32_t* past_len, cudaStream_t stream);
+
+}  // namespace gpt2

@@ -231,3 +231,8 @@ def workload_inputs(name: str, T_override: int | None = None, B_override: int | 
         out["cache"] = draw_kv_cache(d, w.dims, B, T_max, w.cache_len)
         out["past_len"] = np.full((B,), w.cache_len, dtype=np.int32)
     return out
+
+
+def replace_dims(d: Dims, **kw) -> Dims:
+    """A copy of ``d`` with some fields changed (e.g. fewer layers)."""
+    return dataclasses.replace(d, **kw)
