@@ -63,7 +63,7 @@ def _dist():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -77,7 +77,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
 
@@ -356,7 +356,7 @@ def run_ours(args):
                      "frac": achieved / peaks["bf16_tflops_sustained"],
                      "frac_of_burst": achieved / peaks["bf16_tflops"], "peak_source": peaks["source"],
                      "traffic": _traffic_from_profile()},
-        "end_to_end_tflops": total_flops_step / (ms / args.steps / 1e3) / 1e12 / world * world,
+        "end_to_end_tflops": total_flops_step / (ms / args.steps / 1e3) / 1e12,
         "end_to_end_frac": total_flops_step / (ms / args.steps / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
         "kernels": kernels,
         "clocks": clk,
@@ -379,7 +379,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-decode", action="store_true")

@@ -238,12 +238,17 @@ def test_decode_steps_match_oracle():
         assert np.array_equal(g_next, np.argmax(got, -1))  # the kernel's argmax of its own logits
         otok = g_next  # both sides continue from the GPU's choice
         tok.copy_(nxt)
-    # the cache slots written by the GPU hold the new k, v (bf16) of the oracle
+    # the cache slots written by the GPU hold the new k, v of the oracle (up
+    # to the bf16 rounding of the c_attn input and output: ~3e-3 relative;
+    # a value in the wrong slot or head would be off by ~100%)
     kv_np = to_np(kv)
     for b in range(B):
         for s in range(past[b], past[b] + 4):
-            np.testing.assert_allclose(kv_np[:, :, b, :, s], ocache[:, :, b, :, s], rtol=2 ** -7, atol=2e-3)
+            for l in range(dims.n_layer):
+                for kvi in range(2):
+                    assert rel_l2(kv_np[l, kvi, b, :, s], ocache[l, kvi, b, :, s]) < 2e-2, (b, s, l, kvi)
         assert np.all(kv_np[:, :, b, :, past[b] + 4:] == 0)
+        np.testing.assert_array_equal(kv_np[:, :, b, :, :past[b]], ocache[:, :, b, :, :past[b]])
     del keep
 
 
