@@ -22,7 +22,8 @@ __all__ = [
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-library_path = os.path.join(_PKG, "libgpt2gb.so")
+# the in-tree build, or another build of the same sources named by GPT2GB_LIBRARY
+library_path = os.environ.get("GPT2GB_LIBRARY") or os.path.join(_PKG, "libgpt2gb.so")
 
 F32, BF16 = 0, 1
 EPI_NONE, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESIDUAL = 0, 1, 2, 3

@@ -327,6 +327,9 @@ int gpt2_linear(const void* x, const void* w, const void* bias, const float* res
   if (epilogue == GPT2_EPI_BIAS_RESIDUAL && y_t != GPT2_F32) return GPT2_ERR_UNSUPPORTED;
   if (dtype == GPT2_F32 && y_t != GPT2_F32) return GPT2_ERR_UNSUPPORTED;
   if (dtype == GPT2_BF16 && w_layout == GPT2_W_IN_OUT && N % 8 != 0) return GPT2_ERR_UNSUPPORTED;
+  // the tensor-core path stores through TMA: 16-byte aligned rows
+  if (dtype == GPT2_BF16 && (ldy * static_cast<int64_t>(esize(y_t))) % 16 != 0) return GPT2_ERR_UNSUPPORTED;
+  if (epilogue == GPT2_EPI_BIAS_RESIDUAL && N % 4 != 0) return GPT2_ERR_UNSUPPORTED;
   if (M == 0) return GPT2_OK;
   if (!x || !w || !y || !aligned16(x) || !aligned16(w) || !aligned16(y)) return GPT2_ERR_ARG;
   if (epilogue != GPT2_EPI_NONE && (!bias || !aligned16(bias))) return GPT2_ERR_ARG;
@@ -401,6 +404,7 @@ int gpt2_forward_logits(const gpt2_dims* dims, const gpt2_model_weights* w, cons
   if (dims->dtype == GPT2_F32 && logits_t != GPT2_F32) return GPT2_ERR_UNSUPPORTED;
   if (B < 0 || T < 0 || static_cast<int64_t>(B) * T > INT_MAX || ld < dims->vocab) return GPT2_ERR_ARG;
   if (T > dims->n_pos) return GPT2_ERR_ARG;
+  if (dims->dtype == GPT2_BF16 && (ld * static_cast<int64_t>(esize(logits_t))) % 16 != 0) return GPT2_ERR_UNSUPPORTED;
   if (B == 0 || T == 0) return GPT2_OK;
   if (!tokens || !logits || !aligned16(logits)) return GPT2_ERR_ARG;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return GPT2_ERR_ARG;
@@ -446,6 +450,7 @@ int gpt2_decode_step(const gpt2_dims* dims, const gpt2_model_weights* w, void* k
   if (B == 0) return GPT2_OK;
   if (!kv_cache || !past_len || !tokens || !next_tokens || !aligned16(kv_cache)) return GPT2_ERR_ARG;
   if (logits_opt && (ld < dims->vocab || !aligned16(logits_opt))) return GPT2_ERR_ARG;
+  if (logits_opt && ld % 4 != 0) return GPT2_ERR_UNSUPPORTED;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return GPT2_ERR_ARG;
   if (ws_bytes < decode_ws_bytes(dims, B)) return GPT2_ERR_WORKSPACE;
   const int D = dims->d_model, F = dims->d_ff, H = dims->n_head, V = dims->vocab;

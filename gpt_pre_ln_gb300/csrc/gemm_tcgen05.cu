@@ -6,14 +6,28 @@
 //                                          or  [N, K] (wte as the lm_head)
 //   epilogues: none | + bias | gelu_new(+ bias) | + bias + residual (fp32)
 //
-// Design (one persistent CTA per SM, 6 warps):
-//   warp 0      TMA producer: A tile 128 x 64 and B tile BN x 64 per stage,
-//               128-byte swizzled, into a STAGES-deep shared-memory ring.
-//   warp 1      allocates tensor memory; one thread issues tcgen05.mma
-//               (M=128, N=BN, K=16) into one of two fp32 accumulators in
-//               tensor memory and commits stage / accumulator barriers.
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (thread = row),
-//               bias / gelu_new / residual in fp32, direct 16-byte stores.
+// Two persistent kernels share one design (10 warps per CTA):
+//   warp 0      TMA producer: 128-byte-swizzled A and B tiles of 64 K per
+//               stage into a STAGES-deep shared-memory ring.
+//   warp 1      allocates tensor memory; one thread issues tcgen05.mma into
+//               one of two fp32 accumulators in tensor memory and commits
+//               the stage / accumulator barriers.
+//   warps 2-9   epilogue in two halves of four warps (one thread per
+//               accumulator row in each half); half h owns the column chunks
+//               h, h+2, ... (128 bytes of output per row each): tcgen05.ld,
+//               bias / gelu_new / residual in fp32, then each warp writes its
+//               32 rows into a private swizzled staging area and reads them
+//               back transposed, so that every global store instruction
+//               covers four full 128-byte lines.  The fp32 residual is read
+//               the same coalesced way.  No barrier spans more than a warp.
+// gemm_1sm: one CTA per tile of 128 x BN (BN = 128, 192 or 256), MMA
+//   M = 128, N = BN.
+// gemm_2sm: a cluster of two CTAs per tile of 256 x 256; each CTA stages its
+//   128 rows of A and its 128 columns of B, the even CTA issues the pair MMA
+//   (tcgen05.mma.cta_group::2, M = 256, N = 256) and every commit arrives on
+//   the barriers of both CTAs.  Per MMA cycle each SM takes in a third less
+//   operand data than with 128 x 256 tiles, which is what limits these
+//   K = 768 GEMMs (operand delivery, not the tensor core, sets their pace).
 // The two accumulators let the epilogue of tile i overlap the MMAs of tile
 // i+1.  A is always K-major; W [K, N] is consumed MN-major straight from
 // its Conv1D layout (no transpose), wte [N, K] K-major.
@@ -21,8 +35,11 @@
 // Every mbarrier wait is bounded (common.cuh); on a timeout the thread
 // records GPT2_ERR_TIMEOUT, stops issuing work, waits (bounded) for the
 // copies and MMAs it already issued, and the CTA frees its tensor memory.
+// Epilogue lanes combine their wait results with a warp vote, so a warp
+// always takes the same branch.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -33,113 +50,267 @@ namespace gpt2 {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kBK = 64;  // one 128-byte swizzle atom of bf16 along K
-constexpr int kThreads = 192;
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kBK = 64;                 // one 128-byte swizzle atom of bf16 along K
+constexpr int kEpiWarps = 8;            // two per tensor-memory lane quadrant
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kWarpStageBytes = 4096;   // 32 rows x 128 bytes per epilogue warp
+constexpr int kSmemLimit = 232448;      // 227 KB opt-in maximum per block
 
 enum Epi : int { EPI_NONE = 0, EPI_BIAS = 1, EPI_GELU = 2, EPI_RES = 3 };
 
-template <int BN>
+// BN: output columns per CTA tile; B_COLS: columns of B staged per CTA
+// (BN for one CTA, BN / 2 for a pair).
+template <int BN, int B_COLS>
 struct GemmCfg {
   static constexpr int A_BYTES = kBM * kBK * 2;
-  static constexpr int B_BYTES = BN * kBK * 2;
+  static constexpr int B_BYTES = B_COLS * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (kSmemBudget / STAGE_BYTES) > 8 ? 8 : (kSmemBudget / STAGE_BYTES);
-  static constexpr int TMEM_COLS = (2 * BN) < 32 ? 32 : 2 * BN;  // BN in {64,128,256}: power of two
-  static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int FIXED = 1024 + kEpiWarps * kWarpStageBytes + BAR_BYTES;
+  static constexpr int STAGES_FIT = (kSmemLimit - FIXED) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
+  static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;  // power of two >= 2 * BN
+  static constexpr int SMEM_BYTES = FIXED + STAGES * STAGE_BYTES;
+  static_assert(STAGES >= 3, "pipeline too shallow");
+  static_assert(SMEM_BYTES <= kSmemLimit, "shared memory");
+  static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+  static_assert(BN % 64 == 0 && BN <= 256 && B_COLS % 64 == 0, "tile width");
+};
+
+// Byte offset of 16-byte chunk j of row r in a 128-byte-swizzled staging
+// area (8-row groups, chunk index XOR row).
+__device__ __forceinline__ uint32_t swz(int r, int j) { return static_cast<uint32_t>(r * 128 + ((j ^ (r & 7)) << 4)); }
+
+template <typename OutT>
+struct OutTraits {
+  static constexpr int CW = 128 / sizeof(OutT);  // output columns per chunk
+  static constexpr int LD = CW / 32;            // tcgen05.ld x32 per chunk
 };
 
 template <int EPI, typename OutT>
-__device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], int row, int col0, int M, int N,
-                                               const __nv_bfloat16* __restrict__ bias, const float* residual,
-                                               OutT* out, long long ldo, bool vec_ok) {
-  if (row >= M || col0 >= N) return;
-  float v[32];
+__device__ __forceinline__ void apply_bias_act(float (&v)[OutTraits<OutT>::CW], const __nv_bfloat16* __restrict__ bias,
+                                               int col0, int N) {
+  constexpr int CW = OutTraits<OutT>::CW;
+  if (EPI == EPI_NONE) return;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
-  constexpr bool kBf16Out = sizeof(OutT) == 2;
-  if (vec_ok && col0 + 32 <= N) {
-    if (EPI != EPI_NONE) {
-      const uint4* bp = reinterpret_cast<const uint4*>(bias + col0);
+  for (int q = 0; q < CW / 8; ++q) {
+    const int c = col0 + q * 8;
+    float b[8];
+    if (c + 8 <= N) {
+      uint4 u = __ldg(reinterpret_cast<const uint4*>(bias + c));
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 u = __ldg(bp + q);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float2 f = __bfloat1622float2(h[e]);
-          v[q * 8 + 2 * e] += f.x;
-          v[q * 8 + 2 * e + 1] += f.y;
-        }
-      }
-    }
-    if (EPI == EPI_GELU) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = kBf16Out ? gelu_new_fast(v[i]) : gelu_new_accurate(v[i]);
-    }
-    if (EPI == EPI_RES) {
-      const float4* rp = reinterpret_cast<const float4*>(residual + static_cast<long long>(row) * N + col0);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float4 r = rp[q];
-        v[4 * q] += r.x;
-        v[4 * q + 1] += r.y;
-        v[4 * q + 2] += r.z;
-        v[4 * q + 3] += r.w;
-      }
-    }
-    OutT* op = out + static_cast<long long>(row) * ldo + col0;
-    if constexpr (kBf16Out) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 u;
-        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(v[q * 8 + 2 * e], v[q * 8 + 2 * e + 1]);
-        reinterpret_cast<uint4*>(op)[q] = u;
+      for (int e = 0; e < 4; ++e) {
+        float2 f = __bfloat1622float2(h[e]);
+        b[2 * e] = f.x;
+        b[2 * e + 1] = f.y;
       }
     } else {
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        reinterpret_cast<float4*>(op)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      for (int e = 0; e < 8; ++e) b[e] = (c + e < N) ? __bfloat162float(bias[c + e]) : 0.f;
     }
-  } else {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int col = col0 + i;
-      if (col < N) {
-        float t = v[i];
-        if (EPI != EPI_NONE) t += __bfloat162float(bias[col]);
-        if (EPI == EPI_GELU) t = kBf16Out ? gelu_new_fast(t) : gelu_new_accurate(t);
-        if (EPI == EPI_RES) t += residual[static_cast<long long>(row) * N + col];
-        out[static_cast<long long>(row) * ldo + col] = from_f32<OutT>(t);
+    for (int e = 0; e < 8; ++e) v[q * 8 + e] += b[e];
+  }
+  // bf16 outputs: one hardware tanh per element (absolute error below 2^-11,
+  // under the bf16 rounding that follows); fp32 outputs: tanhf
+  if (EPI == EPI_GELU) {
+#pragma unroll
+    for (int i = 0; i < CW; ++i) v[i] = (sizeof(OutT) == 2) ? gelu_new_fast(v[i]) : gelu_new_accurate(v[i]);
+  }
+}
+
+template <typename OutT>
+struct EpiArgs {
+  const __nv_bfloat16* bias;
+  const float* residual;
+  OutT* out;
+  long long ldo;
+  int M, N;
+  unsigned* err;
+};
+
+// Epilogue role (warps 2-9).  Tiles tile_begin, tile_begin + tile_stride, ...
+// < num_tiles; tile t covers rows (t % m_units) * unit_rows + row_off
+// .. + 127 and columns (t / m_units) * BN .. + BN - 1.  After reading its last
+// accumulator columns of a tile, every thread arrives once on the tile's
+// accumulator-empty barrier: locally, or at a cluster address when
+// CLUSTER_ARRIVE (the barrier of the pair's even CTA).
+template <int BN, int EPI, typename OutT, bool CLUSTER_ARRIVE>
+__device__ __forceinline__ void epilogue_role(const EpiArgs<OutT>& a, int warp, int lane, uint32_t stage_base,
+                                              uint32_t tmem_base, uint32_t tfull0, uint32_t tfull1, uint32_t tempty0,
+                                              uint32_t tempty1, int tile_begin, int tile_stride, int num_tiles,
+                                              int m_units, int unit_rows, int row_off) {
+  using OT = OutTraits<OutT>;
+  constexpr int CW = OT::CW;
+  const int quad = warp & 3;  // tensor-memory lanes this warp may access
+  const int half = (warp - 2) >> 2;
+  const uint32_t stage_w = stage_base + (warp - 2) * kWarpStageBytes;
+  const int M = a.M, N = a.N;
+  int t_local = 0;
+  for (int tile = tile_begin; tile < num_tiles; tile += tile_stride, ++t_local) {
+    const int acc = t_local & 1;
+    const uint32_t acc_par = (t_local >> 1) & 1;
+    const uint32_t tempty = acc ? tempty1 : tempty0;
+    const bool got = mbar_wait(acc ? tfull1 : tfull0, acc_par);
+    if (!__all_sync(0xffffffffu, got)) {
+      if (lane == 0) record_error(a.err, kErrTimeout, kSiteGemmEpilogue);
+      return;
+    }
+    tc_fence_after();
+    const int m0 = (tile % m_units) * unit_rows + row_off;
+    const int n0 = (tile / m_units) * BN;
+    const int row0 = m0 + quad * 32;  // first row of this warp
+    const int valid_cols = N - n0 < BN ? N - n0 : BN;
+    const int nch = (valid_cols + CW - 1) / CW;
+    // the last chunk of this half in the tile, after which its accumulator
+    // columns are no longer read (-1: none)
+    const int last_c = (nch - 1 - half) >= 0 ? nch - 1 - ((nch - 1 - half) & 1) : -1;
+    const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+    auto release = [&]() {
+      tc_fence_before();
+      if (CLUSTER_ARRIVE)
+        mbar_arrive_cluster(tempty);
+      else
+        mbar_arrive(tempty);
+    };
+    if (last_c < 0) release();
+#pragma unroll 1
+    for (int c = half; c < nch; c += 2) {
+      const int col0 = n0 + c * CW;
+      // residual chunk (fp32, 32 columns): coalesced loads, 4 rows of 128 B
+      // per instruction, issued before the tensor-memory reads
+      float4 res[8];
+      if (EPI == EPI_RES) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = i * 4 + (lane >> 3);
+          const int cc = col0 + (lane & 7) * 4;
+          res[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (row0 + rr < M && cc < N)
+            res[i] = *reinterpret_cast<const float4*>(a.residual + static_cast<long long>(row0 + rr) * N + cc);
+        }
       }
+      float v[CW];
+      {
+        uint32_t raw[32];
+#pragma unroll
+        for (int l = 0; l < OT::LD; ++l) {
+          tmem_ld_32x32b_x32(t_addr + c * CW + l * 32, raw);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[l * 32 + i] = __uint_as_float(raw[i]);
+        }
+      }
+      if (c == last_c) release();  // this half has read its last columns
+      apply_bias_act<EPI, OutT>(v, a.bias, col0, N);
+      if (EPI == EPI_RES) {
+        // transpose the residual through the staging area: row = lane
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(stage_w + swz(i * 4 + (lane >> 3), lane & 7)),
+                       "f"(res[i].x), "f"(res[i].y), "f"(res[i].z), "f"(res[i].w)
+                       : "memory");
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float4 q;
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(q.x), "=f"(q.y), "=f"(q.z), "=f"(q.w)
+                       : "r"(stage_w + swz(lane, j)));
+          v[4 * j] += q.x;
+          v[4 * j + 1] += q.y;
+          v[4 * j + 2] += q.z;
+          v[4 * j + 3] += q.w;
+        }
+        __syncwarp();
+      }
+      // this lane's row (128 bytes) into the staging area
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t w0, w1, w2, w3;
+        if constexpr (sizeof(OutT) == 2) {
+          __nv_bfloat162 p0 = __floats2bfloat162_rn(v[8 * j], v[8 * j + 1]);
+          __nv_bfloat162 p1 = __floats2bfloat162_rn(v[8 * j + 2], v[8 * j + 3]);
+          __nv_bfloat162 p2 = __floats2bfloat162_rn(v[8 * j + 4], v[8 * j + 5]);
+          __nv_bfloat162 p3 = __floats2bfloat162_rn(v[8 * j + 6], v[8 * j + 7]);
+          w0 = *reinterpret_cast<uint32_t*>(&p0);
+          w1 = *reinterpret_cast<uint32_t*>(&p1);
+          w2 = *reinterpret_cast<uint32_t*>(&p2);
+          w3 = *reinterpret_cast<uint32_t*>(&p3);
+        } else {
+          w0 = __float_as_uint(v[4 * j]);
+          w1 = __float_as_uint(v[4 * j + 1]);
+          w2 = __float_as_uint(v[4 * j + 2]);
+          w3 = __float_as_uint(v[4 * j + 3]);
+        }
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage_w + swz(lane, j)), "r"(w0), "r"(w1),
+                     "r"(w2), "r"(w3)
+                     : "memory");
+      }
+      __syncwarp();
+      // and out to global memory, 4 rows x 128 B per instruction; a 16-byte
+      // piece is stored if it starts before column N (the padding up to the
+      // next 16-byte boundary receives the zeros computed there)
+      constexpr int kPer16 = 16 / static_cast<int>(sizeof(OutT));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = i * 4 + (lane >> 3);
+        const int cc = col0 + (lane & 7) * kPer16;
+        uint32_t w0, w1, w2, w3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                     : "r"(stage_w + swz(rr, lane & 7)));
+        if (row0 + rr < M && cc < N) {
+          uint4* dst = reinterpret_cast<uint4*>(a.out + static_cast<long long>(row0 + rr) * a.ldo + cc);
+          *dst = make_uint4(w0, w1, w2, w3);
+        }
+      }
+      __syncwarp();
     }
   }
 }
 
+// Producer drain: wait for the copies still in flight (the last STAGES
+// issued) on the local full barriers.
+template <int STAGES, typename FullBar>
+__device__ __forceinline__ void drain_loads(long long issued, FullBar full_bar, unsigned* err) {
+  const long long first = issued > STAGES ? issued - STAGES : 0;
+  for (long long i = first; i < issued; ++i) {
+    const int s = static_cast<int>(i % STAGES);
+    const uint32_t par = static_cast<uint32_t>((i / STAGES) & 1);
+    if (!mbar_wait(full_bar(s), par)) {
+      record_error(err, kErrTimeout, kSiteGemmDrain);
+      break;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ 1 SM
 template <int BN, bool B_MN, int EPI, typename OutT>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_bf16_tcgen05(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const __nv_bfloat16* __restrict__ bias, const float* residual, OutT* out, int M, int N, int K,
-                      long long ldo, int vec_ok, unsigned* err) {
-  using Cfg = GemmCfg<BN>;
+    gemm_1sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+             const EpiArgs<OutT> ea, int K) {
+  using Cfg = GemmCfg<BN, BN>;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * Cfg::B_BYTES);
+  uint8_t* sOut = sB + STAGES * Cfg::B_BYTES;  // per-warp staging areas, 1024-aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + kEpiWarps * kWarpStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + STAGES + s); };
   auto tfull_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + 2 + a); };
   const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 4);
+  unsigned* err = ea.err;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int M = ea.M, N = ea.N;
   const int m_tiles = (M + kBM - 1) / kBM;
   const int n_tiles = (N + BN - 1) / BN;
   const int num_tiles = m_tiles * n_tiles;
@@ -154,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 128);
+      mbar_init(tempty_bar(a), kEpiThreads);  // every epilogue thread, once per tile
     }
     mbar_init(drain_bar, 1);
     fence_barrier_init();
@@ -202,16 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // wait for the copies still in flight (the last STAGES issued)
-      long long first = issued > STAGES ? issued - STAGES : 0;
-      for (long long i = first; i < issued; ++i) {
-        const int s = static_cast<int>(i % STAGES);
-        const uint32_t par = static_cast<uint32_t>((i / STAGES) & 1);
-        if (!mbar_wait(full_bar(s), par)) {
-          record_error(err, kErrTimeout, kSiteGemmDrain);
-          break;
-        }
-      }
+      drain_loads<STAGES>(issued, full_bar, err);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -271,32 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------ epilogue (warps 2..5)
-    const int quad = warp & 3;  // tensor-memory lanes this warp may access
-    const int row_in_tile = quad * 32 + lane;
-    int t_local = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t_local) {
-      const int acc = t_local & 1;
-      const uint32_t acc_par = (t_local >> 1) & 1;
-      if (!mbar_wait(tfull_bar(acc), acc_par)) {
-        record_error(err, kErrTimeout, kSiteGemmEpilogue);
-        break;
-      }
-      tc_fence_after();
-      const int m0 = (tile % m_tiles) * kBM;
-      const int n0 = (tile / m_tiles) * BN;
-      const int row = m0 + row_in_tile;
-      const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_addr + c * 32, r);
-        tmem_ld_wait();
-        epilogue_chunk<EPI, OutT>(r, row, n0 + c * 32, M, N, bias, residual, out, ldo, vec_ok != 0);
-      }
-      tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
-    }
+    epilogue_role<BN, EPI, OutT, false>(ea, warp, lane, smem_u32(sOut), tmem_base, tfull_bar(0), tfull_bar(1),
+                                         tempty_bar(0), tempty_bar(1), blockIdx.x, gridDim.x, num_tiles, m_tiles, kBM,
+                                         0);
   }
 
   tc_fence_before();
@@ -304,6 +443,170 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------ CTA pair
+constexpr int kPairBN = 256;
+
+template <bool B_MN, int EPI, typename OutT>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+             const EpiArgs<OutT> ea, int K) {
+  using Cfg = GemmCfg<kPairBN, kPairBN / 2>;
+  constexpr int STAGES = Cfg::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
+  uint8_t* sOut = sB + STAGES * Cfg::B_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + kEpiWarps * kWarpStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + STAGES + s); };
+  auto tfull_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 4);
+  unsigned* err = ea.err;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank() & 1u;  // 0: the CTA that issues the MMAs
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
+  const int M = ea.M, N = ea.N;
+  const int m_units = (M + 2 * kBM - 1) / (2 * kBM);
+  const int n_tiles = (N + kPairBN - 1) / kPairBN;
+  const int num_tiles = m_units * n_tiles;
+  const int k_blocks = K / kBK;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);   // the even CTA's expect_tx; both CTAs' bytes
+      mbar_init(empty_bar(s), 1);  // the pair MMA commit
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 2 * kEpiThreads);  // both CTAs' epilogue threads
+    }
+    mbar_init(drain_bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised before either uses them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
+        const int m0 = (tile % m_units) * (2 * kBM) + static_cast<int>(rank) * kBM;
+        const int nb = (tile / m_units) * kPairBN + static_cast<int>(rank) * (kPairBN / 2);
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1)) {
+            record_error(err, kErrTimeout, kSiteGemmProducer);
+            ok = false;
+            break;
+          }
+          const uint32_t fb = mapa_shared(full_bar(stage), 0);  // the even CTA's barrier
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::STAGE_BYTES);
+          tma_load_2d_pair(smem_u32(sA + stage * Cfg::A_BYTES), &tmA, fb, kb * kBK, m0);
+          const uint32_t b_dst = smem_u32(sB + stage * Cfg::B_BYTES);
+          if constexpr (B_MN) {
+#pragma unroll
+            for (int j = 0; j < kPairBN / 128; ++j)
+              tma_load_2d_pair(b_dst + j * (kBK * 128), &tmB, fb, nb + j * 64, kb * kBK);
+          } else {
+            tma_load_2d_pair(b_dst, &tmB, fb, kb * kBK, nb);
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // the even CTA's full barriers count both CTAs' bytes
+      if (rank == 0) drain_loads<STAGES>(issued, full_bar, err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ------------------------------------------------ pair MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, kPairBN, false, B_MN);
+      constexpr uint16_t kBoth = 0x3;
+      int stage = 0;
+      uint32_t phase = 0;
+      int t_local = 0;
+      bool ok = true;
+      bool any = false;
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs, ++t_local) {
+        const int acc = t_local & 1;
+        const uint32_t acc_par = (t_local >> 1) & 1;
+        if (!mbar_wait(tempty_bar(acc), acc_par ^ 1)) {
+          record_error(err, kErrTimeout, kSiteGemmMma);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kPairBN;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase)) {
+            record_error(err, kErrTimeout, kSiteGemmMma);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + stage * Cfg::A_BYTES);
+          const uint32_t b_base = smem_u32(sB + stage * Cfg::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t adesc = sdesc_sw128(a_base + k * 32, 16, 1024);
+            uint64_t bdesc;
+            if constexpr (B_MN) {
+              bdesc = sdesc_sw128(b_base + k * 2048, kBK * 128, 1024);
+            } else {
+              bdesc = sdesc_sw128(b_base + k * 32, 16, 1024);
+            }
+            umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+            any = true;
+          }
+          umma_commit_pair_multicast(empty_bar(stage), kBoth);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_multicast(tfull_bar(acc), kBoth);
+      }
+      if (any) {
+        umma_commit_pair(drain_bar);
+        if (!mbar_wait(drain_bar, 0)) record_error(err, kErrTimeout, kSiteGemmDrain);
+      }
+    }
+  } else {
+    epilogue_role<kPairBN, EPI, OutT, true>(ea, warp, lane, smem_u32(sOut), tmem_base, tfull_bar(0), tfull_bar(1),
+                                            mapa_shared(tempty_bar(0), 0), mapa_shared(tempty_bar(1), 0), pair,
+                                            num_pairs, num_tiles, m_units, 2 * kBM, static_cast<int>(rank) * kBM);
+  }
+
+  tc_fence_before();
+  // neither CTA leaves while the pair's MMAs may still read its shared memory
+  // or write its tensor memory
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
   }
 }
 
@@ -326,7 +629,8 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major [outer, inner] bf16 matrix, box [box_outer, 64], 128-byte swizzle.
+// Row-major bf16 [outer, inner] matrix; boxes of [box_outer, 64] elements,
+// 128-byte swizzle.
 bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -340,49 +644,140 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool B_MN, int EPI, typename OutT>
-cudaError_t run(const __nv_bfloat16* x, const __nv_bfloat16* w, const __nv_bfloat16* bias, const float* residual,
-                OutT* y, int M, int N, int K, long long ldy, cudaStream_t stream) {
-  using Cfg = GemmCfg<BN>;
-  auto kern = gemm_bf16_tcgen05<BN, B_MN, EPI, OutT>;
-  static int configured[64] = {0};
+template <typename Kern>
+cudaError_t set_smem_once(Kern kern, int bytes, int (&configured)[64]) {
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
+  return cudaSuccess;
+}
+
+template <int BN, bool B_MN, int EPI, typename OutT>
+cudaError_t run_1sm(const __nv_bfloat16* x, const __nv_bfloat16* w, const EpiArgs<OutT>& ea, int K,
+                    cudaStream_t stream) {
+  using Cfg = GemmCfg<BN, BN>;
+  auto kern = gemm_1sm<BN, B_MN, EPI, OutT>;
+  static int configured[64] = {0};
+  cudaError_t e = set_smem_once(kern, Cfg::SMEM_BYTES, configured);
+  if (e != cudaSuccess) return e;
+  const int M = ea.M, N = ea.N;
   CUtensorMap ta, tb;
-  if (!make_map(&ta, x, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kBM)) return cudaErrorInvalidValue;
-  bool okb = B_MN ? make_map(&tb, w, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kBK)
-                  : make_map(&tb, w, static_cast<uint64_t>(K), static_cast<uint64_t>(N), BN);
-  if (!okb) return cudaErrorInvalidValue;
+  if (!make_map(&ta, x, K, M, kBM)) return cudaErrorInvalidValue;
+  if (!(B_MN ? make_map(&tb, w, N, K, kBK) : make_map(&tb, w, K, N, BN))) return cudaErrorInvalidValue;
   const int tiles = ((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  const int vec_ok = ((ldy * static_cast<long long>(sizeof(OutT))) % 16 == 0) && (EPI != EPI_RES || N % 4 == 0);
-  kern<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, bias, residual, y, M, N, K, ldy, vec_ok,
-                                                    device_error_word());
+  kern<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, ea, K);
   return cudaGetLastError();
 }
 
-template <int BN, bool B_MN>
-cudaError_t dispatch_epi(const __nv_bfloat16* x, const __nv_bfloat16* w, const __nv_bfloat16* bias,
-                         const float* residual, void* y, int M, int N, int K, long long ldy, int epi,
-                         gpt2_dtype y_t, cudaStream_t s) {
-  using bf = __nv_bfloat16;
-  if (epi == EPI_RES) return run<BN, B_MN, EPI_RES, float>(x, w, bias, residual, static_cast<float*>(y), M, N, K, ldy, s);
-  if (y_t == GPT2_BF16) {
-    switch (epi) {
-      case EPI_NONE: return run<BN, B_MN, EPI_NONE, bf>(x, w, bias, residual, static_cast<bf*>(y), M, N, K, ldy, s);
-      case EPI_BIAS: return run<BN, B_MN, EPI_BIAS, bf>(x, w, bias, residual, static_cast<bf*>(y), M, N, K, ldy, s);
-      default: return run<BN, B_MN, EPI_GELU, bf>(x, w, bias, residual, static_cast<bf*>(y), M, N, K, ldy, s);
+template <bool B_MN, int EPI, typename OutT>
+cudaError_t run_2sm(const __nv_bfloat16* x, const __nv_bfloat16* w, const EpiArgs<OutT>& ea, int K,
+                    cudaStream_t stream) {
+  using Cfg = GemmCfg<kPairBN, kPairBN / 2>;
+  auto kern = gemm_2sm<B_MN, EPI, OutT>;
+  static int configured[64] = {0};
+  cudaError_t e = set_smem_once(kern, Cfg::SMEM_BYTES, configured);
+  if (e != cudaSuccess) return e;
+  const int M = ea.M, N = ea.N;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, x, K, M, kBM)) return cudaErrorInvalidValue;
+  if (!(B_MN ? make_map(&tb, w, N, K, kBK) : make_map(&tb, w, K, N, kPairBN / 2))) return cudaErrorInvalidValue;
+  // pairs that can be resident at once (a pair needs two SMs of one GPC)
+  static int max_pairs[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && max_pairs[dev] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = num_sms() / 2;
+    max_pairs[dev] = n < num_sms() / 2 ? n : num_sms() / 2;
+  }
+  const int pairs_max = (dev >= 0 && dev < 64) ? max_pairs[dev] : num_sms() / 2;
+  const int tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kPairBN - 1) / kPairBN);
+  const int pairs = tiles < pairs_max ? tiles : pairs_max;
+  kern<<<2 * pairs, kThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, ea, K);
+  return cudaGetLastError();
+}
+
+// Kernel variant for an M x N problem: 0 = CTA pair (256 x 256 tiles),
+// otherwise the tile width of the single-CTA kernel.  Measured on the GPT-2
+// shapes: the pair wins wherever the output is wide (c_attn, c_fc, lm_head:
+// its per-SM operand traffic is lower); for D-wide outputs (N <= 1024) its
+// 256-wide tiles leave too few tiles for 76 pairs and the single-CTA kernel
+// with the tile width that needs the fewest rounds wins.
+int pick_variant(int M, int N) {
+#ifdef GPT2_GEMM_FORCE_BN
+  (void)M;
+  (void)N;
+  return GPT2_GEMM_FORCE_BN;
+#else
+  if (M >= 2 * kBM && N > 1024) return 0;
+  const int sms = num_sms();
+  int best = 192;
+  long long best_cost = -1;
+  for (int bn : {192, 128, 256}) {
+    const long long tiles = static_cast<long long>((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
+    const long long rounds = (tiles + sms - 1) / sms;
+    // cycles per k-block: operand bytes at ~60 B per cycle per SM, at least the MMA time
+    const long long per_kb = std::max<long long>(bn * 2, (kBM + bn) * kBK * 2 / 60);
+    const long long cost = rounds * per_kb;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
     }
   }
+  return best;
+#endif
+}
+
+template <bool B_MN, int EPI, typename OutT>
+cudaError_t run_variant(int v, const __nv_bfloat16* x, const __nv_bfloat16* w, const EpiArgs<OutT>& ea, int K,
+                        cudaStream_t s) {
+  switch (v) {
+    case 0: return run_2sm<B_MN, EPI, OutT>(x, w, ea, K, s);
+    case 128: return run_1sm<128, B_MN, EPI, OutT>(x, w, ea, K, s);
+    case 192: return run_1sm<192, B_MN, EPI, OutT>(x, w, ea, K, s);
+    default: return run_1sm<256, B_MN, EPI, OutT>(x, w, ea, K, s);
+  }
+}
+
+template <bool B_MN>
+cudaError_t dispatch(int v, const __nv_bfloat16* x, const __nv_bfloat16* w, const __nv_bfloat16* bias,
+                     const float* residual, void* y, int M, int N, int K, long long ldy, int epi, gpt2_dtype y_t,
+                     cudaStream_t s) {
+  using bf = __nv_bfloat16;
+  unsigned* err = device_error_word();
+  if (epi == EPI_RES) {
+    EpiArgs<float> ea{bias, residual, static_cast<float*>(y), ldy, M, N, err};
+    return run_variant<B_MN, EPI_RES, float>(v, x, w, ea, K, s);
+  }
+  if (y_t == GPT2_BF16) {
+    EpiArgs<bf> ea{bias, residual, static_cast<bf*>(y), ldy, M, N, err};
+    switch (epi) {
+      case EPI_NONE: return run_variant<B_MN, EPI_NONE, bf>(v, x, w, ea, K, s);
+      case EPI_BIAS: return run_variant<B_MN, EPI_BIAS, bf>(v, x, w, ea, K, s);
+      default: return run_variant<B_MN, EPI_GELU, bf>(v, x, w, ea, K, s);
+    }
+  }
+  EpiArgs<float> ea{bias, residual, static_cast<float*>(y), ldy, M, N, err};
   switch (epi) {
-    case EPI_NONE: return run<BN, B_MN, EPI_NONE, float>(x, w, bias, residual, static_cast<float*>(y), M, N, K, ldy, s);
-    case EPI_BIAS: return run<BN, B_MN, EPI_BIAS, float>(x, w, bias, residual, static_cast<float*>(y), M, N, K, ldy, s);
-    default: return run<BN, B_MN, EPI_GELU, float>(x, w, bias, residual, static_cast<float*>(y), M, N, K, ldy, s);
+    case EPI_NONE: return run_variant<B_MN, EPI_NONE, float>(v, x, w, ea, K, s);
+    case EPI_BIAS: return run_variant<B_MN, EPI_BIAS, float>(v, x, w, ea, K, s);
+    default: return run_variant<B_MN, EPI_GELU, float>(v, x, w, ea, K, s);
   }
 }
 
@@ -392,16 +787,10 @@ cudaError_t launch_gemm_bf16(const __nv_bfloat16* x, const __nv_bfloat16* w, con
                              const float* residual, void* y, int64_t M, int N, int K, int64_t ldy, bool w_out_in,
                              int epilogue, gpt2_dtype y_t, cudaStream_t stream) {
   if (M == 0) return cudaSuccess;
-  // Wide outputs use 128 x 256 tiles; narrow ones (N <= 1024, e.g. the two
-  // D-wide projections) 128 x 128 tiles so that more SMs get work.
-  const bool wide = N > 1024;
   const int m = static_cast<int>(M);
-  if (wide) {
-    return w_out_in ? dispatch_epi<256, false>(x, w, bias, residual, y, m, N, K, ldy, epilogue, y_t, stream)
-                    : dispatch_epi<256, true>(x, w, bias, residual, y, m, N, K, ldy, epilogue, y_t, stream);
-  }
-  return w_out_in ? dispatch_epi<128, false>(x, w, bias, residual, y, m, N, K, ldy, epilogue, y_t, stream)
-                  : dispatch_epi<128, true>(x, w, bias, residual, y, m, N, K, ldy, epilogue, y_t, stream);
+  const int v = pick_variant(m, N);
+  return w_out_in ? dispatch<false>(v, x, w, bias, residual, y, m, N, K, ldy, epilogue, y_t, stream)
+                  : dispatch<true>(v, x, w, bias, residual, y, m, N, K, ldy, epilogue, y_t, stream);
 }
 
 }  // namespace gpt2

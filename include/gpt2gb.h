@@ -146,7 +146,12 @@ int gpt2_layernorm(const void *x, const void *gamma, const void *beta, void *y, 
  * y [M, ldy] of type y_t (fp32 when the epilogue is BIAS_RESIDUAL).
  * The BF16 path runs on the tcgen05 tensor cores (fp32 accumulate in tensor
  * memory); the F32 path on CUDA cores in fp32.
- *   M >= 0, N >= 1, K a multiple of 64, ldy >= N. */
+ *   M >= 0, N >= 1, K a multiple of 64, ldy >= N.  BF16 path: ldy times the
+ *   size of y_t a multiple of 16 bytes (y is written by TMA bulk stores),
+ *   N a multiple of 8 for GPT2_W_IN_OUT; BIAS_RESIDUAL: N a multiple of 4.
+ *   Otherwise GPT2_ERR_UNSUPPORTED.  On the BF16 path the padding columns of
+ *   each row of y from N up to the next 16-byte boundary are written with
+ *   zeros; columns beyond that boundary are never written. */
 int gpt2_linear(const void *x, const void *w, const void *bias, const float *residual, void *y, int64_t M, int N,
                 int K, int64_t ldy, gpt2_weight_layout w_layout, gpt2_epilogue epilogue, gpt2_dtype dtype,
                 gpt2_dtype y_t, gpt2_stream_t stream);
@@ -195,7 +200,8 @@ int gpt2_block_forward(const gpt2_dims *dims, const gpt2_block_weights *w, const
  *   x0 = wte[tokens] + wpe[0..T-1]; n_layer blocks; logits = LN_f(x) wte^T.
  *   tokens: int32 [B, T] device, each in [0, vocab) (else GPT2_ERR_RANGE on
  *   the device; that row's embedding is taken as zero); logits [B, T, ld] of
- *   type logits_t, ld >= vocab; T <= n_pos. */
+ *   type logits_t, ld >= vocab, ld times the element size a multiple of 16
+ *   bytes on the BF16 path; T <= n_pos. */
 int gpt2_forward_logits(const gpt2_dims *dims, const gpt2_model_weights *w, const int32_t *tokens, void *logits,
                         int64_t ld, gpt2_dtype logits_t, int B, int T, void *ws, size_t ws_bytes,
                         gpt2_stream_t stream);
@@ -220,7 +226,7 @@ size_t gpt2_decode_workspace_bytes(const gpt2_dims *dims, int B);
  *   past_len[b] < T_max and < n_pos (else GPT2_ERR_RANGE on the device, and
  *   that sequence is left unchanged); tokens, next_tokens: int32 [B] device
  *   (they may be the same buffer); logits_opt: NULL or fp32 [B, ld] device
- *   receiving the step's logits (ld >= vocab); ws of
+ *   receiving the step's logits (ld >= vocab, a multiple of 4); ws of
  *   gpt2_decode_workspace_bytes(dims, B) bytes.  Only the BF16 path. */
 int gpt2_decode_step(const gpt2_dims *dims, const gpt2_model_weights *w, void *kv_cache, int B, int T_max,
                      int32_t *past_len, const int32_t *tokens, int32_t *next_tokens, float *logits_opt, int64_t ld,

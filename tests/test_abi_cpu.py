@@ -91,6 +91,8 @@ def test_argument_checks_before_any_launch(L):
     assert L.gpt2_linear(16, 16, None, None, 16, 10, 768, 768, 768, 0, 1, 1, 1, None) == 1  # bias missing
     assert L.gpt2_linear(16, 16, 16, None, 16, 10, 770, 768, 770, 0, 1, 1, 1, None) == 2  # N % 8 (bf16 [K,N])
     assert L.gpt2_linear(17, 16, 16, None, 16, 10, 768, 768, 768, 0, 1, 1, 1, None) == 1  # misaligned x
+    assert L.gpt2_linear(16, 16, None, None, 16, 10, 1000, 768, 1001, 1, 0, 1, 1, None) == 2  # bf16 row not 16 B
+    assert L.gpt2_linear(16, 16, 16, 16, 16, 10, 1002, 768, 1004, 1, 3, 1, 0, None) == 2  # residual needs N % 4
     assert L.gpt2_attention_causal(16, 16, 2, 64, 12, 32, 1, None) == 2                  # head_dim != 64
     assert L.gpt2_attention_causal(16, 16, 0, 64, 12, 64, 1, None) == 0                  # B = 0
     d = G.make_dims(2, 768, 12, 3072, 50257, 1024)

@@ -110,14 +110,17 @@ def test_linear_bf16(case, epi):
     bias = bf16(0.5 * r.standard_normal(N))
     res = f32(r.standard_normal((M, N)))
     y_t = "f32" if epi == G.EPI_BIAS_RESIDUAL else "bf16"
-    ld = N + (8 if N % 8 == 0 else 8 - N % 8) if layout == G.W_OUT_IN else N  # padded row stride for logits
+    ld = (N + 15) // 8 * 8 if layout == G.W_OUT_IN else N  # padded row stride (at least 8 spare columns)
     y = torch.full((M, ld), float("nan"), device="cuda", dtype=torch.float32 if y_t == "f32" else torch.bfloat16)
     rt = to_t(res, "f32")
     G.gpt2_linear(to_t(x, "bf16"), to_t(w, "bf16"), to_t(bias, "bf16"), rt, y, M, N, K, ld, layout, epi, G.BF16,
                   G.F32 if y_t == "f32" else G.BF16)
     torch.cuda.synchronize()
     got = to_np(y)
-    assert np.all(np.isnan(got[:, N:])), "wrote past N"
+    esz = 4 if y_t == "f32" else 2
+    n16 = (N * esz + 15) // 16 * 16 // esz  # the row padding up to 16 bytes is written with zeros
+    assert np.all(got[:, N:n16] == 0), "padding up to the 16-byte boundary"
+    assert np.all(np.isnan(got[:, n16:])), "wrote past the 16-byte boundary after N"
     got = got[:, :N]
     ref, absz, pre = _linear_ref(x, w, bias, res, epi, layout)
     rtol = 2.0 ** -8 if y_t == "bf16" else 2.0 ** -20
