@@ -16,7 +16,8 @@ __all__ = [
     "GPT2Error", "F32", "BF16", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_GELU", "EPI_BIAS_RESIDUAL", "W_IN_OUT",
     "W_OUT_IN", "Dims", "BlockWeights", "ModelWeights", "lib", "library_path", "gpt2_abi_version",
     "gpt2_status_string", "gpt2_last_error", "gpt2_layernorm", "gpt2_linear", "gpt2_attention_causal",
-    "gpt2_mlp_workspace_bytes", "gpt2_mlp", "gpt2_workspace_bytes", "gpt2_block_forward", "gpt2_forward_logits",
+    "gpt2_mlp_workspace_bytes", "gpt2_mlp", "gpt2_mlp_noalloc", "gpt2_mlp_noalloc_max_scratch_bytes",
+    "gpt2_workspace_bytes", "gpt2_block_forward", "gpt2_forward_logits",
     "gpt2_kv_cache_bytes", "gpt2_decode_workspace_bytes", "gpt2_decode_step", "gpt2_profile_begin",
     "gpt2_profile_end", "gpt2_profile_read", "ProfileEntry",
 ]
@@ -83,6 +84,8 @@ _SIGS = {
     "gpt2_decode_workspace_bytes": (_SZ, [ctypes.POINTER(Dims), _I32]),
     "gpt2_decode_step": (_I32, [ctypes.POINTER(Dims), ctypes.POINTER(ModelWeights), _VP, _I32, _I32, _VP, _VP, _VP,
                                 _VP, _I64, _VP, _SZ, _VP]),
+    "gpt2_mlp_noalloc_max_scratch_bytes": (_SZ, []),
+    "gpt2_mlp_noalloc": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I32, _I32, _I32, _VP]),
     "gpt2_profile_begin": (_I32, [_I32]),
     "gpt2_profile_end": (_I32, []),
     "gpt2_profile_read": (_I32, [ctypes.POINTER(ProfileEntry), _I32, ctypes.POINTER(ctypes.c_int)]),
@@ -164,6 +167,16 @@ def gpt2_mlp_workspace_bytes(M, F, dtype) -> int:
 def gpt2_mlp(x, w_fc, b_fc, w_proj, b_proj, residual, out, M, D, F, ws, ws_bytes, dtype, stream=None):
     _check(lib().gpt2_mlp(_ptr(x), _ptr(w_fc), _ptr(b_fc), _ptr(w_proj), _ptr(b_proj), _ptr(residual), _ptr(out), M,
                           D, F, _ptr(ws), ws_bytes, dtype, _stream(stream)), "gpt2_mlp")
+
+
+def gpt2_mlp_noalloc_max_scratch_bytes() -> int:
+    return lib().gpt2_mlp_noalloc_max_scratch_bytes()
+
+
+def gpt2_mlp_noalloc(x, w_fc, b_fc, w_proj, b_proj, residual, out, M, D, F, dtype, stream=None):
+    """gpt2_mlp with the library's own fixed scratch instead of a workspace."""
+    _check(lib().gpt2_mlp_noalloc(_ptr(x), _ptr(w_fc), _ptr(b_fc), _ptr(w_proj), _ptr(b_proj), _ptr(residual),
+                                  _ptr(out), M, D, F, dtype, _stream(stream)), "gpt2_mlp_noalloc")
 
 
 def gpt2_workspace_bytes(dims: Dims, B: int, T: int) -> int:

@@ -182,6 +182,28 @@ int gpt2_mlp(const void *x, const void *w_fc, const void *b_fc, const void *w_pr
              const float *residual, float *out, int64_t M, int D, int F, void *ws, size_t ws_bytes,
              gpt2_dtype dtype, gpt2_stream_t stream);
 
+/* gpt2_mlp without a workspace argument, for callers that cannot allocate
+ * device memory when they call in (for example a plug-in whose host
+ * framework has reserved the GPU's memory in its own pool, or code running
+ * while a stream is captured into a CUDA graph, where cudaMalloc is not
+ * allowed).  The pages have no counterpart of this call: it is a deployment
+ * convenience over gpt2_mlp, with identical arguments apart from the
+ * workspace and identical results.
+ *   The [M, F] hidden activation is kept in a scratch array in device memory
+ *   that the library owns: gpt2_mlp_noalloc_max_scratch_bytes() bytes per
+ *   GPU (16 MiB), held from the library's first use on a device until the
+ *   process exits.  M * F * (2 for BF16, 4 for F32) above that size returns
+ *   GPT2_ERR_WORKSPACE and runs nothing.  Nothing is allocated by the call.
+ *   The first call on each device looks up the scratch array's device
+ *   address (cudaGetSymbolAddress); make that first call outside stream
+ *   capture.  All calls on a device share the one array: calls whose GPU
+ *   work may overlap (unordered streams) race on it; calls ordered on one
+ *   stream are safe.  No part of the array needs clearing between calls. */
+size_t gpt2_mlp_noalloc_max_scratch_bytes(void);
+int gpt2_mlp_noalloc(const void *x, const void *w_fc, const void *b_fc, const void *w_proj, const void *b_proj,
+                     const float *residual, float *out, int64_t M, int D, int F, gpt2_dtype dtype,
+                     gpt2_stream_t stream);
+
 /* Workspace needed by gpt2_block_forward and gpt2_forward_logits for a
  * [B, T] batch (0 if the dims are invalid). */
 size_t gpt2_workspace_bytes(const gpt2_dims *dims, int B, int T);
