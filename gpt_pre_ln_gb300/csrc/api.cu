@@ -198,11 +198,19 @@ cudaError_t attention(gpt2_dtype dt, const void* qkv, void* out, int B, int T, i
   // causal algorithmic work: q.k and p.v over the j <= i pairs only
   const double pairs = static_cast<double>(B) * H * T * (T + 1.0) / 2.0;
   const double D = 64.0 * H;
+#ifdef GPT2_ATTN_MMA_SYNC
   ProfScope prof(dt == GPT2_BF16 ? "attn_causal_bf16_mma" : "attn_causal_f32", 4.0 * 64.0 * pairs,
                  static_cast<double>(B) * T * 4.0 * D * esize(dt), s);
   if (dt == GPT2_BF16)
     return launch_attention_bf16(static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out), B, T, H,
                                  s);
+#else
+  ProfScope prof(dt == GPT2_BF16 ? "attn_causal_bf16_tc" : "attn_causal_f32", 4.0 * 64.0 * pairs,
+                 static_cast<double>(B) * T * 4.0 * D * esize(dt), s);
+  if (dt == GPT2_BF16)
+    return launch_attention_bf16_tc(static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out), B, T,
+                                    H, s);
+#endif
   return launch_attention_f32(static_cast<const float*>(qkv), static_cast<float*>(out), B, T, H, s);
 }
 

@@ -1,0 +1,380 @@
+// Causal multi-head self-attention on the 5th-generation tensor cores.
+//
+//   out[b, i, h*64 + d] = sum_{j <= i} softmax_j(q_i . k_j / sqrt(64)) v_j[d]
+//
+// ("逐行拆GPT-2源码", GPT2Attention ``_split_heads`` / ``_attn`` /
+// ``_merge_heads``; llm.c notes 2.2-2.3: scale 1/sqrt(d_k), future positions
+// masked before the softmax, row maximum subtracted.)
+//
+// One CTA per (batch, head, tile of 128 queries), two CTAs per SM so that one
+// CTA's softmax overlaps the other's tensor-core work.  Per key tile of 128:
+//   S = Q K^T          tcgen05.mma M=128 N=128 K=64 -> tensor memory (fp32)
+//   softmax            4 warps, thread = query row = tensor-memory lane: the
+//                      row maximum and sum need no cross-thread exchange;
+//                      P = exp2(S * log2(e)/8 - m) written back as bf16 over
+//                      the S columns (tcgen05.st)
+//   O += P V           tcgen05.mma M=128 N=64 K=128 with A = P read from
+//                      tensor memory and V from shared memory (MN-major)
+// The running maximum m is only raised (and O, l rescaled) when a row's new
+// maximum exceeds it by more than 8 in the log2 domain; otherwise P may reach
+// 2^8, harmless in fp32 sums and bf16.  Key tiles entirely above the
+// diagonal are never loaded; the diagonal tile is masked by index.  Q, K, V
+// tiles are read by TMA straight from the packed [B*T, 3D] c_attn output (the
+// Q|K|V split and head split are the TMA coordinates); the head merge is
+// the store into [B, T, D].
+//
+// Waits are bounded (common.cuh): a timeout records GPT2_ERR_TIMEOUT and the
+// roles unwind; tensor memory is freed on every path.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gpt2 {
+
+namespace {
+
+constexpr int kHd = 64;
+constexpr int kTq = 128;  // queries per CTA
+constexpr int kTk = 128;  // keys per tile
+constexpr int kAttnThreads = 192;
+constexpr int kTileBytes = kTq * kHd * 2;  // 16 KB, 128-byte rows, swizzled
+constexpr int kSmemBytes = 1024 + 5 * kTileBytes + 256;
+constexpr uint32_t kTmemCols = 256;  // S: 128 columns, O: 64 columns
+constexpr uint32_t kOCol = 128;
+constexpr float kRescaleLog2 = 8.f;
+
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 2)
+    attn_causal_tc(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict__ out, int T, int H,
+                   unsigned* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sQ = smem_u32(smem);
+  const uint32_t sK0 = sQ + kTileBytes;      // K stages 0, 1
+  const uint32_t sV0 = sQ + 3 * kTileBytes;  // V stages 0, 1
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 5 * kTileBytes);
+  const uint32_t q_full = smem_u32(bars + 0);
+  auto kv_full = [&](int s) { return smem_u32(bars + 1 + s); };
+  auto kv_empty = [&](int s) { return smem_u32(bars + 3 + s); };
+  const uint32_t s_full = smem_u32(bars + 5);
+  const uint32_t p_ready = smem_u32(bars + 6);
+  const uint32_t pv_done = smem_u32(bars + 7);
+  const uint32_t drain = smem_u32(bars + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int b = bh / H;
+  const int h = bh % H;
+  const int D = H * kHd;
+  const int n_qt = (T + kTq - 1) / kTq;
+  const int qt = n_qt - 1 - static_cast<int>(blockIdx.y);  // heaviest tiles first
+  const int q0 = qt * kTq;
+  const int n_kv = qt + 1;  // key tiles 0..qt; later ones are fully masked
+  const int row_base = b * T;  // first row of this sequence in [B*T, 3D]
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tm_qkv);
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_ready, 128);
+    mbar_init(pv_done, 1);
+    mbar_init(drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      mbar_arrive_expect_tx(q_full, kTileBytes);
+      tma_load_2d(sQ, &tm_qkv, q_full, h * kHd, row_base + q0);
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(kv_empty(st), ((j >> 1) & 1) ^ 1)) {
+          record_error(err, kErrTimeout, kSiteAttnProducer);
+          break;
+        }
+        mbar_arrive_expect_tx(kv_full(st), 2 * kTileBytes);
+        tma_load_2d(sK0 + st * kTileBytes, &tm_qkv, kv_full(st), D + h * kHd, row_base + j * kTk);
+        tma_load_2d(sV0 + st * kTileBytes, &tm_qkv, kv_full(st), 2 * D + h * kHd, row_base + j * kTk);
+        ++issued;
+      }
+      // copies still in flight: the Q tile and the last (up to two) stages
+      if (!mbar_wait(q_full, 0)) record_error(err, kErrTimeout, kSiteAttnProducer);
+      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
+        if (!mbar_wait(kv_full(j & 1), (j >> 1) & 1)) {
+          record_error(err, kErrTimeout, kSiteAttnProducer);
+          break;
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kTq, kTk, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(kTq, kHd, false, true);
+      bool ok = mbar_wait(q_full, 0);
+      bool any = false;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int st = j & 1;
+        ok = mbar_wait(kv_full(st), (j >> 1) & 1);
+        // the previous P.V has read P (which lies over S) before S is rewritten
+        if (ok && j > 0) ok = mbar_wait(pv_done, (j - 1) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t kb = sK0 + st * kTileBytes;
+#pragma unroll
+        for (int k = 0; k < kHd / 16; ++k)
+          umma_bf16(tmem, sdesc_sw128(sQ + k * 32, 16, 1024), sdesc_sw128(kb + k * 32, 16, 1024), idesc_s,
+                    k > 0 ? 1u : 0u);
+        umma_commit(s_full);
+        any = true;
+        if (!mbar_wait(p_ready, j & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t vb = sV0 + st * kTileBytes;
+#pragma unroll
+        for (int k = 0; k < kTk / 16; ++k)  // P: 8 tensor-memory columns (16 bf16) per K=16
+          umma_bf16_ts(tmem + kOCol, tmem + k * 8, sdesc_sw128(vb + k * 2048, 8192, 1024), idesc_pv,
+                       (j | k) != 0 ? 1u : 0u);
+        umma_commit(pv_done);
+        umma_commit(kv_empty(st));
+      }
+      if (!ok) record_error(err, kErrTimeout, kSiteAttnMma);
+      if (any) {
+        umma_commit(drain);
+        if (!mbar_wait(drain, 0)) record_error(err, kErrTimeout, kSiteAttnMma);
+      }
+    }
+  } else {
+    // ------------------------------------------------ softmax (warps 2..5)
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // query row within the tile
+    const int q = q0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_off;
+    const uint32_t tO = tmem + lane_off + kOCol;
+    const float scale = 1.4426950408889634f * 0.125f;  // log2(e) / sqrt(64)
+    float m_run = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const bool got = mbar_wait(s_full, j & 1);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool diag = (j == qt);
+      const int k0 = j * kTk;
+      // pass 1: row maximum of the raw scores (8 independent partial maxima;
+      // the scale is positive, so it is applied once to the maximum)
+      float pm[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) pm[e] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kTk / 32; ++c) {
+        uint32_t raw[32];
+        tmem_ld_32x32b_x32(tS + c * 32, raw);
+        tmem_ld_wait();
+        if (diag) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (k0 + c * 32 + i <= q) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(raw[i]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(raw[i]));
+        }
+      }
+      const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * scale;
+      const bool raise = mx > m_run + kRescaleLog2;
+      // tcgen05.ld / tcgen05.st are warp-collective: the whole warp takes
+      // the rescale branch if any of its rows needs it (alpha = 1 for the
+      // others)
+      if (j > 0 && __any_sync(0xffffffffu, raise)) {
+        // O and l were accumulated against m_run: bring them to mx
+        const float alpha = raise ? ex2_approx(m_run - mx) : 1.f;
+        l *= alpha;
+#pragma unroll
+        for (int c = 0; c < kHd / 32; ++c) {
+          uint32_t raw[32];
+          tmem_ld_32x32b_x32(tO + c * 32, raw);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) raw[i] = __float_as_uint(__uint_as_float(raw[i]) * alpha);
+          tmem_st_32x32b_x32(tO + c * 32, raw);
+        }
+      }
+      if (raise) m_run = mx;
+      // pass 2: P = exp2(s * scale - m_run) as bf16 over the S columns;
+      // 8 independent partial sums
+      float ps[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ps[e] = 0.f;
+      const float neg_m = -m_run;
+#pragma unroll
+      for (int c = 0; c < kTk / 32; ++c) {
+        uint32_t raw[32];
+        tmem_ld_32x32b_x32(tS + c * 32, raw);
+        tmem_ld_wait();
+        float pv[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pv[i] = ex2_approx(fmaf(__uint_as_float(raw[i]), scale, neg_m));
+        if (diag) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (k0 + c * 32 + i > q) pv[i] = 0.f;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          ps[(2 * i) & 7] += pv[2 * i];
+          ps[(2 * i + 1) & 7] += pv[2 * i + 1];
+          __nv_bfloat162 pb = __floats2bfloat162_rn(pv[2 * i], pv[2 * i + 1]);
+          pk[i] = *reinterpret_cast<uint32_t*>(&pb);
+        }
+        tmem_st_32x32b_x16(tS + c * 16, pk);
+      }
+      l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_ready);
+    }
+    // the last P.V has completed when pv_done reaches its n_kv-th phase
+    if (ok) {
+      const bool got = mbar_wait(pv_done, (n_kv - 1) & 1);
+      ok = __all_sync(0xffffffffu, got);
+    }
+    if (!ok) {
+      if (lane == 0) record_error(err, kErrTimeout, kSiteAttnSoftmax);
+    } else {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      __nv_bfloat16* orow = out + (static_cast<long long>(row_base) + q) * D + h * kHd;
+#pragma unroll
+      for (int c = 0; c < kHd / 32; ++c) {
+        uint32_t raw[32];
+        tmem_ld_32x32b_x32(tO + c * 32, raw);
+        tmem_ld_wait();
+        if (q < T) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 u;
+            __nv_bfloat162* hp = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              hp[e] = __floats2bfloat162_rn(__uint_as_float(raw[v * 8 + 2 * e]) * inv,
+                                            __uint_as_float(raw[v * 8 + 2 * e + 1]) * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + v * 8) = u;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+cudaError_t launch_attention_bf16_tc(const __nv_bfloat16* qkv, __nv_bfloat16* out, int B, int T, int n_head,
+                                     cudaStream_t stream) {
+  if (B == 0 || T == 0) return cudaSuccess;
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorInvalidValue;
+  const uint64_t D = static_cast<uint64_t>(n_head) * kHd;
+  CUtensorMap map;
+  cuuint64_t dims[2] = {3 * D, static_cast<cuuint64_t>(B) * T};
+  cuuint64_t strides[1] = {3 * D * 2};
+  cuuint32_t box[2] = {kHd, kTq};
+  cuuint32_t estr[2] = {1, 1};
+  if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(qkv), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(attn_causal_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  dim3 grid(B * n_head, (T + kTq - 1) / kTq);
+  attn_causal_tc<<<grid, kAttnThreads, kSmemBytes, stream>>>(map, out, T, n_head, device_error_word());
+  return cudaGetLastError();
+}
+
+}  // namespace gpt2

@@ -24,6 +24,9 @@ enum ErrSite : unsigned {
   kSiteGemmMma = 2,
   kSiteGemmEpilogue = 3,
   kSiteGemmDrain = 4,
+  kSiteAttnProducer = 5,
+  kSiteAttnMma = 6,
+  kSiteAttnSoftmax = 7,
   kSiteEmbedToken = 10,
   kSiteDecodePos = 11,
   kSiteDecodeToken = 12,

@@ -92,7 +92,7 @@ template <int EPI, typename OutT>
 __device__ __forceinline__ void apply_bias_act(float (&v)[OutTraits<OutT>::CW], const __nv_bfloat16* __restrict__ bias,
                                                int col0, int N) {
   constexpr int CW = OutTraits<OutT>::CW;
-  if (EPI == EPI_NONE) return;
+  if constexpr (EPI == EPI_NONE) return;
 #pragma unroll
   for (int q = 0; q < CW / 8; ++q) {
     const int c = col0 + q * 8;

@@ -36,6 +36,9 @@ cudaError_t launch_gemm_f32(const float* x, const float* w, const float* bias, c
 
 cudaError_t launch_attention_bf16(const __nv_bfloat16* qkv, __nv_bfloat16* out, int B, int T, int n_head,
                                   cudaStream_t stream);
+// tcgen05 version (S and O in tensor memory), head_dim 64.
+cudaError_t launch_attention_bf16_tc(const __nv_bfloat16* qkv, __nv_bfloat16* out, int B, int T, int n_head,
+                                     cudaStream_t stream);
 cudaError_t launch_attention_f32(const float* qkv, float* out, int B, int T, int n_head, cudaStream_t stream);
 
 // Decode-step kernels (bf16 path).
