@@ -14,7 +14,7 @@ namespace gpt2 {
 
 namespace {
 
-constexpr int kLnThreads = 256;  // 8 rows per block
+constexpr int kLnThreads = 128;  // 4 rows per block
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -53,12 +53,39 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, const fl
   *reinterpret_cast<uint2*>(p) = u;
 }
 
+// gamma / beta for 4 consecutive columns, kept in their storage type until
+// use (bf16: 8 bytes) so that preloading them costs few registers.
+template <typename T> struct Raw4;
+template <> struct Raw4<float> {
+  float4 v;
+  __device__ __forceinline__ void load(const float* p) { v = *reinterpret_cast<const float4*>(p); }
+  __device__ __forceinline__ float get(int e) const { return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w; }
+};
+template <> struct Raw4<__nv_bfloat16> {
+  uint2 v;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { v = *reinterpret_cast<const uint2*>(p); }
+  __device__ __forceinline__ float get(int e) const {
+    const uint32_t w = e < 2 ? v.x : v.y;
+    return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+  }
+};
+
 // Normalises the row held in v (NV groups of 4 per lane, lane-strided) and
-// writes it to yr.  Groups beyond D/4 hold zeros and are skipped.
+// writes it to yr.  Groups beyond D/4 hold zeros and are skipped.  gamma and
+// beta are loaded before the reductions so that their latency overlaps them.
 template <typename YT, int NV>
 __device__ __forceinline__ void ln_finish(float (&v)[NV][4], int lane, int D, float eps, const YT* gamma,
                                           const YT* beta, YT* yr) {
   const int nvec = D >> 2;
+  Raw4<YT> g[NV], bb[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = (lane + i * 32) * 4;
+    if (c < D) {
+      g[i].load(gamma + c);
+      bb[i].load(beta + c);
+    }
+  }
   float s = 0.f;
 #pragma unroll
   for (int i = 0; i < NV; ++i) s += (v[i][0] + v[i][1]) + (v[i][2] + v[i][3]);
@@ -80,11 +107,9 @@ __device__ __forceinline__ void ln_finish(float (&v)[NV][4], int lane, int D, fl
   for (int i = 0; i < NV; ++i) {
     const int c = (lane + i * 32) * 4;
     if (c < D) {
-      float g[4], b[4], o[4];
-      load4<YT>(gamma + c, g);
-      load4<YT>(beta + c, b);
+      float o[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) o[e] = fmaf((v[i][e] - mean) * rstd, g[e], b[e]);
+      for (int e = 0; e < 4; ++e) o[e] = fmaf((v[i][e] - mean) * rstd, g[i].get(e), bb[i].get(e));
       store4<YT>(yr + c, o);
     }
   }
@@ -161,8 +186,12 @@ cudaError_t ln_dispatch(const void* x, const void* g, const void* b, void* y, lo
   auto Y = static_cast<YT*>(y);
   if (D <= 512)
     layernorm_rows<XT, YT, 4><<<blocks, kLnThreads, 0, s>>>(X, G, Bt, Y, rows, D, eps);
+  else if (D <= 768)
+    layernorm_rows<XT, YT, 6><<<blocks, kLnThreads, 0, s>>>(X, G, Bt, Y, rows, D, eps);
   else if (D <= 1024)
     layernorm_rows<XT, YT, 8><<<blocks, kLnThreads, 0, s>>>(X, G, Bt, Y, rows, D, eps);
+  else if (D <= 1664)
+    layernorm_rows<XT, YT, 13><<<blocks, kLnThreads, 0, s>>>(X, G, Bt, Y, rows, D, eps);
   else if (D <= 2048)
     layernorm_rows<XT, YT, 16><<<blocks, kLnThreads, 0, s>>>(X, G, Bt, Y, rows, D, eps);
   else
@@ -182,6 +211,8 @@ cudaError_t embed_dispatch(const int32_t* tokens, const void* wte, const void* w
   unsigned* err = device_error_word();
   if (D <= 512)
     embed_ln_rows<WT, 4><<<blocks, kLnThreads, 0, s>>>(tokens, E, P, G, Bt, x, Y, rows, T, D, V, eps, err);
+  else if (D <= 768)
+    embed_ln_rows<WT, 6><<<blocks, kLnThreads, 0, s>>>(tokens, E, P, G, Bt, x, Y, rows, T, D, V, eps, err);
   else if (D <= 1024)
     embed_ln_rows<WT, 8><<<blocks, kLnThreads, 0, s>>>(tokens, E, P, G, Bt, x, Y, rows, T, D, V, eps, err);
   else if (D <= 2048)
