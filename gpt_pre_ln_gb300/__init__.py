@@ -13,7 +13,7 @@ import ctypes
 import os
 
 __all__ = [
-    "GPT2Error", "F32", "BF16", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_GELU", "EPI_BIAS_RESIDUAL", "W_IN_OUT",
+    "GPT2Error", "F32", "BF16", "F16", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_GELU", "EPI_BIAS_RESIDUAL", "W_IN_OUT",
     "W_OUT_IN", "Dims", "BlockWeights", "ModelWeights", "lib", "library_path", "gpt2_abi_version",
     "gpt2_status_string", "gpt2_last_error", "gpt2_layernorm", "gpt2_linear", "gpt2_attention_causal",
     "gpt2_mlp_workspace_bytes", "gpt2_mlp", "gpt2_mlp_noalloc", "gpt2_mlp_noalloc_max_scratch_bytes",
@@ -26,7 +26,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 # the in-tree build, or another build of the same sources named by GPT2GB_LIBRARY
 library_path = os.environ.get("GPT2GB_LIBRARY") or os.path.join(_PKG, "libgpt2gb.so")
 
-F32, BF16 = 0, 1
+F32, BF16, F16 = 0, 1, 2
 EPI_NONE, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESIDUAL = 0, 1, 2, 3
 W_IN_OUT, W_OUT_IN = 0, 1
 
@@ -246,13 +246,13 @@ def model_weights(tensors: dict):
 def to_device(params: dict, dtype: int, device="cuda"):
     """Copy a parameter dict of float32 numpy arrays to device tensors.
 
-    Arrays are converted to bf16 (``dtype == BF16``) or kept fp32; the values
-    are expected to be exactly representable already.  Returns the same
+    Arrays are converted to bf16 (``dtype == BF16``), fp16 (``F16``) or kept
+    fp32; the values are expected to be exactly representable already.  Returns the same
     nesting ({..., "blocks": [dict]}) with torch tensors.
     """
     import numpy as np
     import torch
-    tdt = torch.bfloat16 if dtype == BF16 else torch.float32
+    tdt = {BF16: torch.bfloat16, F16: torch.float16}.get(dtype, torch.float32)
 
     def up(a):
         return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device=device).to(tdt).contiguous()

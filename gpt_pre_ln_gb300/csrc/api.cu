@@ -130,8 +130,9 @@ class ProfScope {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
-inline size_t esize(gpt2_dtype t) { return t == GPT2_BF16 ? 2 : 4; }
-inline bool valid_dtype(int t) { return t == GPT2_F32 || t == GPT2_BF16; }
+inline size_t esize(gpt2_dtype t) { return t == GPT2_F32 ? 4 : 2; }
+inline bool valid_dtype(int t) { return t == GPT2_F32 || t == GPT2_BF16 || t == GPT2_F16; }
+inline bool is16(gpt2_dtype t) { return t == GPT2_BF16 || t == GPT2_F16; }
 inline cudaStream_t cs(gpt2_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
 struct Carve {
@@ -186,10 +187,9 @@ cudaError_t linear(gpt2_dtype dt, const void* x, const void* w, const void* bias
   const double bytes = (static_cast<double>(M) * K + static_cast<double>(K) * N) * e +
                        (epi != GPT2_EPI_NONE ? N * e : 0.0) +
                        (epi == GPT2_EPI_BIAS_RESIDUAL ? 4.0 * M * N : 0.0) + static_cast<double>(M) * N * esize(y_t);
-  ProfScope prof(dt == GPT2_BF16 ? "gemm_bf16_tcgen05" : "gemm_f32_simt", 2.0 * M * N * K, bytes, s);
-  if (dt == GPT2_BF16)
-    return launch_gemm_bf16(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w),
-                            static_cast<const __nv_bfloat16*>(bias), res, y, M, N, K, ldy, w_out_in, epi, y_t, s);
+  ProfScope prof(dt == GPT2_BF16 ? "gemm_bf16_tcgen05" : dt == GPT2_F16 ? "gemm_f16_tcgen05" : "gemm_f32_simt",
+                 2.0 * M * N * K, bytes, s);
+  if (is16(dt)) return launch_gemm_16(dt, x, w, bias, res, y, M, N, K, ldy, w_out_in, epi, y_t, s);
   return launch_gemm_f32(static_cast<const float*>(x), static_cast<const float*>(w), static_cast<const float*>(bias),
                          res, static_cast<float*>(y), M, N, K, ldy, w_out_in, epi, s);
 }
@@ -198,19 +198,9 @@ cudaError_t attention(gpt2_dtype dt, const void* qkv, void* out, int B, int T, i
   // causal algorithmic work: q.k and p.v over the j <= i pairs only
   const double pairs = static_cast<double>(B) * H * T * (T + 1.0) / 2.0;
   const double D = 64.0 * H;
-#ifdef GPT2_ATTN_MMA_SYNC
-  ProfScope prof(dt == GPT2_BF16 ? "attn_causal_bf16_mma" : "attn_causal_f32", 4.0 * 64.0 * pairs,
-                 static_cast<double>(B) * T * 4.0 * D * esize(dt), s);
-  if (dt == GPT2_BF16)
-    return launch_attention_bf16(static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out), B, T, H,
-                                 s);
-#else
-  ProfScope prof(dt == GPT2_BF16 ? "attn_causal_bf16_tc" : "attn_causal_f32", 4.0 * 64.0 * pairs,
-                 static_cast<double>(B) * T * 4.0 * D * esize(dt), s);
-  if (dt == GPT2_BF16)
-    return launch_attention_bf16_tc(static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out), B, T,
-                                    H, s);
-#endif
+  ProfScope prof(dt == GPT2_BF16 ? "attn_causal_bf16_tc" : dt == GPT2_F16 ? "attn_causal_f16_tc" : "attn_causal_f32",
+                 4.0 * 64.0 * pairs, static_cast<double>(B) * T * 4.0 * D * esize(dt), s);
+  if (is16(dt)) return launch_attention_tc(dt, qkv, out, B, T, H, s);
   return launch_attention_f32(static_cast<const float*>(qkv), static_cast<float*>(out), B, T, H, s);
 }
 
@@ -334,9 +324,10 @@ int gpt2_linear(const void* x, const void* w, const void* bias, const float* res
   if (K % 64 != 0) return GPT2_ERR_UNSUPPORTED;
   if (epilogue == GPT2_EPI_BIAS_RESIDUAL && y_t != GPT2_F32) return GPT2_ERR_UNSUPPORTED;
   if (dtype == GPT2_F32 && y_t != GPT2_F32) return GPT2_ERR_UNSUPPORTED;
-  if (dtype == GPT2_BF16 && w_layout == GPT2_W_IN_OUT && N % 8 != 0) return GPT2_ERR_UNSUPPORTED;
-  // the tensor-core path stores through TMA: 16-byte aligned rows
-  if (dtype == GPT2_BF16 && (ldy * static_cast<int64_t>(esize(y_t))) % 16 != 0) return GPT2_ERR_UNSUPPORTED;
+  if (is16(dtype) && y_t != dtype && y_t != GPT2_F32) return GPT2_ERR_UNSUPPORTED;
+  if (is16(dtype) && w_layout == GPT2_W_IN_OUT && N % 8 != 0) return GPT2_ERR_UNSUPPORTED;
+  // the tensor-core epilogue stores 16-byte pieces: 16-byte aligned rows
+  if (is16(dtype) && (ldy * static_cast<int64_t>(esize(y_t))) % 16 != 0) return GPT2_ERR_UNSUPPORTED;
   if (epilogue == GPT2_EPI_BIAS_RESIDUAL && N % 4 != 0) return GPT2_ERR_UNSUPPORTED;
   if (M == 0) return GPT2_OK;
   if (!x || !w || !y || !aligned16(x) || !aligned16(w) || !aligned16(y)) return GPT2_ERR_ARG;
@@ -409,10 +400,10 @@ int gpt2_forward_logits(const gpt2_dims* dims, const gpt2_model_weights* w, cons
                         gpt2_stream_t stream) {
   GPT2_TRY(check_model(dims, w));
   if (!valid_dtype(logits_t)) return GPT2_ERR_ARG;
-  if (dims->dtype == GPT2_F32 && logits_t != GPT2_F32) return GPT2_ERR_UNSUPPORTED;
+  if (logits_t != GPT2_F32 && logits_t != dims->dtype) return GPT2_ERR_UNSUPPORTED;
   if (B < 0 || T < 0 || static_cast<int64_t>(B) * T > INT_MAX || ld < dims->vocab) return GPT2_ERR_ARG;
   if (T > dims->n_pos) return GPT2_ERR_ARG;
-  if (dims->dtype == GPT2_BF16 && (ld * static_cast<int64_t>(esize(logits_t))) % 16 != 0) return GPT2_ERR_UNSUPPORTED;
+  if (is16(dims->dtype) && (ld * static_cast<int64_t>(esize(logits_t))) % 16 != 0) return GPT2_ERR_UNSUPPORTED;
   if (B == 0 || T == 0) return GPT2_OK;
   if (!tokens || !logits || !aligned16(logits)) return GPT2_ERR_ARG;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return GPT2_ERR_ARG;
@@ -453,7 +444,7 @@ int gpt2_decode_step(const gpt2_dims* dims, const gpt2_model_weights* w, void* k
                      int32_t* past_len, const int32_t* tokens, int32_t* next_tokens, float* logits_opt, int64_t ld,
                      void* ws, size_t ws_bytes, gpt2_stream_t stream) {
   GPT2_TRY(check_model(dims, w));
-  if (dims->dtype != GPT2_BF16) return GPT2_ERR_UNSUPPORTED;
+  if (!is16(dims->dtype)) return GPT2_ERR_UNSUPPORTED;
   if (B < 0 || T_max <= 0) return GPT2_ERR_ARG;
   if (B == 0) return GPT2_OK;
   if (!kv_cache || !past_len || !tokens || !next_tokens || !aligned16(kv_cache)) return GPT2_ERR_ARG;
@@ -469,45 +460,39 @@ int gpt2_decode_step(const gpt2_dims* dims, const gpt2_model_weights* w, void* k
   A.a = c.take<char>(static_cast<size_t>(B) * D, 2);
   A.qkv = c.take<char>(static_cast<size_t>(B) * 3 * D, 2);
   A.o = c.take<char>(static_cast<size_t>(B) * D, 2);
-  A.g = c.take<char>(static_cast<size_t>(B) * F, 2);
+  A.g = c.take<char>(static_cast<size_t>(B) * F, 2);  // 16-bit paths only
   const int64_t Vp = (static_cast<int64_t>(V) + 3) & ~static_cast<int64_t>(3);
   float* lg = c.take<float>(static_cast<size_t>(B) * Vp, 4);
   int* valid = c.take<int>(static_cast<size_t>(B), 4);
   float* logits = logits_opt ? logits_opt : lg;
   const int64_t lld = logits_opt ? ld : Vp;
   cudaStream_t s = cs(stream);
-  using bf = __nv_bfloat16;
+  const gpt2_dtype dt = dims->dtype;
   const size_t layer_elems = static_cast<size_t>(2) * B * H * static_cast<size_t>(T_max) * 64;
   {
     ProfScope prof("decode_embed_layernorm", 8.0 * B * D, static_cast<double>(B) * D * 10.0, s);
-    GPT2_CUDA(launch_decode_embed_ln(tokens, past_len, static_cast<const bf*>(w->wte), static_cast<const bf*>(w->wpe),
-                                   static_cast<const bf*>(w->blocks[0].ln1_g),
-                                   static_cast<const bf*>(w->blocks[0].ln1_b), A.x, static_cast<bf*>(A.a), B, D, V,
-                                     dims->n_pos, T_max, dims->eps, valid, s));
+    GPT2_CUDA(launch_decode_embed_ln(dt, tokens, past_len, w->wte, w->wpe, w->blocks[0].ln1_g, w->blocks[0].ln1_b,
+                                     A.x, A.a, B, D, V, dims->n_pos, T_max, dims->eps, valid, s));
   }
   for (int l = 0; l < dims->n_layer; ++l) {
     const gpt2_block_weights* bw = &w->blocks[l];
-    if (l > 0) GPT2_CUDA(layernorm(A.x, bw->ln1_g, bw->ln1_b, A.a, B, D, dims->eps, GPT2_F32, GPT2_BF16, s));
-    GPT2_CUDA(linear(GPT2_BF16, A.a, bw->w_qkv, bw->b_qkv, nullptr, A.qkv, B, 3 * D, D, 3 * D, false, GPT2_EPI_BIAS,
-                     GPT2_BF16, s));
-    bf* kv_layer = static_cast<bf*>(kv_cache) + l * layer_elems;
+    if (l > 0) GPT2_CUDA(layernorm(A.x, bw->ln1_g, bw->ln1_b, A.a, B, D, dims->eps, GPT2_F32, dt, s));
+    GPT2_CUDA(linear(dt, A.a, bw->w_qkv, bw->b_qkv, nullptr, A.qkv, B, 3 * D, D, 3 * D, false, GPT2_EPI_BIAS, dt, s));
+    void* kv_layer = static_cast<char*>(kv_cache) + l * layer_elems * esize(dt);
     {
       // the cached lengths live on the device: the bytes of this kernel are
       // left to the caller, who knows them
       ProfScope prof("decode_attn", 0.0, 0.0, s);
-      GPT2_CUDA(launch_decode_attention(static_cast<const bf*>(A.qkv), kv_layer, static_cast<bf*>(A.o), past_len,
-                                        valid, B, H, T_max, s));
+      GPT2_CUDA(launch_decode_attention(dt, A.qkv, kv_layer, A.o, past_len, valid, B, H, T_max, s));
     }
-    GPT2_CUDA(linear(GPT2_BF16, A.o, bw->w_o, bw->b_o, A.x, A.h, B, D, D, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32,
+    GPT2_CUDA(linear(dt, A.o, bw->w_o, bw->b_o, A.x, A.h, B, D, D, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32, s));
+    GPT2_CUDA(layernorm(A.h, bw->ln2_g, bw->ln2_b, A.a, B, D, dims->eps, GPT2_F32, dt, s));
+    GPT2_CUDA(linear(dt, A.a, bw->w_fc, bw->b_fc, nullptr, A.g, B, F, D, F, false, GPT2_EPI_BIAS_GELU, dt, s));
+    GPT2_CUDA(linear(dt, A.g, bw->w_proj, bw->b_proj, A.h, A.x, B, D, F, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32,
                      s));
-    GPT2_CUDA(layernorm(A.h, bw->ln2_g, bw->ln2_b, A.a, B, D, dims->eps, GPT2_F32, GPT2_BF16, s));
-    GPT2_CUDA(linear(GPT2_BF16, A.a, bw->w_fc, bw->b_fc, nullptr, A.g, B, F, D, F, false, GPT2_EPI_BIAS_GELU,
-                     GPT2_BF16, s));
-    GPT2_CUDA(linear(GPT2_BF16, A.g, bw->w_proj, bw->b_proj, A.h, A.x, B, D, F, D, false, GPT2_EPI_BIAS_RESIDUAL,
-                     GPT2_F32, s));
   }
-  GPT2_CUDA(layernorm(A.x, w->lnf_g, w->lnf_b, A.a, B, D, dims->eps, GPT2_F32, GPT2_BF16, s));
-  GPT2_CUDA(linear(GPT2_BF16, A.a, w->wte, nullptr, nullptr, logits, B, V, D, lld, true, GPT2_EPI_NONE, GPT2_F32, s));
+  GPT2_CUDA(layernorm(A.x, w->lnf_g, w->lnf_b, A.a, B, D, dims->eps, GPT2_F32, dt, s));
+  GPT2_CUDA(linear(dt, A.a, w->wte, nullptr, nullptr, logits, B, V, D, lld, true, GPT2_EPI_NONE, GPT2_F32, s));
   {
     ProfScope prof("argmax_rows", static_cast<double>(B) * V, static_cast<double>(B) * V * 4.0, s);
     GPT2_CUDA(launch_argmax_rows(logits, lld, B, V, valid, next_tokens, past_len, s));

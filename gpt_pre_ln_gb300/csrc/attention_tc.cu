@@ -77,9 +77,9 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+template <typename T16>
 __global__ void __launch_bounds__(kAttnThreads, 2)
-    attn_causal_tc(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict__ out, int T, int H,
-                   unsigned* err) {
+    attn_causal_tc(const __grid_constant__ CUtensorMap tm_qkv, T16* __restrict__ out, int T, int H, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(smem);
@@ -157,8 +157,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc_s = idesc_bf16_f32(kTq, kTk, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(kTq, kHd, false, true);
+      constexpr uint32_t idesc_s = idesc_f16kind_f32(kTq, kTk, false, false, Type16<T16>::kFormat);
+      constexpr uint32_t idesc_pv = idesc_f16kind_f32(kTq, kHd, false, true, Type16<T16>::kFormat);
       bool ok = mbar_wait(q_full, 0);
       bool any = false;
       for (int j = 0; j < n_kv && ok; ++j) {
@@ -279,8 +279,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         for (int i = 0; i < 16; ++i) {
           ps[(2 * i) & 7] += pv[2 * i];
           ps[(2 * i + 1) & 7] += pv[2 * i + 1];
-          __nv_bfloat162 pb = __floats2bfloat162_rn(pv[2 * i], pv[2 * i + 1]);
-          pk[i] = *reinterpret_cast<uint32_t*>(&pb);
+          pk[i] = Type16<T16>::pack2(pv[2 * i], pv[2 * i + 1]);
         }
         tmem_st_32x32b_x16(tS + c * 16, pk);
       }
@@ -299,7 +298,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     } else {
       tc_fence_after();
       const float inv = 1.f / l;
-      __nv_bfloat16* orow = out + (static_cast<long long>(row_base) + q) * D + h * kHd;
+      T16* orow = out + (static_cast<long long>(row_base) + q) * D + h * kHd;
 #pragma unroll
       for (int c = 0; c < kHd / 32; ++c) {
         uint32_t raw[32];
@@ -308,13 +307,12 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         if (q < T) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            uint4 u;
-            __nv_bfloat162* hp = reinterpret_cast<__nv_bfloat162*>(&u);
+            uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              hp[e] = __floats2bfloat162_rn(__uint_as_float(raw[v * 8 + 2 * e]) * inv,
-                                            __uint_as_float(raw[v * 8 + 2 * e + 1]) * inv);
-            *reinterpret_cast<uint4*>(orow + c * 32 + v * 8) = u;
+              w[e] = Type16<T16>::pack2(__uint_as_float(raw[v * 8 + 2 * e]) * inv,
+                                        __uint_as_float(raw[v * 8 + 2 * e + 1]) * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + v * 8) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
       }
@@ -347,10 +345,8 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-}  // namespace
-
-cudaError_t launch_attention_bf16_tc(const __nv_bfloat16* qkv, __nv_bfloat16* out, int B, int T, int n_head,
-                                     cudaStream_t stream) {
+template <typename T16>
+cudaError_t launch_t(const void* qkv, void* out, int B, int T, int n_head, cudaStream_t stream) {
   if (B == 0 || T == 0) return cudaSuccess;
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorInvalidValue;
@@ -360,7 +356,7 @@ cudaError_t launch_attention_bf16_tc(const __nv_bfloat16* qkv, __nv_bfloat16* ou
   cuuint64_t strides[1] = {3 * D * 2};
   cuuint32_t box[2] = {kHd, kTq};
   cuuint32_t estr[2] = {1, 1};
-  if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(qkv), dims, strides, box, estr,
+  if (fn(&map, Type16<T16>::kTma, 2, const_cast<void*>(qkv), dims, strides, box, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
@@ -368,13 +364,23 @@ cudaError_t launch_attention_bf16_tc(const __nv_bfloat16* qkv, __nv_bfloat16* ou
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_causal_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_causal_tc<T16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   dim3 grid(B * n_head, (T + kTq - 1) / kTq);
-  attn_causal_tc<<<grid, kAttnThreads, kSmemBytes, stream>>>(map, out, T, n_head, device_error_word());
+  attn_causal_tc<T16><<<grid, kAttnThreads, kSmemBytes, stream>>>(map, static_cast<T16*>(out), T, n_head,
+                                                                   device_error_word());
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention_tc(gpt2_dtype dt, const void* qkv, void* out, int B, int T, int n_head,
+                                cudaStream_t stream) {
+  if (dt == GPT2_F16) return launch_t<__half>(qkv, out, B, T, n_head, stream);
+  return launch_t<__nv_bfloat16>(qkv, out, B, T, n_head, stream);
 }
 
 }  // namespace gpt2

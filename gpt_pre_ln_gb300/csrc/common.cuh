@@ -9,6 +9,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -53,10 +54,38 @@ __device__ __forceinline__ float bf16_to_f32(__nv_bfloat16 v) { return __bfloat1
 template <typename T> __device__ __forceinline__ float to_f32(T v);
 template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
 template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <> __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
 
 template <typename T> __device__ __forceinline__ T from_f32(float v);
 template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
+
+// 16-bit storage types of the tensor-core paths: bf16 (the BF16 path) and
+// fp16 (the F16 path).  kFormat is the A/B format field of a kind::f16
+// instruction descriptor; pack2 / unpack2 convert two fp32 values to and
+// from one 32-bit word (round to nearest even, low half = first value).
+template <typename T> struct Type16;
+template <> struct Type16<__nv_bfloat16> {
+  static constexpr uint32_t kFormat = 1;
+  static constexpr CUtensorMapDataType kTma = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  static __device__ __forceinline__ uint32_t pack2(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  static __device__ __forceinline__ float2 unpack2(uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w));
+  }
+};
+template <> struct Type16<__half> {
+  static constexpr uint32_t kFormat = 0;
+  static constexpr CUtensorMapDataType kTma = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  static __device__ __forceinline__ uint32_t pack2(float a, float b) {
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  static __device__ __forceinline__ float2 unpack2(uint32_t w) { return __half22float2(*reinterpret_cast<__half2*>(&w)); }
+};
 
 // gelu_new(x) = 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
 __device__ __forceinline__ float gelu_new_accurate(float x) {
@@ -318,13 +347,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16.
-//   bits 4-5 D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format;
-//   bit 15 A major (0 = K-major); bit 16 B major (1 = MN-major);
-//   bits 17-22 N >> 3; bits 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+// Instruction descriptor, kind::f16: D fp32, A and B of one 16-bit format.
+//   bits 4-5 D format (1 = f32); 7-9 A format (0 = f16, 1 = bf16); 10-12
+//   B format (the same); bit 15 A major (0 = K-major); bit 16 B major
+//   (1 = MN-major); bits 17-22 N >> 3; bits 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(int M, int N, bool a_mn_major, bool b_mn_major,
+                                                         uint32_t fmt) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return idesc_f16kind_f32(M, N, a_mn_major, b_mn_major, 1u);
 }
 
 }  // namespace gpt2

@@ -1,9 +1,9 @@
-// Kernels of the KV-cache decode step (bf16 path).
+// Kernels of the KV-cache decode step (16-bit paths: bf16 or fp16 storage).
 //
 // "逐行拆GPT-2源码", GPT2Model / GPT2Attention: with past_key_values the
 // new token's position is past_length; its k, v are concatenated after the
 // cached ones along the sequence axis and its query attends over all of
-// them.  Here the cache is a preallocated [L, 2, B, H, T_max, 64] bf16 arena
+// them.  Here the cache is a preallocated [L, 2, B, H, T_max, 64] 16-bit arena
 // and "concatenate" is a write into slot past_len[b].  The next token is the
 // argmax of the tied lm_head scores (huaweicloud page, section 九), lowest
 // index on ties.
@@ -28,11 +28,12 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // One warp per sequence: valid[b] = position and token in range;
 // x = wte[token] + wpe[pos]; y = LN(x).
+template <typename T16>
 __global__ void decode_embed_ln(const int32_t* __restrict__ tokens, const int32_t* __restrict__ past_len,
-                                const __nv_bfloat16* __restrict__ wte, const __nv_bfloat16* __restrict__ wpe,
-                                const __nv_bfloat16* __restrict__ gamma, const __nv_bfloat16* __restrict__ beta,
-                                float* __restrict__ x, __nv_bfloat16* __restrict__ y, int B, int D, int V, int n_pos,
-                                int T_max, float eps, int* __restrict__ valid, unsigned* err) {
+                                const T16* __restrict__ wte, const T16* __restrict__ wpe,
+                                const T16* __restrict__ gamma, const T16* __restrict__ beta, float* __restrict__ x,
+                                T16* __restrict__ y, int B, int D, int V, int n_pos, int T_max, float eps,
+                                int* __restrict__ valid, unsigned* err) {
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (b >= B) return;
   const int lane = threadIdx.x & 31;
@@ -46,12 +47,12 @@ __global__ void decode_embed_ln(const int32_t* __restrict__ tokens, const int32_
     if (!tok_ok) record_error(err, kErrRange, kSiteDecodeToken);
   }
   const bool ok = pos_ok && tok_ok;
-  const __nv_bfloat16* er = wte + static_cast<long long>(ok ? tok : 0) * D;
-  const __nv_bfloat16* pr = wpe + static_cast<long long>(ok ? pos : 0) * D;
+  const T16* er = wte + static_cast<long long>(ok ? tok : 0) * D;
+  const T16* pr = wpe + static_cast<long long>(ok ? pos : 0) * D;
   float* xr = x + static_cast<long long>(b) * D;
   float s = 0.f;
   for (int c = lane; c < D; c += 32) {
-    const float v = ok ? (__bfloat162float(er[c]) + __bfloat162float(pr[c])) : 0.f;
+    const float v = ok ? (to_f32<T16>(er[c]) + to_f32<T16>(pr[c])) : 0.f;
     xr[c] = v;
     s += v;
   }
@@ -62,9 +63,9 @@ __global__ void decode_embed_ln(const int32_t* __restrict__ tokens, const int32_
     q = fmaf(d, d, q);
   }
   const float rstd = rsqrtf(warp_sum(q) / D + eps);
-  __nv_bfloat16* yr = y + static_cast<long long>(b) * D;
+  T16* yr = y + static_cast<long long>(b) * D;
   for (int c = lane; c < D; c += 32)
-    yr[c] = __float2bfloat16_rn((xr[c] - mean) * rstd * __bfloat162float(gamma[c]) + __bfloat162float(beta[c]));
+    yr[c] = from_f32<T16>((xr[c] - mean) * rstd * to_f32<T16>(gamma[c]) + to_f32<T16>(beta[c]));
 }
 
 // One CTA per (b, h): append k, v of the new token at slot pos, then
@@ -72,8 +73,9 @@ __global__ void decode_embed_ln(const int32_t* __restrict__ tokens, const int32_
 // contiguous range of slots; within a warp 8 lanes share one key (16 bytes
 // of the 128-byte row each), 4 keys per step; online softmax per lane group,
 // merged across groups and warps at the end.
+template <typename T16>
 __global__ void __launch_bounds__(kDecThreads)
-    decode_attn(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16* kv_layer, __nv_bfloat16* __restrict__ out,
+    decode_attn(const T16* __restrict__ qkv, T16* kv_layer, T16* __restrict__ out,
                 const int32_t* __restrict__ past_len, const int* __restrict__ valid, int B, int H, int T_max) {
   __shared__ float s_m[kDecThreads / 8], s_l[kDecThreads / 8];
   __shared__ float s_acc[kDecThreads / 8][kHd];
@@ -83,14 +85,14 @@ __global__ void __launch_bounds__(kDecThreads)
   const int D = H * kHd;
   const int tid = threadIdx.x;
   if (!valid[b]) {
-    if (tid < kHd) out[static_cast<long long>(b) * D + h * kHd + tid] = __float2bfloat16_rn(0.f);
+    if (tid < kHd) out[static_cast<long long>(b) * D + h * kHd + tid] = from_f32<T16>(0.f);
     return;
   }
   const int pos = past_len[b];
-  const __nv_bfloat16* row = qkv + static_cast<long long>(b) * 3 * D;
+  const T16* row = qkv + static_cast<long long>(b) * 3 * D;
   const long long kv_stride = static_cast<long long>(B) * H * T_max * kHd;  // K block -> V block
-  __nv_bfloat16* kc = kv_layer + (static_cast<long long>(b) * H + h) * T_max * kHd;
-  __nv_bfloat16* vc = kc + kv_stride;
+  T16* kc = kv_layer + (static_cast<long long>(b) * H + h) * T_max * kHd;
+  T16* vc = kc + kv_stride;
   if (tid < kHd) {
     kc[static_cast<long long>(pos) * kHd + tid] = row[D + h * kHd + tid];
     vc[static_cast<long long>(pos) * kHd + tid] = row[2 * D + h * kHd + tid];
@@ -104,10 +106,10 @@ __global__ void __launch_bounds__(kDecThreads)
   float q[8];
   {
     uint4 u = *reinterpret_cast<const uint4*>(row + h * kHd + sub * 8);
-    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
+    const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      float2 f = __bfloat1622float2(p[e]);
+      float2 f = Type16<T16>::unpack2(uw[e]);
       q[2 * e] = f.x * 0.125f;  // fold 1/sqrt(64) into q
       q[2 * e + 1] = f.y * 0.125f;
     }
@@ -125,6 +127,7 @@ __global__ void __launch_bounds__(kDecThreads)
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int j = j0 + u * 4 + grp;
+      kr[u] = vr[u] = make_uint4(0u, 0u, 0u, 0u);
       if (j < j_end) {
         kr[u] = *reinterpret_cast<const uint4*>(kc + static_cast<long long>(j) * kHd + sub * 8);
         vr[u] = *reinterpret_cast<const uint4*>(vc + static_cast<long long>(j) * kHd + sub * 8);
@@ -133,11 +136,11 @@ __global__ void __launch_bounds__(kDecThreads)
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int j = j0 + u * 4 + grp;
-      const __nv_bfloat162* kp = reinterpret_cast<const __nv_bfloat162*>(&kr[u]);
+      const uint32_t kw[4] = {kr[u].x, kr[u].y, kr[u].z, kr[u].w};
       float d = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        float2 f = __bfloat1622float2(kp[e]);
+        float2 f = Type16<T16>::unpack2(kw[e]);
         d = fmaf(q[2 * e], f.x, d);
         d = fmaf(q[2 * e + 1], f.y, d);
       }
@@ -149,10 +152,10 @@ __global__ void __launch_bounds__(kDecThreads)
         const float alpha = __expf(m - m_new);
         const float p = __expf(d - m_new);
         l = l * alpha + p;
-        const __nv_bfloat162* vp = reinterpret_cast<const __nv_bfloat162*>(&vr[u]);
+        const uint32_t vw[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          float2 f = __bfloat1622float2(vp[e]);
+          float2 f = Type16<T16>::unpack2(vw[e]);
           acc[2 * e] = fmaf(p, f.x, acc[2 * e] * alpha);
           acc[2 * e + 1] = fmaf(p, f.y, acc[2 * e + 1] * alpha);
         }
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(kDecThreads)
       L += s_l[i] * w;
       A += s_acc[i][tid] * w;
     }
-    out[static_cast<long long>(b) * D + h * kHd + tid] = __float2bfloat16_rn(A / L);
+    out[static_cast<long long>(b) * D + h * kHd + tid] = from_f32<T16>(A / L);
   }
 }
 
@@ -231,21 +234,39 @@ __global__ void __launch_bounds__(1024) argmax_rows(const float* __restrict__ lo
 
 }  // namespace
 
-cudaError_t launch_decode_embed_ln(const int32_t* tokens, const int32_t* past_len, const __nv_bfloat16* wte,
-                                   const __nv_bfloat16* wpe, const __nv_bfloat16* gamma, const __nv_bfloat16* beta,
-                                   float* x, __nv_bfloat16* y, int B, int D, int V, int n_pos, int T_max, float eps,
-                                   int* valid, cudaStream_t stream) {
+cudaError_t launch_decode_embed_ln(gpt2_dtype dt, const int32_t* tokens, const int32_t* past_len, const void* wte,
+                                   const void* wpe, const void* gamma, const void* beta, float* x, void* y, int B,
+                                   int D, int V, int n_pos, int T_max, float eps, int* valid, cudaStream_t stream) {
   const int warps = 4;
-  decode_embed_ln<<<(B + warps - 1) / warps, warps * 32, 0, stream>>>(tokens, past_len, wte, wpe, gamma, beta, x, y,
-                                                                      B, D, V, n_pos, T_max, eps, valid,
-                                                                      device_error_word());
+  const dim3 grid((B + warps - 1) / warps), block(warps * 32);
+  unsigned* err = device_error_word();
+  if (dt == GPT2_F16) {
+    using T = __half;
+    decode_embed_ln<T><<<grid, block, 0, stream>>>(tokens, past_len, static_cast<const T*>(wte),
+                                                   static_cast<const T*>(wpe), static_cast<const T*>(gamma),
+                                                   static_cast<const T*>(beta), x, static_cast<T*>(y), B, D, V, n_pos,
+                                                   T_max, eps, valid, err);
+  } else {
+    using T = __nv_bfloat16;
+    decode_embed_ln<T><<<grid, block, 0, stream>>>(tokens, past_len, static_cast<const T*>(wte),
+                                                   static_cast<const T*>(wpe), static_cast<const T*>(gamma),
+                                                   static_cast<const T*>(beta), x, static_cast<T*>(y), B, D, V, n_pos,
+                                                   T_max, eps, valid, err);
+  }
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode_attention(const __nv_bfloat16* qkv, __nv_bfloat16* kv_layer, __nv_bfloat16* out,
-                                    const int32_t* past_len, const int* valid, int B, int n_head, int T_max,
-                                    cudaStream_t stream) {
-  decode_attn<<<B * n_head, kDecThreads, 0, stream>>>(qkv, kv_layer, out, past_len, valid, B, n_head, T_max);
+cudaError_t launch_decode_attention(gpt2_dtype dt, const void* qkv, void* kv_layer, void* out, const int32_t* past_len,
+                                    const int* valid, int B, int n_head, int T_max, cudaStream_t stream) {
+  if (dt == GPT2_F16) {
+    using T = __half;
+    decode_attn<T><<<B * n_head, kDecThreads, 0, stream>>>(static_cast<const T*>(qkv), static_cast<T*>(kv_layer),
+                                                           static_cast<T*>(out), past_len, valid, B, n_head, T_max);
+  } else {
+    using T = __nv_bfloat16;
+    decode_attn<T><<<B * n_head, kDecThreads, 0, stream>>>(static_cast<const T*>(qkv), static_cast<T*>(kv_layer),
+                                                           static_cast<T*>(out), past_len, valid, B, n_head, T_max);
+  }
   return cudaGetLastError();
 }
 

@@ -88,42 +88,43 @@ struct OutTraits {
   static constexpr int LD = CW / 32;            // tcgen05.ld x32 per chunk
 };
 
-template <int EPI, typename OutT>
-__device__ __forceinline__ void apply_bias_act(float (&v)[OutTraits<OutT>::CW], const __nv_bfloat16* __restrict__ bias,
+template <int EPI, typename OutT, typename T16>
+__device__ __forceinline__ void apply_bias_act(float (&v)[OutTraits<OutT>::CW], const T16* __restrict__ bias,
                                                int col0, int N) {
   constexpr int CW = OutTraits<OutT>::CW;
-  if constexpr (EPI == EPI_NONE) return;
+  if constexpr (EPI != EPI_NONE) {
 #pragma unroll
-  for (int q = 0; q < CW / 8; ++q) {
-    const int c = col0 + q * 8;
-    float b[8];
-    if (c + 8 <= N) {
-      uint4 u = __ldg(reinterpret_cast<const uint4*>(bias + c));
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+    for (int q = 0; q < CW / 8; ++q) {
+      const int c = col0 + q * 8;
+      float b[8];
+      if (c + 8 <= N) {
+        uint4 u = __ldg(reinterpret_cast<const uint4*>(bias + c));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float2 f = __bfloat1622float2(h[e]);
-        b[2 * e] = f.x;
-        b[2 * e + 1] = f.y;
+        for (int e = 0; e < 4; ++e) {
+          float2 f = Type16<T16>::unpack2(w[e]);
+          b[2 * e] = f.x;
+          b[2 * e + 1] = f.y;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) b[e] = (c + e < N) ? to_f32<T16>(bias[c + e]) : 0.f;
       }
-    } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) b[e] = (c + e < N) ? __bfloat162float(bias[c + e]) : 0.f;
+      for (int e = 0; e < 8; ++e) v[q * 8 + e] += b[e];
     }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[q * 8 + e] += b[e];
   }
-  // bf16 outputs: one hardware tanh per element (absolute error below 2^-11,
-  // under the bf16 rounding that follows); fp32 outputs: tanhf
-  if (EPI == EPI_GELU) {
+  // 16-bit outputs: one hardware tanh per element (absolute error below
+  // 2^-11, under the rounding that follows); fp32 outputs: tanhf
+  if constexpr (EPI == EPI_GELU) {
 #pragma unroll
     for (int i = 0; i < CW; ++i) v[i] = (sizeof(OutT) == 2) ? gelu_new_fast(v[i]) : gelu_new_accurate(v[i]);
   }
 }
 
-template <typename OutT>
+template <typename OutT, typename T16>
 struct EpiArgs {
-  const __nv_bfloat16* bias;
+  const T16* bias;
   const float* residual;
   OutT* out;
   long long ldo;
@@ -137,8 +138,8 @@ struct EpiArgs {
 // accumulator columns of a tile, every thread arrives once on the tile's
 // accumulator-empty barrier: locally, or at a cluster address when
 // CLUSTER_ARRIVE (the barrier of the pair's even CTA).
-template <int BN, int EPI, typename OutT, bool CLUSTER_ARRIVE>
-__device__ __forceinline__ void epilogue_role(const EpiArgs<OutT>& a, int warp, int lane, uint32_t stage_base,
+template <int BN, int EPI, typename OutT, typename T16, bool CLUSTER_ARRIVE>
+__device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, int warp, int lane, uint32_t stage_base,
                                               uint32_t tmem_base, uint32_t tfull0, uint32_t tfull1, uint32_t tempty0,
                                               uint32_t tempty1, int tile_begin, int tile_stride, int num_tiles,
                                               int m_units, int unit_rows, int row_off) {
@@ -204,7 +205,7 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT>& a, int warp, 
         }
       }
       if (c == last_c) release();  // this half has read its last columns
-      apply_bias_act<EPI, OutT>(v, a.bias, col0, N);
+      apply_bias_act<EPI, OutT, T16>(v, a.bias, col0, N);
       if (EPI == EPI_RES) {
         // transpose the residual through the staging area: row = lane
 #pragma unroll
@@ -231,14 +232,10 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT>& a, int warp, 
       for (int j = 0; j < 8; ++j) {
         uint32_t w0, w1, w2, w3;
         if constexpr (sizeof(OutT) == 2) {
-          __nv_bfloat162 p0 = __floats2bfloat162_rn(v[8 * j], v[8 * j + 1]);
-          __nv_bfloat162 p1 = __floats2bfloat162_rn(v[8 * j + 2], v[8 * j + 3]);
-          __nv_bfloat162 p2 = __floats2bfloat162_rn(v[8 * j + 4], v[8 * j + 5]);
-          __nv_bfloat162 p3 = __floats2bfloat162_rn(v[8 * j + 6], v[8 * j + 7]);
-          w0 = *reinterpret_cast<uint32_t*>(&p0);
-          w1 = *reinterpret_cast<uint32_t*>(&p1);
-          w2 = *reinterpret_cast<uint32_t*>(&p2);
-          w3 = *reinterpret_cast<uint32_t*>(&p3);
+          w0 = Type16<OutT>::pack2(v[8 * j], v[8 * j + 1]);
+          w1 = Type16<OutT>::pack2(v[8 * j + 2], v[8 * j + 3]);
+          w2 = Type16<OutT>::pack2(v[8 * j + 4], v[8 * j + 5]);
+          w3 = Type16<OutT>::pack2(v[8 * j + 6], v[8 * j + 7]);
         } else {
           w0 = __float_as_uint(v[4 * j]);
           w1 = __float_as_uint(v[4 * j + 1]);
@@ -288,10 +285,10 @@ __device__ __forceinline__ void drain_loads(long long issued, FullBar full_bar, 
 }
 
 // ------------------------------------------------------------------ 1 SM
-template <int BN, bool B_MN, int EPI, typename OutT>
+template <int BN, bool B_MN, int EPI, typename OutT, typename T16>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_1sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-             const EpiArgs<OutT> ea, int K) {
+             const EpiArgs<OutT, T16> ea, int K) {
   using Cfg = GemmCfg<BN, BN>;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -378,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, false, B_MN);
+      constexpr uint32_t idesc = idesc_f16kind_f32(kBM, BN, false, B_MN, Type16<T16>::kFormat);
       int stage = 0;
       uint32_t phase = 0;
       int t_local = 0;
@@ -433,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    epilogue_role<BN, EPI, OutT, false>(ea, warp, lane, smem_u32(sOut), tmem_base, tfull_bar(0), tfull_bar(1),
+    epilogue_role<BN, EPI, OutT, T16, false>(ea, warp, lane, smem_u32(sOut), tmem_base, tfull_bar(0), tfull_bar(1),
                                          tempty_bar(0), tempty_bar(1), blockIdx.x, gridDim.x, num_tiles, m_tiles, kBM,
                                          0);
   }
@@ -449,10 +446,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------ CTA pair
 constexpr int kPairBN = 256;
 
-template <bool B_MN, int EPI, typename OutT>
+template <bool B_MN, int EPI, typename OutT, typename T16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-             const EpiArgs<OutT> ea, int K) {
+             const EpiArgs<OutT, T16> ea, int K) {
   using Cfg = GemmCfg<kPairBN, kPairBN / 2>;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -543,7 +540,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ------------------------------------------------ pair MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, kPairBN, false, B_MN);
+      constexpr uint32_t idesc = idesc_f16kind_f32(2 * kBM, kPairBN, false, B_MN, Type16<T16>::kFormat);
       constexpr uint16_t kBoth = 0x3;
       int stage = 0;
       uint32_t phase = 0;
@@ -595,7 +592,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    epilogue_role<kPairBN, EPI, OutT, true>(ea, warp, lane, smem_u32(sOut), tmem_base, tfull_bar(0), tfull_bar(1),
+    epilogue_role<kPairBN, EPI, OutT, T16, true>(ea, warp, lane, smem_u32(sOut), tmem_base, tfull_bar(0), tfull_bar(1),
                                             mapa_shared(tempty_bar(0), 0), mapa_shared(tempty_bar(1), 0), pair,
                                             num_pairs, num_tiles, m_units, 2 * kBM, static_cast<int>(rank) * kBM);
   }
@@ -629,16 +626,17 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major bf16 [outer, inner] matrix; boxes of [box_outer, 64] elements,
+// Row-major 16-bit [outer, inner] matrix; boxes of [box_outer, 64] elements,
 // 128-byte swizzle.
-bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+bool make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+              uint32_t box_outer) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * 2};
   cuuint32_t box[2] = {64, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -656,36 +654,37 @@ cudaError_t set_smem_once(Kern kern, int bytes, int (&configured)[64]) {
   return cudaSuccess;
 }
 
-template <int BN, bool B_MN, int EPI, typename OutT>
-cudaError_t run_1sm(const __nv_bfloat16* x, const __nv_bfloat16* w, const EpiArgs<OutT>& ea, int K,
-                    cudaStream_t stream) {
+template <int BN, bool B_MN, int EPI, typename OutT, typename T16>
+cudaError_t run_1sm(const T16* x, const T16* w, const EpiArgs<OutT, T16>& ea, int K, cudaStream_t stream) {
   using Cfg = GemmCfg<BN, BN>;
-  auto kern = gemm_1sm<BN, B_MN, EPI, OutT>;
+  auto kern = gemm_1sm<BN, B_MN, EPI, OutT, T16>;
+  constexpr CUtensorMapDataType dt = Type16<T16>::kTma;
   static int configured[64] = {0};
   cudaError_t e = set_smem_once(kern, Cfg::SMEM_BYTES, configured);
   if (e != cudaSuccess) return e;
   const int M = ea.M, N = ea.N;
   CUtensorMap ta, tb;
-  if (!make_map(&ta, x, K, M, kBM)) return cudaErrorInvalidValue;
-  if (!(B_MN ? make_map(&tb, w, N, K, kBK) : make_map(&tb, w, K, N, BN))) return cudaErrorInvalidValue;
+  if (!make_map(&ta, dt, x, K, M, kBM)) return cudaErrorInvalidValue;
+  if (!(B_MN ? make_map(&tb, dt, w, N, K, kBK) : make_map(&tb, dt, w, K, N, BN))) return cudaErrorInvalidValue;
   const int tiles = ((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
   kern<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, ea, K);
   return cudaGetLastError();
 }
 
-template <bool B_MN, int EPI, typename OutT>
-cudaError_t run_2sm(const __nv_bfloat16* x, const __nv_bfloat16* w, const EpiArgs<OutT>& ea, int K,
-                    cudaStream_t stream) {
+template <bool B_MN, int EPI, typename OutT, typename T16>
+cudaError_t run_2sm(const T16* x, const T16* w, const EpiArgs<OutT, T16>& ea, int K, cudaStream_t stream) {
   using Cfg = GemmCfg<kPairBN, kPairBN / 2>;
-  auto kern = gemm_2sm<B_MN, EPI, OutT>;
+  auto kern = gemm_2sm<B_MN, EPI, OutT, T16>;
+  constexpr CUtensorMapDataType dt = Type16<T16>::kTma;
   static int configured[64] = {0};
   cudaError_t e = set_smem_once(kern, Cfg::SMEM_BYTES, configured);
   if (e != cudaSuccess) return e;
   const int M = ea.M, N = ea.N;
   CUtensorMap ta, tb;
-  if (!make_map(&ta, x, K, M, kBM)) return cudaErrorInvalidValue;
-  if (!(B_MN ? make_map(&tb, w, N, K, kBK) : make_map(&tb, w, K, N, kPairBN / 2))) return cudaErrorInvalidValue;
+  if (!make_map(&ta, dt, x, K, M, kBM)) return cudaErrorInvalidValue;
+  if (!(B_MN ? make_map(&tb, dt, w, N, K, kBK) : make_map(&tb, dt, w, K, N, kPairBN / 2)))
+    return cudaErrorInvalidValue;
   // pairs that can be resident at once (a pair needs two SMs of one GPC)
   static int max_pairs[64] = {0};
   int dev = 0;
@@ -744,53 +743,61 @@ int pick_variant(int M, int N) {
 #endif
 }
 
-template <bool B_MN, int EPI, typename OutT>
-cudaError_t run_variant(int v, const __nv_bfloat16* x, const __nv_bfloat16* w, const EpiArgs<OutT>& ea, int K,
-                        cudaStream_t s) {
+template <bool B_MN, int EPI, typename OutT, typename T16>
+cudaError_t run_variant(int v, const T16* x, const T16* w, const EpiArgs<OutT, T16>& ea, int K, cudaStream_t s) {
   switch (v) {
-    case 0: return run_2sm<B_MN, EPI, OutT>(x, w, ea, K, s);
-    case 128: return run_1sm<128, B_MN, EPI, OutT>(x, w, ea, K, s);
-    case 192: return run_1sm<192, B_MN, EPI, OutT>(x, w, ea, K, s);
-    default: return run_1sm<256, B_MN, EPI, OutT>(x, w, ea, K, s);
+    case 0: return run_2sm<B_MN, EPI, OutT, T16>(x, w, ea, K, s);
+    case 128: return run_1sm<128, B_MN, EPI, OutT, T16>(x, w, ea, K, s);
+    case 192: return run_1sm<192, B_MN, EPI, OutT, T16>(x, w, ea, K, s);
+    default: return run_1sm<256, B_MN, EPI, OutT, T16>(x, w, ea, K, s);
   }
 }
 
-template <bool B_MN>
-cudaError_t dispatch(int v, const __nv_bfloat16* x, const __nv_bfloat16* w, const __nv_bfloat16* bias,
-                     const float* residual, void* y, int M, int N, int K, long long ldy, int epi, gpt2_dtype y_t,
-                     cudaStream_t s) {
-  using bf = __nv_bfloat16;
+template <bool B_MN, typename T16>
+cudaError_t dispatch(int v, const T16* x, const T16* w, const T16* bias, const float* residual, void* y, int M, int N,
+                     int K, long long ldy, int epi, gpt2_dtype y_t, cudaStream_t s) {
   unsigned* err = device_error_word();
   if (epi == EPI_RES) {
-    EpiArgs<float> ea{bias, residual, static_cast<float*>(y), ldy, M, N, err};
-    return run_variant<B_MN, EPI_RES, float>(v, x, w, ea, K, s);
+    EpiArgs<float, T16> ea{bias, residual, static_cast<float*>(y), ldy, M, N, err};
+    return run_variant<B_MN, EPI_RES, float, T16>(v, x, w, ea, K, s);
   }
-  if (y_t == GPT2_BF16) {
-    EpiArgs<bf> ea{bias, residual, static_cast<bf*>(y), ldy, M, N, err};
+  if (y_t != GPT2_F32) {
+    EpiArgs<T16, T16> ea{bias, residual, static_cast<T16*>(y), ldy, M, N, err};
     switch (epi) {
-      case EPI_NONE: return run_variant<B_MN, EPI_NONE, bf>(v, x, w, ea, K, s);
-      case EPI_BIAS: return run_variant<B_MN, EPI_BIAS, bf>(v, x, w, ea, K, s);
-      default: return run_variant<B_MN, EPI_GELU, bf>(v, x, w, ea, K, s);
+      case EPI_NONE: return run_variant<B_MN, EPI_NONE, T16, T16>(v, x, w, ea, K, s);
+      case EPI_BIAS: return run_variant<B_MN, EPI_BIAS, T16, T16>(v, x, w, ea, K, s);
+      default: return run_variant<B_MN, EPI_GELU, T16, T16>(v, x, w, ea, K, s);
     }
   }
-  EpiArgs<float> ea{bias, residual, static_cast<float*>(y), ldy, M, N, err};
+  EpiArgs<float, T16> ea{bias, residual, static_cast<float*>(y), ldy, M, N, err};
   switch (epi) {
-    case EPI_NONE: return run_variant<B_MN, EPI_NONE, float>(v, x, w, ea, K, s);
-    case EPI_BIAS: return run_variant<B_MN, EPI_BIAS, float>(v, x, w, ea, K, s);
-    default: return run_variant<B_MN, EPI_GELU, float>(v, x, w, ea, K, s);
+    case EPI_NONE: return run_variant<B_MN, EPI_NONE, float, T16>(v, x, w, ea, K, s);
+    case EPI_BIAS: return run_variant<B_MN, EPI_BIAS, float, T16>(v, x, w, ea, K, s);
+    default: return run_variant<B_MN, EPI_GELU, float, T16>(v, x, w, ea, K, s);
   }
+}
+
+template <typename T16>
+cudaError_t launch(const void* x, const void* w, const void* bias, const float* residual, void* y, int64_t M, int N,
+                   int K, int64_t ldy, bool w_out_in, int epilogue, gpt2_dtype y_t, cudaStream_t stream) {
+  if (M == 0) return cudaSuccess;
+  const int m = static_cast<int>(M);
+  const int v = pick_variant(m, N);
+  const T16* X = static_cast<const T16*>(x);
+  const T16* W = static_cast<const T16*>(w);
+  const T16* Bv = static_cast<const T16*>(bias);
+  return w_out_in ? dispatch<false, T16>(v, X, W, Bv, residual, y, m, N, K, ldy, epilogue, y_t, stream)
+                  : dispatch<true, T16>(v, X, W, Bv, residual, y, m, N, K, ldy, epilogue, y_t, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_bf16(const __nv_bfloat16* x, const __nv_bfloat16* w, const __nv_bfloat16* bias,
-                             const float* residual, void* y, int64_t M, int N, int K, int64_t ldy, bool w_out_in,
-                             int epilogue, gpt2_dtype y_t, cudaStream_t stream) {
-  if (M == 0) return cudaSuccess;
-  const int m = static_cast<int>(M);
-  const int v = pick_variant(m, N);
-  return w_out_in ? dispatch<false>(v, x, w, bias, residual, y, m, N, K, ldy, epilogue, y_t, stream)
-                  : dispatch<true>(v, x, w, bias, residual, y, m, N, K, ldy, epilogue, y_t, stream);
+cudaError_t launch_gemm_16(gpt2_dtype dt, const void* x, const void* w, const void* bias, const float* residual,
+                           void* y, int64_t M, int N, int K, int64_t ldy, bool w_out_in, int epilogue, gpt2_dtype y_t,
+                           cudaStream_t stream) {
+  if (dt == GPT2_F16)
+    return launch<__half>(x, w, bias, residual, y, M, N, K, ldy, w_out_in, epilogue, y_t, stream);
+  return launch<__nv_bfloat16>(x, w, bias, residual, y, M, N, K, ldy, w_out_in, epilogue, y_t, stream);
 }
 
 }  // namespace gpt2

@@ -25,30 +25,28 @@ cudaError_t launch_embed_ln(const int32_t* tokens, const void* wte, const void* 
                             const void* beta, float* x, void* y, int B, int T, int D, int V, float eps, gpt2_dtype dt,
                             cudaStream_t stream);
 
-// bf16 tensor-core GEMM with a fused epilogue (tcgen05 + TMA).
-cudaError_t launch_gemm_bf16(const __nv_bfloat16* x, const __nv_bfloat16* w, const __nv_bfloat16* bias,
-                             const float* residual, void* y, int64_t M, int N, int K, int64_t ldy, bool w_out_in,
-                             int epilogue, gpt2_dtype y_t, cudaStream_t stream);
+// 16-bit tensor-core GEMM with a fused epilogue (tcgen05 + TMA); dt is
+// GPT2_BF16 or GPT2_F16 (x, w, bias of that type), y_t is dt or GPT2_F32.
+cudaError_t launch_gemm_16(gpt2_dtype dt, const void* x, const void* w, const void* bias, const float* residual,
+                           void* y, int64_t M, int N, int K, int64_t ldy, bool w_out_in, int epilogue, gpt2_dtype y_t,
+                           cudaStream_t stream);
 
 // fp32 CUDA-core GEMM with the same epilogues.
 cudaError_t launch_gemm_f32(const float* x, const float* w, const float* bias, const float* residual, float* y,
                             int64_t M, int N, int K, int64_t ldy, bool w_out_in, int epilogue, cudaStream_t stream);
 
-cudaError_t launch_attention_bf16(const __nv_bfloat16* qkv, __nv_bfloat16* out, int B, int T, int n_head,
-                                  cudaStream_t stream);
-// tcgen05 version (S and O in tensor memory), head_dim 64.
-cudaError_t launch_attention_bf16_tc(const __nv_bfloat16* qkv, __nv_bfloat16* out, int B, int T, int n_head,
-                                     cudaStream_t stream);
+// tcgen05 version (S and O in tensor memory), head_dim 64; dt GPT2_BF16 or
+// GPT2_F16.
+cudaError_t launch_attention_tc(gpt2_dtype dt, const void* qkv, void* out, int B, int T, int n_head,
+                                cudaStream_t stream);
 cudaError_t launch_attention_f32(const float* qkv, float* out, int B, int T, int n_head, cudaStream_t stream);
 
-// Decode-step kernels (bf16 path).
-cudaError_t launch_decode_embed_ln(const int32_t* tokens, const int32_t* past_len, const __nv_bfloat16* wte,
-                                   const __nv_bfloat16* wpe, const __nv_bfloat16* gamma, const __nv_bfloat16* beta,
-                                   float* x, __nv_bfloat16* y, int B, int D, int V, int n_pos, int T_max, float eps,
-                                   int* valid, cudaStream_t stream);
-cudaError_t launch_decode_attention(const __nv_bfloat16* qkv, __nv_bfloat16* kv_layer, __nv_bfloat16* out,
-                                    const int32_t* past_len, const int* valid, int B, int n_head, int T_max,
-                                    cudaStream_t stream);
+// Decode-step kernels (16-bit paths; dt GPT2_BF16 or GPT2_F16).
+cudaError_t launch_decode_embed_ln(gpt2_dtype dt, const int32_t* tokens, const int32_t* past_len, const void* wte,
+                                   const void* wpe, const void* gamma, const void* beta, float* x, void* y, int B,
+                                   int D, int V, int n_pos, int T_max, float eps, int* valid, cudaStream_t stream);
+cudaError_t launch_decode_attention(gpt2_dtype dt, const void* qkv, void* kv_layer, void* out, const int32_t* past_len,
+                                    const int* valid, int B, int n_head, int T_max, cudaStream_t stream);
 cudaError_t launch_argmax_rows(const float* logits, int64_t ld, int B, int V, const int* valid, int32_t* next_tokens,
                                int32_t* past_len, cudaStream_t stream);
 

@@ -37,6 +37,14 @@ __device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, flo
   v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
 }
 
+template <>
+__device__ __forceinline__ void load4<__half>(const __half* p, float (&v)[4]) {
+  uint2 u = *reinterpret_cast<const uint2*>(p);
+  float2 a = __half22float2(*reinterpret_cast<__half2*>(&u.x));
+  float2 b = __half22float2(*reinterpret_cast<__half2*>(&u.y));
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+
 template <typename T>
 __device__ __forceinline__ void store4(T* p, const float (&v)[4]);
 template <>
@@ -47,6 +55,16 @@ template <>
 __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, const float (&v)[4]) {
   __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
   __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+template <>
+__device__ __forceinline__ void store4<__half>(__half* p, const float (&v)[4]) {
+  __half2 a = __floats2half2_rn(v[0], v[1]);
+  __half2 b = __floats2half2_rn(v[2], v[3]);
   uint2 u;
   u.x = *reinterpret_cast<uint32_t*>(&a);
   u.y = *reinterpret_cast<uint32_t*>(&b);
@@ -67,6 +85,16 @@ template <> struct Raw4<__nv_bfloat16> {
   __device__ __forceinline__ float get(int e) const {
     const uint32_t w = e < 2 ? v.x : v.y;
     return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+  }
+};
+
+template <> struct Raw4<__half> {
+  uint2 v;
+  __device__ __forceinline__ void load(const __half* p) { v = *reinterpret_cast<const uint2*>(p); }
+  __device__ __forceinline__ float get(int e) const {
+    const uint32_t w = e < 2 ? v.x : v.y;
+    const unsigned short h = (e & 1) ? static_cast<unsigned short>(w >> 16) : static_cast<unsigned short>(w & 0xffffu);
+    return __half2float(__ushort_as_half(h));
   }
 };
 
@@ -222,16 +250,22 @@ cudaError_t embed_dispatch(const int32_t* tokens, const void* wte, const void* w
   return cudaGetLastError();
 }
 
+template <typename XT>
+cudaError_t ln_by_y(const void* x, const void* g, const void* b, void* y, long long rows, int D, float eps,
+                    gpt2_dtype y_t, cudaStream_t s) {
+  if (y_t == GPT2_F32) return ln_dispatch<XT, float>(x, g, b, y, rows, D, eps, s);
+  if (y_t == GPT2_F16) return ln_dispatch<XT, __half>(x, g, b, y, rows, D, eps, s);
+  return ln_dispatch<XT, __nv_bfloat16>(x, g, b, y, rows, D, eps, s);
+}
+
 }  // namespace
 
 cudaError_t launch_layernorm(const void* x, const void* gamma, const void* beta, void* y, int64_t rows, int D,
                              float eps, gpt2_dtype x_t, gpt2_dtype y_t, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
-  using bf = __nv_bfloat16;
-  if (x_t == GPT2_F32 && y_t == GPT2_F32) return ln_dispatch<float, float>(x, gamma, beta, y, rows, D, eps, stream);
-  if (x_t == GPT2_F32 && y_t == GPT2_BF16) return ln_dispatch<float, bf>(x, gamma, beta, y, rows, D, eps, stream);
-  if (x_t == GPT2_BF16 && y_t == GPT2_F32) return ln_dispatch<bf, float>(x, gamma, beta, y, rows, D, eps, stream);
-  return ln_dispatch<bf, bf>(x, gamma, beta, y, rows, D, eps, stream);
+  if (x_t == GPT2_F32) return ln_by_y<float>(x, gamma, beta, y, rows, D, eps, y_t, stream);
+  if (x_t == GPT2_F16) return ln_by_y<__half>(x, gamma, beta, y, rows, D, eps, y_t, stream);
+  return ln_by_y<__nv_bfloat16>(x, gamma, beta, y, rows, D, eps, y_t, stream);
 }
 
 cudaError_t launch_embed_ln(const int32_t* tokens, const void* wte, const void* wpe, const void* gamma,
@@ -240,6 +274,7 @@ cudaError_t launch_embed_ln(const int32_t* tokens, const void* wte, const void* 
   const long long rows = static_cast<long long>(B) * T;
   if (rows == 0) return cudaSuccess;
   if (dt == GPT2_F32) return embed_dispatch<float>(tokens, wte, wpe, gamma, beta, x, y, rows, T, D, V, eps, stream);
+  if (dt == GPT2_F16) return embed_dispatch<__half>(tokens, wte, wpe, gamma, beta, x, y, rows, T, D, V, eps, stream);
   return embed_dispatch<__nv_bfloat16>(tokens, wte, wpe, gamma, beta, x, y, rows, T, D, V, eps, stream);
 }
 

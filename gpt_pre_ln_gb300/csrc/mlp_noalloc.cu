@@ -64,10 +64,10 @@ size_t gpt2_mlp_noalloc_max_scratch_bytes(void) { return kMlpScratchBytes; }
 int gpt2_mlp_noalloc(const void* x, const void* w_fc, const void* b_fc, const void* w_proj, const void* b_proj,
                      const float* residual, float* out, int64_t M, int D, int F, gpt2_dtype dtype,
                      gpt2_stream_t stream) {
-  if (dtype != GPT2_F32 && dtype != GPT2_BF16) return GPT2_ERR_ARG;
+  if (dtype != GPT2_F32 && dtype != GPT2_BF16 && dtype != GPT2_F16) return GPT2_ERR_ARG;
   if (M < 0 || D <= 0 || F <= 0) return GPT2_ERR_ARG;
   if (D % 64 != 0 || F % 64 != 0) return GPT2_ERR_UNSUPPORTED;
-  const size_t esz = dtype == GPT2_BF16 ? 2 : 4;
+  const size_t esz = dtype == GPT2_F32 ? 4 : 2;
   if (static_cast<size_t>(M) * static_cast<size_t>(F) * esz > kMlpScratchBytes) return GPT2_ERR_WORKSPACE;
   if (M == 0) return GPT2_OK;
   const void* ps[6] = {x, w_fc, b_fc, w_proj, b_proj, out};
@@ -78,14 +78,11 @@ int gpt2_mlp_noalloc(const void* x, const void* w_fc, const void* b_fc, const vo
   if (!g) return GPT2_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (dtype == GPT2_BF16) {
-    using bf = __nv_bfloat16;
-    e = launch_gemm_bf16(static_cast<const bf*>(x), static_cast<const bf*>(w_fc), static_cast<const bf*>(b_fc),
-                         nullptr, g, M, F, D, F, false, GPT2_EPI_BIAS_GELU, GPT2_BF16, s);
+  if (dtype != GPT2_F32) {
+    e = launch_gemm_16(dtype, x, w_fc, b_fc, nullptr, g, M, F, D, F, false, GPT2_EPI_BIAS_GELU, dtype, s);
     if (e != cudaSuccess) return GPT2_ERR_CUDA;
-    e = launch_gemm_bf16(static_cast<const bf*>(g), static_cast<const bf*>(w_proj), static_cast<const bf*>(b_proj),
-                         residual, out, M, D, F, D, false,
-                         residual ? GPT2_EPI_BIAS_RESIDUAL : GPT2_EPI_BIAS, GPT2_F32, s);
+    e = launch_gemm_16(dtype, g, w_proj, b_proj, residual, out, M, D, F, D, false,
+                       residual ? GPT2_EPI_BIAS_RESIDUAL : GPT2_EPI_BIAS, GPT2_F32, s);
   } else {
     e = launch_gemm_f32(static_cast<const float*>(x), static_cast<const float*>(w_fc),
                         static_cast<const float*>(b_fc), nullptr, static_cast<float*>(g), M, F, D, F, false,

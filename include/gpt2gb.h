@@ -34,7 +34,10 @@
  * Number types (gpt2_dtype): the BF16 path keeps weights, LayerNorm outputs,
  *   QKV, attention output and MLP hidden in bf16, accumulates in fp32 and
  *   keeps the residual stream, LayerNorm statistics and the softmax in fp32.
- *   The F32 path keeps everything in fp32.
+ *   The F16 path is the same with fp16 in place of bf16 (fp16 carries 3 more
+ *   mantissa bits; bf16 weights convert to fp16 exactly down to magnitude
+ *   2^-17, so a bf16 model runs on it unchanged in practice).  The F32 path
+ *   keeps everything in fp32.
  * Supported shapes: head_dim = d_model / n_head must be 64; d_model a
  *   multiple of 64; d_ff a multiple of 64; T <= n_pos.  Anything else returns
  *   GPT2_ERR_UNSUPPORTED (shape) or GPT2_ERR_ARG (a null or inconsistent
@@ -64,7 +67,7 @@ typedef enum {
   GPT2_ERR_RANGE = 6         /* device side: a token id or position out of range */
 } gpt2_status;
 
-typedef enum { GPT2_F32 = 0, GPT2_BF16 = 1 } gpt2_dtype;
+typedef enum { GPT2_F32 = 0, GPT2_BF16 = 1, GPT2_F16 = 2 } gpt2_dtype;
 
 /* Model hyper-parameters (GPT2Config on "逐行拆GPT-2源码": n_layer, n_embd,
  * n_head, n_inner = 4 * n_embd by default, vocab_size, n_positions,

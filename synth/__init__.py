@@ -24,7 +24,7 @@ Face GPT-2 code, "逐行拆GPT-2源码", GPT2Attention section), so
 ``y = x @ W + b``.
 
 Values are returned as ``np.float32`` arrays whose every element is exactly
-representable in the path dtype ("f32" or "bf16").  Rounding is float64 ->
+representable in the path dtype ("f32", "bf16" or "f16").  Rounding is float64 ->
 float32 (round to nearest even) and, for bf16, float32 -> bf16 (round to
 nearest even on the bit pattern).
 """
@@ -93,6 +93,8 @@ def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
     x32 = np.asarray(x, dtype=np.float64).astype(np.float32)
     if dtype == "f32":
         return x32
+    if dtype == "f16":
+        return x32.astype(np.float16).astype(np.float32)
     if dtype != "bf16":
         raise ValueError(f"unknown dtype {dtype!r}")
     bits = x32.view(np.uint32)
@@ -230,6 +232,14 @@ def workload_inputs(name: str, T_override: int | None = None, B_override: int | 
         out["T_max"] = T_max
         out["cache"] = draw_kv_cache(d, w.dims, B, T_max, w.cache_len)
         out["past_len"] = np.full((B,), w.cache_len, dtype=np.int32)
+    return out
+
+
+def convert_params(params: dict, dtype: str) -> dict:
+    """The same parameters rounded to another path dtype (e.g. a bf16 model's
+    weights as fp16 operands: exact for magnitudes from 2^-17 up)."""
+    out = {k: round_to(v, dtype) for k, v in params.items() if k != "blocks"}
+    out["blocks"] = [{k: round_to(v, dtype) for k, v in b.items()} for b in params["blocks"]]
     return out
 
 

@@ -18,10 +18,15 @@ def f32(a):
     return synth.round_to(a, "f32")
 
 
+def f16(a):
+    return synth.round_to(a, "f16")
+
+
 def to_t(a, dtype, device="cuda"):
     import torch
     t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
-    return t.to(torch.bfloat16 if dtype == "bf16" else torch.float32).contiguous()
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16}.get(dtype, torch.float32)
+    return t.to(tdt).contiguous()
 
 
 def to_np(t):
