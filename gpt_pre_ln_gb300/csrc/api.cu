@@ -447,6 +447,7 @@ int gpt2_decode_step(const gpt2_dims* dims, const gpt2_model_weights* w, void* k
   if (!is16(dims->dtype)) return GPT2_ERR_UNSUPPORTED;
   if (B < 0 || T_max <= 0) return GPT2_ERR_ARG;
   if (B == 0) return GPT2_OK;
+  if (2ll * B * dims->n_head * T_max >= (1ll << 31)) return GPT2_ERR_UNSUPPORTED;
   if (!kv_cache || !past_len || !tokens || !next_tokens || !aligned16(kv_cache)) return GPT2_ERR_ARG;
   if (logits_opt && (ld < dims->vocab || !aligned16(logits_opt))) return GPT2_ERR_ARG;
   if (logits_opt && ld % 4 != 0) return GPT2_ERR_UNSUPPORTED;

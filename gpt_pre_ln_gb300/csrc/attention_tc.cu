@@ -25,10 +25,6 @@
 //
 // Waits are bounded (common.cuh): a timeout records GPT2_ERR_TIMEOUT and the
 // roles unwind; tensor memory is freed on every path.
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "common.cuh"
 #include "internal.h"
 
@@ -327,38 +323,12 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   }
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
 template <typename T16>
 cudaError_t launch_t(const void* qkv, void* out, int B, int T, int n_head, cudaStream_t stream) {
   if (B == 0 || T == 0) return cudaSuccess;
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return cudaErrorInvalidValue;
   const uint64_t D = static_cast<uint64_t>(n_head) * kHd;
   CUtensorMap map;
-  cuuint64_t dims[2] = {3 * D, static_cast<cuuint64_t>(B) * T};
-  cuuint64_t strides[1] = {3 * D * 2};
-  cuuint32_t box[2] = {kHd, kTq};
-  cuuint32_t estr[2] = {1, 1};
-  if (fn(&map, Type16<T16>::kTma, 2, const_cast<void*>(qkv), dims, strides, box, estr,
-         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  if (!encode_tma_2d(&map, Type16<T16>::kTma, qkv, 3 * D, static_cast<uint64_t>(B) * T, 3 * D * 2, kHd, kTq))
     return cudaErrorInvalidValue;
   static int configured[64] = {0};
   int dev = 0;

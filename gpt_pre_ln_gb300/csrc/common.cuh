@@ -31,6 +31,7 @@ enum ErrSite : unsigned {
   kSiteEmbedToken = 10,
   kSiteDecodePos = 11,
   kSiteDecodeToken = 12,
+  kSiteDecodeAttn = 13,
 };
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
@@ -105,6 +106,27 @@ __device__ __forceinline__ float gelu_new_fast(float x) {
   float u = k0 * fmaf(0.044715f * x, x * x, x);
   float hx = 0.5f * x;
   return fmaf(hx, tanh_hw(u), hx);
+}
+
+// Two fp32 FMAs in one instruction (sm_100 family): d = a * b + c for each
+// half of the pair, rounded to nearest: the same results as two fmaf calls.
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -18,7 +18,6 @@ namespace gpt2 {
 namespace {
 
 constexpr int kHd = 64;
-constexpr int kDecThreads = 256;  // 8 warps per (b, h)
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -68,120 +67,188 @@ __global__ void decode_embed_ln(const int32_t* __restrict__ tokens, const int32_
     yr[c] = from_f32<T16>((xr[c] - mean) * rstd * to_f32<T16>(gamma[c]) + to_f32<T16>(beta[c]));
 }
 
-// One CTA per (b, h): append k, v of the new token at slot pos, then
-// out = softmax_j(q . k_j / 8) v_j over slots 0..pos.  Each warp takes a
-// contiguous range of slots; within a warp 8 lanes share one key (16 bytes
-// of the 128-byte row each), 4 keys per step; online softmax per lane group,
-// merged across groups and warps at the end.
+// Attention of the new token over the cache, one CTA of four warps per
+// (b, h).  The cached keys 0..pos-1 are cut into chunks of 16; warp w takes
+// chunks w, w+4, w+8, ...  Each warp double-buffers its chunks in shared
+// memory: its lane 0 loads a chunk's 16 K rows and 16 V rows as two TMA
+// boxes with the 128-byte swizzle (16-byte unit u of row r lands at unit
+// u ^ (r & 7)), which makes the reads below free of bank conflicts.
+// Scores take two lanes per key (32 dimensions each, one shuffle to add) and
+// live in log2 units (q carries log2(e) / sqrt(64)); the probabilities go
+// through shared memory to the P.V phase, where lane (par, dq) accumulates
+// dimensions 4dq..4dq+3 over the chunk's keys of parity par (the two halves
+// of the warp are added once at the end).  Each warp keeps an online-softmax
+// partial (running max, sum, accumulator); the new token's k, v are written
+// to cache slot pos and enter as one more partial from registers, so no load
+// of this launch reads a value it writes.
+constexpr int kDaWarps = 4;
+constexpr int kDaChunk = 16;
+constexpr int kDaStages = 2;
+constexpr int kDaBox = kDaChunk * kHd * 2;  // one box: 16 rows of 64 16-bit values
+constexpr int kDaStageBytes = 2 * kDaBox;   // K and V of one chunk
+constexpr int kDaSmem = kDaWarps * kDaStages * kDaStageBytes + 1024;  // + slack for 1024-byte alignment
+
 template <typename T16>
-__global__ void __launch_bounds__(kDecThreads)
-    decode_attn(const T16* __restrict__ qkv, T16* kv_layer, T16* __restrict__ out,
-                const int32_t* __restrict__ past_len, const int* __restrict__ valid, int B, int H, int T_max) {
-  __shared__ float s_m[kDecThreads / 8], s_l[kDecThreads / 8];
-  __shared__ float s_acc[kDecThreads / 8][kHd];
-  const int bh = blockIdx.x;
-  const int b = bh / H;
-  const int h = bh % H;
+__global__ void __launch_bounds__(kDaWarps * 32, 6)
+    decode_attn_tma(const __grid_constant__ CUtensorMap kv_map, const T16* __restrict__ qkv, T16* kv_layer,
+                    T16* __restrict__ out, const int32_t* __restrict__ past_len, const int* __restrict__ valid, int B,
+                    int H, int T_max, unsigned* err) {
+  extern __shared__ uint8_t da_smem_raw[];
+  __shared__ __align__(8) uint64_t bars[kDaWarps][kDaStages];
+  __shared__ float s_q[kHd];
+  __shared__ __align__(16) float s_p[kDaWarps][kDaChunk];  // key k at (k & 1) * 8 + (k >> 1)
+  __shared__ float s_m[kDaWarps + 1], s_l[kDaWarps + 1];
+  __shared__ __align__(16) float s_acc[kDaWarps + 1][kHd];
+  const int b = blockIdx.x / H;
+  const int h = blockIdx.x % H;
   const int D = H * kHd;
   const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  T16* orow = out + static_cast<long long>(b) * D + h * kHd;
   if (!valid[b]) {
-    if (tid < kHd) out[static_cast<long long>(b) * D + h * kHd + tid] = from_f32<T16>(0.f);
+    if (tid < kHd) orow[tid] = from_f32<T16>(0.f);
     return;
   }
   const int pos = past_len[b];
   const T16* row = qkv + static_cast<long long>(b) * 3 * D;
-  const long long kv_stride = static_cast<long long>(B) * H * T_max * kHd;  // K block -> V block
-  T16* kc = kv_layer + (static_cast<long long>(b) * H + h) * T_max * kHd;
-  T16* vc = kc + kv_stride;
-  if (tid < kHd) {
-    kc[static_cast<long long>(pos) * kHd + tid] = row[D + h * kHd + tid];
-    vc[static_cast<long long>(pos) * kHd + tid] = row[2 * D + h * kHd + tid];
+  constexpr float kQScale = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) * log2(e)
+  if (tid < kHd) s_q[tid] = to_f32<T16>(row[h * kHd + tid]) * kQScale;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(da_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* wbuf = smem + warp * kDaStages * kDaStageBytes;
+  if (lane == 0) {
+    for (int st = 0; st < kDaStages; ++st) mbar_init(smem_u32(&bars[warp][st]), 1);
+    fence_barrier_init();
   }
-  __syncthreads();  // the new slot is visible to the whole block
+  __syncthreads();
 
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const int grp = lane >> 3;  // key within the step
-  const int sub = lane & 7;   // 16-byte chunk of the row
-  float q[8];
-  {
-    uint4 u = *reinterpret_cast<const uint4*>(row + h * kHd + sub * 8);
-    const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+  const int n_chunks = (pos + kDaChunk - 1) / kDaChunk;
+  const int my_chunks = n_chunks > warp ? (n_chunks - warp + kDaWarps - 1) / kDaWarps : 0;
+  const int row_k = (b * H + h) * T_max;  // row of slot 0 of this (b, h) in the K half
+  const int row_v = row_k + B * H * T_max;  // and in the V half
+  auto issue = [&](int i) {
+    const int st = i % kDaStages;
+    const int j0 = (warp + i * kDaWarps) * kDaChunk;
+    const uint32_t bar = smem_u32(&bars[warp][st]);
+    const uint32_t dst = smem_u32(wbuf + st * kDaStageBytes);
+    mbar_arrive_expect_tx(bar, kDaStageBytes);
+    tma_load_2d(dst, &kv_map, bar, 0, row_k + j0);
+    tma_load_2d(dst + kDaBox, &kv_map, bar, 0, row_v + j0);
+  };
+  if (lane == 0)
+    for (int i = 0; i < kDaStages && i < my_chunks; ++i) issue(i);
+
+  const int key = lane >> 1;  // score phase: key of the chunk
+  const int hf = lane & 1;    // and which 32 of its 64 dimensions
+  float2 q2[16];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float2 f = Type16<T16>::unpack2(uw[e]);
-      q[2 * e] = f.x * 0.125f;  // fold 1/sqrt(64) into q
-      q[2 * e + 1] = f.y * 0.125f;
+  for (int e = 0; e < 16; ++e) q2[e] = make_float2(s_q[hf * 32 + 2 * e], s_q[hf * 32 + 2 * e + 1]);
+  const int par = lane >> 4;  // P.V phase: keys of this parity
+  const int dq = lane & 15;   // dimensions 4dq..4dq+3: 8 bytes of the row
+  float m = -1e30f, l = 0.f;
+  float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
+  int i = 0;
+  for (; i < my_chunks; ++i) {
+    const int st = i % kDaStages;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars[warp][st]), (i / kDaStages) & 1));
+    if (!ok) {
+      if (lane == 0) record_error(err, kErrTimeout, kSiteDecodeAttn);
+      break;
     }
-  }
-  const int n_keys = pos + 1;
-  const int per_warp = (n_keys + (kDecThreads / 32) - 1) / (kDecThreads / 32);
-  const int j_begin = warp * per_warp;
-  const int j_end = min(n_keys, j_begin + per_warp);
-  float m = -1e30f, l = 0.f, acc[8];
+    const uint8_t* kb = wbuf + st * kDaStageBytes;
+    const uint8_t* vb = kb + kDaBox;
+    const int cnt = min(kDaChunk, pos - (warp + i * kDaWarps) * kDaChunk);
+    float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  constexpr int kUnroll = 4;
-  for (int j0 = j_begin; j0 < j_end; j0 += 4 * kUnroll) {
-    uint4 kr[kUnroll], vr[kUnroll];
+    for (int t = 0; t < 4; ++t) {
+      const uint4 u = *reinterpret_cast<const uint4*>(kb + key * 128 + (((hf * 4 + t) ^ (key & 7)) << 4));
+      s2 = fma_f32x2(q2[4 * t + 0], Type16<T16>::unpack2(u.x), s2);
+      s2 = fma_f32x2(q2[4 * t + 1], Type16<T16>::unpack2(u.y), s2);
+      s2 = fma_f32x2(q2[4 * t + 2], Type16<T16>::unpack2(u.z), s2);
+      s2 = fma_f32x2(q2[4 * t + 3], Type16<T16>::unpack2(u.w), s2);
+    }
+    float s = s2.x + s2.y;
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    if (key >= cnt) s = -INFINITY;
+    float cm = s;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int j = j0 + u * 4 + grp;
-      kr[u] = vr[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (j < j_end) {
-        kr[u] = *reinterpret_cast<const uint4*>(kc + static_cast<long long>(j) * kHd + sub * 8);
-        vr[u] = *reinterpret_cast<const uint4*>(vc + static_cast<long long>(j) * kHd + sub * 8);
+    for (int o = 2; o < 32; o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+    const float m_new = fmaxf(m, cm);
+    const float alpha = ex2_approx(m - m_new);
+    const float p = ex2_approx(s - m_new);
+    l = fmaf(l, alpha, hf == 0 ? p : 0.f);  // each key counted by one lane of its pair
+    if (hf == 0) s_p[warp][(key & 1) * 8 + (key >> 1)] = p;
+    m = m_new;
+    const float2 a2 = make_float2(alpha, alpha);
+    acc01 = mul_f32x2(acc01, a2);
+    acc23 = mul_f32x2(acc23, a2);
+    __syncwarp();
+    const float4 pa = *reinterpret_cast<const float4*>(&s_p[warp][par * 8]);
+    const float4 pb = *reinterpret_cast<const float4*>(&s_p[warp][par * 8 + 4]);
+    const float pk[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int kk = 2 * t + par;
+      if (kk < cnt) {
+        const uint2 w = *reinterpret_cast<const uint2*>(vb + kk * 128 + (((dq >> 1) ^ (kk & 7)) << 4) + (dq & 1) * 8);
+        const float2 p2 = make_float2(pk[t], pk[t]);
+        acc01 = fma_f32x2(p2, Type16<T16>::unpack2(w.x), acc01);
+        acc23 = fma_f32x2(p2, Type16<T16>::unpack2(w.y), acc23);
       }
     }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int j = j0 + u * 4 + grp;
-      const uint32_t kw[4] = {kr[u].x, kr[u].y, kr[u].z, kr[u].w};
-      float d = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float2 f = Type16<T16>::unpack2(kw[e]);
-        d = fmaf(q[2 * e], f.x, d);
-        d = fmaf(q[2 * e + 1], f.y, d);
-      }
-      d += __shfl_xor_sync(0xffffffffu, d, 1);
-      d += __shfl_xor_sync(0xffffffffu, d, 2);
-      d += __shfl_xor_sync(0xffffffffu, d, 4);
-      if (j < j_end) {
-        const float m_new = fmaxf(m, d);
-        const float alpha = __expf(m - m_new);
-        const float p = __expf(d - m_new);
-        l = l * alpha + p;
-        const uint32_t vw[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float2 f = Type16<T16>::unpack2(vw[e]);
-          acc[2 * e] = fmaf(p, f.x, acc[2 * e] * alpha);
-          acc[2 * e + 1] = fmaf(p, f.y, acc[2 * e + 1] * alpha);
-        }
-        m = m_new;
-      }
+    __syncwarp();
+    if (lane == 0 && i + kDaStages < my_chunks) {
+      fence_proxy_async_smem();
+      issue(i + kDaStages);
     }
   }
-  // one partial (m, l, acc[64]) per lane group of 8
-  const int g = tid >> 3;
-  if (sub == 0) {
-    s_m[g] = m;
-    s_l[g] = l;
+  if (i < my_chunks && lane == 0) {
+    // timed out: wait (bounded) for this warp's loads still in flight
+    for (int k = i; k < my_chunks && k < i + kDaStages; ++k)
+      (void)mbar_wait(smem_u32(&bars[warp][k % kDaStages]), (k / kDaStages) & 1);
   }
 #pragma unroll
-  for (int e = 0; e < 8; ++e) s_acc[g][sub * 8 + e] = acc[e];
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+  acc01.x += __shfl_xor_sync(0xffffffffu, acc01.x, 16);  // add the two key parities
+  acc01.y += __shfl_xor_sync(0xffffffffu, acc01.y, 16);
+  acc23.x += __shfl_xor_sync(0xffffffffu, acc23.x, 16);
+  acc23.y += __shfl_xor_sync(0xffffffffu, acc23.y, 16);
+  if (lane == 0) {
+    s_m[warp] = m;
+    s_l[warp] = l;
+  }
+  if (par == 0) *reinterpret_cast<float4*>(&s_acc[warp][4 * dq]) = make_float4(acc01.x, acc01.y, acc23.x, acc23.y);
+  if (warp == 0) {
+    // the new token: score, value, and its slot in the cache
+    const uint32_t kw = reinterpret_cast<const uint32_t*>(row + D + h * kHd)[lane];
+    const uint32_t vw = reinterpret_cast<const uint32_t*>(row + 2 * D + h * kHd)[lane];
+    const float2 kf = Type16<T16>::unpack2(kw);
+    float sn = fmaf(s_q[2 * lane], kf.x, s_q[2 * lane + 1] * kf.y);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sn += __shfl_xor_sync(0xffffffffu, sn, o);
+    const float2 vf = Type16<T16>::unpack2(vw);
+    if (lane == 0) {
+      s_m[kDaWarps] = sn;
+      s_l[kDaWarps] = 1.f;
+    }
+    s_acc[kDaWarps][2 * lane] = vf.x;
+    s_acc[kDaWarps][2 * lane + 1] = vf.y;
+    reinterpret_cast<uint32_t*>(kv_layer + (static_cast<long long>(row_k) + pos) * kHd)[lane] = kw;
+    reinterpret_cast<uint32_t*>(kv_layer + (static_cast<long long>(row_v) + pos) * kHd)[lane] = vw;
+  }
   __syncthreads();
   if (tid < kHd) {
-    float M = -1e30f;
-    for (int i = 0; i < kDecThreads / 8; ++i) M = fmaxf(M, s_m[i]);
+    float M = s_m[0];
+#pragma unroll
+    for (int w = 1; w <= kDaWarps; ++w) M = fmaxf(M, s_m[w]);
     float L = 0.f, A = 0.f;
-    for (int i = 0; i < kDecThreads / 8; ++i) {
-      const float w = __expf(s_m[i] - M);
-      L += s_l[i] * w;
-      A += s_acc[i][tid] * w;
+#pragma unroll
+    for (int w = 0; w <= kDaWarps; ++w) {
+      const float c = ex2_approx(s_m[w] - M);
+      L = fmaf(s_l[w], c, L);
+      A = fmaf(s_acc[w][tid], c, A);
     }
-    out[static_cast<long long>(b) * D + h * kHd + tid] = from_f32<T16>(A / L);
+    orow[tid] = from_f32<T16>(A / L);
   }
 }
 
@@ -256,18 +323,27 @@ cudaError_t launch_decode_embed_ln(gpt2_dtype dt, const int32_t* tokens, const i
   return cudaGetLastError();
 }
 
+namespace {
+template <typename T16>
+cudaError_t launch_decode_attn_t(const void* qkv, void* kv_layer, void* out, const int32_t* past_len, const int* valid,
+                                 int B, int n_head, int T_max, cudaStream_t stream) {
+  // the layer's K and V halves as one [2 * B * n_head * T_max, 64] matrix
+  const uint64_t rows = 2ull * B * n_head * static_cast<uint64_t>(T_max);
+  if (rows >= (1ull << 31)) return cudaErrorInvalidValue;
+  CUtensorMap map;
+  if (!encode_tma_2d(&map, Type16<T16>::kTma, kv_layer, kHd, rows, kHd * 2, kHd, kDaChunk))
+    return cudaErrorInvalidValue;
+  decode_attn_tma<T16><<<B * n_head, kDaWarps * 32, kDaSmem, stream>>>(
+      map, static_cast<const T16*>(qkv), static_cast<T16*>(kv_layer), static_cast<T16*>(out), past_len, valid, B,
+      n_head, T_max, device_error_word());
+  return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_decode_attention(gpt2_dtype dt, const void* qkv, void* kv_layer, void* out, const int32_t* past_len,
                                     const int* valid, int B, int n_head, int T_max, cudaStream_t stream) {
-  if (dt == GPT2_F16) {
-    using T = __half;
-    decode_attn<T><<<B * n_head, kDecThreads, 0, stream>>>(static_cast<const T*>(qkv), static_cast<T*>(kv_layer),
-                                                           static_cast<T*>(out), past_len, valid, B, n_head, T_max);
-  } else {
-    using T = __nv_bfloat16;
-    decode_attn<T><<<B * n_head, kDecThreads, 0, stream>>>(static_cast<const T*>(qkv), static_cast<T*>(kv_layer),
-                                                           static_cast<T*>(out), past_len, valid, B, n_head, T_max);
-  }
-  return cudaGetLastError();
+  if (dt == GPT2_F16) return launch_decode_attn_t<__half>(qkv, kv_layer, out, past_len, valid, B, n_head, T_max, stream);
+  return launch_decode_attn_t<__nv_bfloat16>(qkv, kv_layer, out, past_len, valid, B, n_head, T_max, stream);
 }
 
 cudaError_t launch_argmax_rows(const float* logits, int64_t ld, int B, int V, const int* valid, int32_t* next_tokens,

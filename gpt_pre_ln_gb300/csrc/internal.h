@@ -1,6 +1,7 @@
 // Host-side declarations shared by the translation units of libgpt2gb.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -14,6 +15,12 @@ namespace gpt2 {
 unsigned* device_error_word();
 // Number of SMs of the current device (cached per device).
 int num_sms();
+
+// 2-D TMA map over a row-major [outer, inner] matrix with the given row pitch
+// in bytes; boxes of [box_outer, box_inner] elements, 128-byte swizzle,
+// out-of-range elements read as zero.  False if the driver rejects it.
+bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 
 // Each launcher validates nothing beyond what its kernel needs (the C-ABI
 // layer has checked the arguments) and returns the launch status.

@@ -232,7 +232,7 @@ int gpt2_forward_logits(const gpt2_dims *dims, const gpt2_model_weights *w, cons
                         gpt2_stream_t stream);
 
 /* Bytes of a KV cache laid out [n_layer, 2 (K, V), B, n_head, T_max, 64] in
- * the path's element type (bf16 for BF16, fp32 for F32). */
+ * the path's element type (2 bytes for BF16 and F16, 4 for F32). */
 size_t gpt2_kv_cache_bytes(const gpt2_dims *dims, int B, int T_max);
 
 /* Workspace needed by gpt2_decode_step for a batch of B sequences. */
@@ -252,7 +252,8 @@ size_t gpt2_decode_workspace_bytes(const gpt2_dims *dims, int B);
  *   that sequence is left unchanged); tokens, next_tokens: int32 [B] device
  *   (they may be the same buffer); logits_opt: NULL or fp32 [B, ld] device
  *   receiving the step's logits (ld >= vocab, a multiple of 4); ws of
- *   gpt2_decode_workspace_bytes(dims, B) bytes.  Only the BF16 path. */
+ *   gpt2_decode_workspace_bytes(dims, B) bytes.  16-bit paths only (BF16,
+ *   F16: GPT2_ERR_UNSUPPORTED for F32), and 2 * B * n_head * T_max < 2^31. */
 int gpt2_decode_step(const gpt2_dims *dims, const gpt2_model_weights *w, void *kv_cache, int B, int T_max,
                      int32_t *past_len, const int32_t *tokens, int32_t *next_tokens, float *logits_opt, int64_t ld,
                      void *ws, size_t ws_bytes, gpt2_stream_t stream);
