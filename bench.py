@@ -159,7 +159,14 @@ def run_reference(args):
 
 
 def _decode_measure(G, torch, steps=64):
-    """64 greedy decode steps at B=64 over a 1023-long cache; achieved GB/s."""
+    """64 greedy decode steps at B=64 over a 1023-long cache; achieved GB/s.
+
+    The steps run as a serving loop runs them: one decode step captured into
+    a CUDA graph (the step reads and advances the lengths and tokens on the
+    device), replayed `steps` times.  The same steps launched eagerly are
+    timed too, and a third pass with a CUDA event pair around every launch
+    gives the per-kernel times (the state is reset before each pass).
+    """
     import synth
     dims = synth.GPT2_SMALL_DECODE
     B, cache_len = 64, 1023
@@ -173,26 +180,60 @@ def _decode_measure(G, torch, steps=64):
     kv = torch.zeros(L, 2, B, H, T_max, 64, device="cuda", dtype=torch.bfloat16)
     kv[..., :cache_len, :] = torch.randn(L, 2, B, H, cache_len, 64, device="cuda", generator=g).to(torch.bfloat16)
     tokens0 = torch.from_numpy(synth.draw_tokens(d, B, 1, dims.vocab)[:, 0].copy()).cuda()
-    past = torch.full((B,), cache_len, dtype=torch.int32, device="cuda")
+    past0 = torch.full((B,), cache_len, dtype=torch.int32, device="cuda")
+    past = past0.clone()
     tok = tokens0.clone()
     wsb = G.gpt2_decode_workspace_bytes(cd, B)
     ws = torch.empty(wsb, device="cuda", dtype=torch.uint8)
-    # warm-up (does not advance the measured state)
-    for _ in range(3):
-        p2 = past.clone()
-        t2 = tok.clone()
-        G.gpt2_decode_step(cd, mw, kv, B, T_max, p2, t2, t2, None, 0, ws, wsb)
-    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+
+    def reset():
+        past.copy_(past0)
+        tok.copy_(tokens0)
+
+    def one(s_):
+        G.gpt2_decode_step(cd, mw, kv, B, T_max, past, tok, tok, None, 0, ws, wsb, s_)
+
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    G.gpt2_profile_begin(200 * steps)
-    s.record()
-    for _ in range(steps):
-        G.gpt2_decode_step(cd, mw, kv, B, T_max, past, tok, tok, None, 0, ws, wsb)
-    e.record()
-    torch.cuda.synchronize()
-    G.gpt2_profile_end()
+    with torch.cuda.stream(stream):
+        for _ in range(3):  # warm-up
+            reset()
+            one(stream)
+        torch.cuda.synchronize()
+        # eager launches
+        reset()
+        torch.cuda.synchronize()
+        s.record(stream)
+        for _ in range(steps):
+            one(stream)
+        e.record(stream)
+        torch.cuda.synchronize()
+        eager_ms = s.elapsed_time(e)
+        eager_tokens = tok.clone()
+        # one step captured, replayed
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            one(stream)
+        reset()
+        graph.replay()  # warm the graph
+        reset()
+        torch.cuda.synchronize()
+        s.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        e.record(stream)
+        torch.cuda.synchronize()
+        ms = s.elapsed_time(e)
+        same = bool(torch.equal(tok, eager_tokens))
+        # per-kernel times
+        reset()
+        torch.cuda.synchronize()
+        G.gpt2_profile_begin(200 * steps)
+        for _ in range(steps):
+            one(stream)
+        torch.cuda.synchronize()
+        G.gpt2_profile_end()
     prof = G.gpt2_profile_read()
-    ms = s.elapsed_time(e)
     st, site = G.gpt2_last_error()
     # algorithmic bytes: every step reads the cached K, V of all layers for
     # positions 0..p (p = 1023 .. 1086) plus every weight once
@@ -201,16 +242,18 @@ def _decode_measure(G, torch, steps=64):
     w_bytes = steps * 2 * (dims.vocab * dims.d_model + L * (dims.d_model * 3 * dims.d_model + dims.d_model ** 2 +
                                                            2 * dims.d_model * dims.d_ff))
     attn = prof.get("decode_attn", (0, 0.0, 0.0, 0.0))
-    attn_kv = kv_bytes
-    del keep
+    prof_ms = sum(v[1] for v in prof.values())
+    del keep, graph
     return {
         "workload": "gpt2_small_decode_b64", "batch": B, "cached": cache_len, "steps": steps,
+        "launch": "one step captured in a CUDA graph, replayed",
         "tokens_per_s": B * steps / (ms / 1e3), "ms_per_step": ms / steps,
+        "eager_ms_per_step": eager_ms / steps, "graph_matches_eager": same,
         "algorithmic_gb_per_step": (kv_bytes + w_bytes) / steps / 1e9,
         "achieved_gbs": (kv_bytes + w_bytes) / (ms / 1e3) / 1e9,
-        "attn_kernel_gbs": attn_kv / (attn[1] / 1e3) / 1e9 if attn[1] > 0 else None,
-        "attn_share": attn[1] / ms if ms > 0 else None,
-        "device_status": st, "launches": sum(v[0] for v in prof.values()),
+        "attn_kernel_gbs": kv_bytes / (attn[1] / 1e3) / 1e9 if attn[1] > 0 else None,
+        "kernel_share": {k: v[1] / prof_ms for k, v in prof.items()},
+        "device_status": st, "launches_per_step": sum(v[0] for v in prof.values()) / steps,
     }
 
 
@@ -279,7 +322,6 @@ def run_ours(args):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    G.gpt2_profile_begin(200 * args.steps)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -289,12 +331,10 @@ def run_ours(args):
         step()
     ev1.record(stream)
     torch.cuda.synchronize()
-    G.gpt2_profile_end()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
-    prof = G.gpt2_profile_read()
     st, site = G.gpt2_last_error()
     if st != 0:
         raise RuntimeError(f"device error {st} at site {site} in the timed region")
@@ -304,7 +344,19 @@ def run_ours(args):
         ms = float(t.item())
     tokens_all = B * T * args.steps * world
     value = tokens_all / (ms / 1e3)
-    launches = sum(v[0] for v in prof.values())
+
+    # per-kernel times: a separate pass with a CUDA event pair around every
+    # launch (the events serialise the kernels, so this pass is not timed
+    # as a whole)
+    prof_steps = max(1, min(args.steps, 10))
+    G.gpt2_profile_begin(200 * prof_steps)
+    for _ in range(prof_steps):
+        step()
+    torch.cuda.synchronize()
+    G.gpt2_profile_end()
+    prof = G.gpt2_profile_read()
+    launches_per_step = sum(v[0] for v in prof.values()) / prof_steps
+    launches = int(round(launches_per_step * args.steps))
 
     # ---------------------------------------------------------- e2e (host)
     # Every step copies its token ids host -> device and its full fp32 logits
@@ -358,8 +410,8 @@ def run_ours(args):
     g_launch_ms = gemm[1] / gemm[0]
     g_flops_launch = gemm[2] / gemm[0]
     achieved = g_flops_launch / (g_launch_ms / 1e3) / 1e12
-    total_flops_step = sum(v[2] for v in prof.values()) / args.steps
-    kernels = {k: {"launches_per_step": v[0] / args.steps, "ms_per_step": v[1] / args.steps,
+    total_flops_step = sum(v[2] for v in prof.values()) / prof_steps
+    kernels = {k: {"launches_per_step": v[0] / prof_steps, "ms_per_step": v[1] / prof_steps,
                    "share": v[1] / sum(x[1] for x in prof.values())} for k, v in prof.items()}
 
     out = {
@@ -379,6 +431,7 @@ def run_ours(args):
         "end_to_end_tflops": total_flops_step / (ms / args.steps / 1e3) / 1e12,
         "end_to_end_frac": total_flops_step / (ms / args.steps / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
         "kernels": kernels,
+        "kernel_times": "separate pass: a CUDA event pair around every launch",
         "clocks": clk,
     }
     if rank == 0 and not args.no_decode:

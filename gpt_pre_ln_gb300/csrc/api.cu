@@ -187,7 +187,10 @@ cudaError_t linear(gpt2_dtype dt, const void* x, const void* w, const void* bias
   const double bytes = (static_cast<double>(M) * K + static_cast<double>(K) * N) * e +
                        (epi != GPT2_EPI_NONE ? N * e : 0.0) +
                        (epi == GPT2_EPI_BIAS_RESIDUAL ? 4.0 * M * N : 0.0) + static_cast<double>(M) * N * esize(y_t);
-  ProfScope prof(dt == GPT2_BF16 ? "gemm_bf16_tcgen05" : dt == GPT2_F16 ? "gemm_f16_tcgen05" : "gemm_f32_simt",
+  const bool rows = M <= kMaxRowsGemm;  // the few-row kernel (gemm_rows.cu)
+  ProfScope prof(dt == GPT2_BF16   ? (rows ? "gemm_rows_bf16_tcgen05" : "gemm_bf16_tcgen05")
+                 : dt == GPT2_F16 ? (rows ? "gemm_rows_f16_tcgen05" : "gemm_f16_tcgen05")
+                                  : "gemm_f32_simt",
                  2.0 * M * N * K, bytes, s);
   if (is16(dt)) return launch_gemm_16(dt, x, w, bias, res, y, M, N, K, ldy, w_out_in, epi, y_t, s);
   return launch_gemm_f32(static_cast<const float*>(x), static_cast<const float*>(w), static_cast<const float*>(bias),
@@ -265,10 +268,14 @@ int check_model(const gpt2_dims* dims, const gpt2_model_weights* w) {
   return GPT2_OK;
 }
 
+// Up to kMaxRowsGemm sequences the lm_head's epilogue makes argmax
+// candidates (no logits buffer); beyond, fp32 logits feed argmax_rows.
 size_t decode_ws_bytes(const gpt2_dims* d, int B) {
   const size_t M = static_cast<size_t>(B);
   const size_t Vp = (static_cast<size_t>(d->vocab) + 3) & ~static_cast<size_t>(3);
-  return acts_bytes(d, static_cast<int64_t>(M)) + align256(M * Vp * 4) + align256(M * 4);
+  const size_t head = B <= kMaxRowsGemm ? align256(M * rows_argmax_candidates(d->vocab) * sizeof(float2))
+                                        : align256(M * Vp * 4);
+  return acts_bytes(d, static_cast<int64_t>(M)) + head + align256(M * 4);
 }
 
 }  // namespace
@@ -463,10 +470,15 @@ int gpt2_decode_step(const gpt2_dims* dims, const gpt2_model_weights* w, void* k
   A.o = c.take<char>(static_cast<size_t>(B) * D, 2);
   A.g = c.take<char>(static_cast<size_t>(B) * F, 2);  // 16-bit paths only
   const int64_t Vp = (static_cast<int64_t>(V) + 3) & ~static_cast<int64_t>(3);
-  float* lg = c.take<float>(static_cast<size_t>(B) * Vp, 4);
+  const bool fused_argmax = B <= kMaxRowsGemm;
+  const int n_cand = rows_argmax_candidates(V);
+  float2* cand = nullptr;
+  float* lg = nullptr;
+  if (fused_argmax)
+    cand = c.take<float2>(static_cast<size_t>(B) * n_cand, sizeof(float2));
+  else
+    lg = c.take<float>(static_cast<size_t>(B) * Vp, 4);
   int* valid = c.take<int>(static_cast<size_t>(B), 4);
-  float* logits = logits_opt ? logits_opt : lg;
-  const int64_t lld = logits_opt ? ld : Vp;
   cudaStream_t s = cs(stream);
   const gpt2_dtype dt = dims->dtype;
   const size_t layer_elems = static_cast<size_t>(2) * B * H * static_cast<size_t>(T_max) * 64;
@@ -493,8 +505,19 @@ int gpt2_decode_step(const gpt2_dims* dims, const gpt2_model_weights* w, void* k
                      s));
   }
   GPT2_CUDA(layernorm(A.x, w->lnf_g, w->lnf_b, A.a, B, D, dims->eps, GPT2_F32, dt, s));
-  GPT2_CUDA(linear(dt, A.a, w->wte, nullptr, nullptr, logits, B, V, D, lld, true, GPT2_EPI_NONE, GPT2_F32, s));
-  {
+  if (fused_argmax) {
+    {
+      ProfScope prof(dt == GPT2_BF16 ? "gemm_rows_bf16_tcgen05" : "gemm_rows_f16_tcgen05", 2.0 * B * V * D,
+                     (static_cast<double>(B) + V) * D * esize(dt) + (logits_opt ? 4.0 * B * V : 0.0), s);
+      GPT2_CUDA(launch_gemm_rows_16(dt, A.a, w->wte, nullptr, nullptr, logits_opt, B, V, D, logits_opt ? ld : V, true,
+                                    GPT2_EPI_NONE, GPT2_F32, s, cand));
+    }
+    ProfScope prof("argmax_candidates", static_cast<double>(B) * n_cand, static_cast<double>(B) * n_cand * 8.0, s);
+    GPT2_CUDA(launch_argmax_candidates(cand, n_cand, B, valid, next_tokens, past_len, s));
+  } else {
+    float* logits = logits_opt ? logits_opt : lg;
+    const int64_t lld = logits_opt ? ld : Vp;
+    GPT2_CUDA(linear(dt, A.a, w->wte, nullptr, nullptr, logits, B, V, D, lld, true, GPT2_EPI_NONE, GPT2_F32, s));
     ProfScope prof("argmax_rows", static_cast<double>(B) * V, static_cast<double>(B) * V * 4.0, s);
     GPT2_CUDA(launch_argmax_rows(logits, lld, B, V, valid, next_tokens, past_len, s));
   }

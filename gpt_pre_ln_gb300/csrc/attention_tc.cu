@@ -116,6 +116,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     mbar_init(drain, 1);
     fence_barrier_init();
   }
+  griddep_wait();  // qkv comes from the kernel before; tensor memory only after it completed
+  griddep_launch_dependents();
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -340,9 +342,8 @@ cudaError_t launch_t(const void* qkv, void* out, int B, int T, int n_head, cudaS
     configured[dev] = 1;
   }
   dim3 grid(B * n_head, (T + kTq - 1) / kTq);
-  attn_causal_tc<T16><<<grid, kAttnThreads, kSmemBytes, stream>>>(map, static_cast<T16*>(out), T, n_head,
-                                                                   device_error_word());
-  return cudaGetLastError();
+  return launch_pdl(attn_causal_tc<T16>, grid, kAttnThreads, kSmemBytes, stream, 0, map, static_cast<T16*>(out), T,
+                    n_head, device_error_word());
 }
 
 }  // namespace

@@ -32,6 +32,9 @@ enum ErrSite : unsigned {
   kSiteDecodePos = 11,
   kSiteDecodeToken = 12,
   kSiteDecodeAttn = 13,
+  kSiteRowsProducer = 14,
+  kSiteRowsMma = 15,
+  kSiteRowsEpilogue = 16,
 };
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
@@ -149,6 +152,23 @@ __device__ __forceinline__ float gelu_new_ex2(float x) {
   const float t = fmaf(-2.f, rcp_approx(1.f + ex2_approx(two_log2e * u)), 1.f);
   const float hx = 0.5f * x;
   return fmaf(hx, t, hx);
+}
+
+// ------------------------------------------------ programmatic dependent launch
+// Every kernel of the 16-bit path is launched with programmatic stream
+// serialisation (launch_pdl in internal.h): it may start while the kernel
+// before it on the stream is still running.  griddep_wait() returns once that
+// kernel has completed and its memory operations are visible.  Each kernel
+// waits before it reads anything the kernel before it may have written and
+// before it writes anything, and signals its own dependents only after that
+// wait.  So the code before a kernel's wait may read data written two or more
+// kernels back (weights, the cache of earlier steps, lengths set at the start
+// of a step) but nothing newer, and it allocates no tensor memory (a kernel
+// still running may need it).  In a kernel launched without the attribute
+// both calls do nothing.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ mbarrier

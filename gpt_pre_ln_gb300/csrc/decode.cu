@@ -33,6 +33,8 @@ __global__ void decode_embed_ln(const int32_t* __restrict__ tokens, const int32_
                                 const T16* __restrict__ gamma, const T16* __restrict__ beta, float* __restrict__ x,
                                 T16* __restrict__ y, int B, int D, int V, int n_pos, int T_max, float eps,
                                 int* __restrict__ valid, unsigned* err) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (b >= B) return;
   const int lane = threadIdx.x & 31;
@@ -106,22 +108,13 @@ __global__ void __launch_bounds__(kDaWarps * 32, 6)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   T16* orow = out + static_cast<long long>(b) * D + h * kHd;
-  if (!valid[b]) {
-    if (tid < kHd) orow[tid] = from_f32<T16>(0.f);
-    return;
-  }
-  const int pos = past_len[b];
-  const T16* row = qkv + static_cast<long long>(b) * 3 * D;
-  constexpr float kQScale = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) * log2(e)
-  if (tid < kHd) s_q[tid] = to_f32<T16>(row[h * kHd + tid]) * kQScale;
+  // valid and past_len were written at the start of the step, two or more
+  // kernels back: readable before the dependency wait, and so are the cached
+  // keys and values of slots below pos (earlier steps)
+  const bool is_valid = valid[b] != 0;
+  const int pos = is_valid ? past_len[b] : 0;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(da_smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* wbuf = smem + warp * kDaStages * kDaStageBytes;
-  if (lane == 0) {
-    for (int st = 0; st < kDaStages; ++st) mbar_init(smem_u32(&bars[warp][st]), 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
-
   const int n_chunks = (pos + kDaChunk - 1) / kDaChunk;
   const int my_chunks = n_chunks > warp ? (n_chunks - warp + kDaWarps - 1) / kDaWarps : 0;
   const int row_k = (b * H + h) * T_max;  // row of slot 0 of this (b, h) in the K half
@@ -135,8 +128,21 @@ __global__ void __launch_bounds__(kDaWarps * 32, 6)
     tma_load_2d(dst, &kv_map, bar, 0, row_k + j0);
     tma_load_2d(dst + kDaBox, &kv_map, bar, 0, row_v + j0);
   };
-  if (lane == 0)
+  if (lane == 0) {
+    for (int st = 0; st < kDaStages; ++st) mbar_init(smem_u32(&bars[warp][st]), 1);
+    fence_barrier_init();
     for (int i = 0; i < kDaStages && i < my_chunks; ++i) issue(i);
+  }
+  griddep_wait();  // q, k, v of the new token come from the kernel before
+  griddep_launch_dependents();
+  if (!is_valid) {
+    if (tid < kHd) orow[tid] = from_f32<T16>(0.f);
+    return;
+  }
+  const T16* row = qkv + static_cast<long long>(b) * 3 * D;
+  constexpr float kQScale = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) * log2(e)
+  if (tid < kHd) s_q[tid] = to_f32<T16>(row[h * kHd + tid]) * kQScale;
+  __syncthreads();
 
   const int key = lane >> 1;  // score phase: key of the chunk
   const int hf = lane & 1;    // and which 32 of its 64 dimensions
@@ -252,23 +258,11 @@ __global__ void __launch_bounds__(kDaWarps * 32, 6)
   }
 }
 
-// One CTA per row: lowest index of the maximum; then past_len[b] += 1.
-__global__ void __launch_bounds__(1024) argmax_rows(const float* __restrict__ logits, long long ld, int V,
-                                                    const int* __restrict__ valid, int32_t* __restrict__ next_tokens,
-                                                    int32_t* __restrict__ past_len) {
+// (best, bi) of every thread of the block -> the block's maximum with the
+// lowest index on ties, returned to thread 0.
+__device__ __forceinline__ void block_argmax(float& best, int& bi) {
   __shared__ float s_v[32];
   __shared__ int s_i[32];
-  const int b = blockIdx.x;
-  const float* r = logits + static_cast<long long>(b) * ld;
-  float best = -INFINITY;
-  int bi = 0x7fffffff;
-  for (int c = threadIdx.x; c < V; c += blockDim.x) {
-    const float v = r[c];
-    if (v > best) {  // strictly greater keeps the first (lowest) index per thread
-      best = v;
-      bi = c;
-    }
-  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float ov = __shfl_xor_sync(0xffffffffu, best, o);
@@ -287,15 +281,64 @@ __global__ void __launch_bounds__(1024) argmax_rows(const float* __restrict__ lo
   if (threadIdx.x == 0) {
     best = s_v[0];
     bi = s_i[0];
-    for (int w = 1; w < (blockDim.x >> 5); ++w)
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w)
       if (s_v[w] > best || (s_v[w] == best && s_i[w] < bi)) {
         best = s_v[w];
         bi = s_i[w];
       }
-    if (valid[b]) {
-      next_tokens[b] = bi;
-      past_len[b] += 1;
+  }
+}
+
+// One CTA per row: lowest index of the maximum; then past_len[b] += 1.
+__global__ void __launch_bounds__(1024) argmax_rows(const float* __restrict__ logits, long long ld, int V,
+                                                    const int* __restrict__ valid, int32_t* __restrict__ next_tokens,
+                                                    int32_t* __restrict__ past_len) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int b = blockIdx.x;
+  const float* r = logits + static_cast<long long>(b) * ld;
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int c = threadIdx.x; c < V; c += blockDim.x) {
+    const float v = r[c];
+    if (v > best) {  // strictly greater keeps the first (lowest) index per thread
+      best = v;
+      bi = c;
     }
+  }
+  block_argmax(best, bi);
+  if (threadIdx.x == 0 && valid[b]) {
+    next_tokens[b] = bi;
+    past_len[b] += 1;
+  }
+}
+
+// The same from the per-row candidates (value, index bits) of the lm_head
+// GEMM's epilogue: every candidate is the maximum of a disjoint set of
+// columns with its lowest index, so the maximum candidate with the lowest
+// index is the row's argmax.
+__global__ void __launch_bounds__(256) argmax_candidates(const float2* __restrict__ cand, int n_cand,
+                                                         const int* __restrict__ valid,
+                                                         int32_t* __restrict__ next_tokens,
+                                                         int32_t* __restrict__ past_len) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int b = blockIdx.x;
+  const float2* c = cand + static_cast<long long>(b) * n_cand;
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int k = threadIdx.x; k < n_cand; k += blockDim.x) {
+    const float2 e = c[k];
+    const int ei = __float_as_int(e.y);
+    if (e.x > best || (e.x == best && ei < bi)) {
+      best = e.x;
+      bi = ei;
+    }
+  }
+  block_argmax(best, bi);
+  if (threadIdx.x == 0 && valid[b]) {
+    next_tokens[b] = bi;
+    past_len[b] += 1;
   }
 }
 
@@ -309,18 +352,14 @@ cudaError_t launch_decode_embed_ln(gpt2_dtype dt, const int32_t* tokens, const i
   unsigned* err = device_error_word();
   if (dt == GPT2_F16) {
     using T = __half;
-    decode_embed_ln<T><<<grid, block, 0, stream>>>(tokens, past_len, static_cast<const T*>(wte),
-                                                   static_cast<const T*>(wpe), static_cast<const T*>(gamma),
-                                                   static_cast<const T*>(beta), x, static_cast<T*>(y), B, D, V, n_pos,
-                                                   T_max, eps, valid, err);
-  } else {
-    using T = __nv_bfloat16;
-    decode_embed_ln<T><<<grid, block, 0, stream>>>(tokens, past_len, static_cast<const T*>(wte),
-                                                   static_cast<const T*>(wpe), static_cast<const T*>(gamma),
-                                                   static_cast<const T*>(beta), x, static_cast<T*>(y), B, D, V, n_pos,
-                                                   T_max, eps, valid, err);
+    return launch_pdl(decode_embed_ln<T>, grid, block, 0, stream, 0, tokens, past_len, static_cast<const T*>(wte),
+                      static_cast<const T*>(wpe), static_cast<const T*>(gamma), static_cast<const T*>(beta), x,
+                      static_cast<T*>(y), B, D, V, n_pos, T_max, eps, valid, err);
   }
-  return cudaGetLastError();
+  using T = __nv_bfloat16;
+  return launch_pdl(decode_embed_ln<T>, grid, block, 0, stream, 0, tokens, past_len, static_cast<const T*>(wte),
+                    static_cast<const T*>(wpe), static_cast<const T*>(gamma), static_cast<const T*>(beta), x,
+                    static_cast<T*>(y), B, D, V, n_pos, T_max, eps, valid, err);
 }
 
 namespace {
@@ -333,10 +372,9 @@ cudaError_t launch_decode_attn_t(const void* qkv, void* kv_layer, void* out, con
   CUtensorMap map;
   if (!encode_tma_2d(&map, Type16<T16>::kTma, kv_layer, kHd, rows, kHd * 2, kHd, kDaChunk))
     return cudaErrorInvalidValue;
-  decode_attn_tma<T16><<<B * n_head, kDaWarps * 32, kDaSmem, stream>>>(
-      map, static_cast<const T16*>(qkv), static_cast<T16*>(kv_layer), static_cast<T16*>(out), past_len, valid, B,
-      n_head, T_max, device_error_word());
-  return cudaGetLastError();
+  return launch_pdl(decode_attn_tma<T16>, B * n_head, kDaWarps * 32, kDaSmem, stream, 0, map,
+                    static_cast<const T16*>(qkv), static_cast<T16*>(kv_layer), static_cast<T16*>(out), past_len,
+                    valid, B, n_head, T_max, device_error_word());
 }
 }  // namespace
 
@@ -346,10 +384,15 @@ cudaError_t launch_decode_attention(gpt2_dtype dt, const void* qkv, void* kv_lay
   return launch_decode_attn_t<__nv_bfloat16>(qkv, kv_layer, out, past_len, valid, B, n_head, T_max, stream);
 }
 
+cudaError_t launch_argmax_candidates(const float2* cand, int n_cand, int B, const int* valid, int32_t* next_tokens,
+                                     int32_t* past_len, cudaStream_t stream) {
+  return launch_pdl(argmax_candidates, B, 256, 0, stream, 0, cand, n_cand, valid, next_tokens, past_len);
+}
+
 cudaError_t launch_argmax_rows(const float* logits, int64_t ld, int B, int V, const int* valid, int32_t* next_tokens,
                                int32_t* past_len, cudaStream_t stream) {
-  argmax_rows<<<B, 1024, 0, stream>>>(logits, ld, V, valid, next_tokens, past_len);
-  return cudaGetLastError();
+  return launch_pdl(argmax_rows, B, 1024, 0, stream, 0, logits, static_cast<long long>(ld), V, valid, next_tokens,
+                    past_len);
 }
 
 }  // namespace gpt2

@@ -324,6 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain_bar, 1);
     fence_barrier_init();
   }
+  griddep_wait();  // x (and the residual) come from earlier kernels; tensor memory only after they completed
+  griddep_launch_dependents();
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
     tmem_relinquish();
@@ -488,6 +490,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(drain_bar, 1);
     fence_barrier_init();
   }
+  griddep_wait();  // x (and the residual) come from earlier kernels; tensor memory only after they completed
+  griddep_launch_dependents();
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), Cfg::TMEM_COLS);
     tmem_relinquish_pair();
@@ -638,8 +642,7 @@ cudaError_t run_1sm(const T16* x, const T16* w, const EpiArgs<OutT, T16>& ea, in
   if (!(B_MN ? make_map(&tb, dt, w, N, K, kBK) : make_map(&tb, dt, w, K, N, BN))) return cudaErrorInvalidValue;
   const int tiles = ((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  kern<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, ea, K);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, kThreads, Cfg::SMEM_BYTES, stream, 0, ta, tb, ea, K);
 }
 
 template <bool B_MN, int EPI, typename OutT, typename T16>
@@ -678,8 +681,7 @@ cudaError_t run_2sm(const T16* x, const T16* w, const EpiArgs<OutT, T16>& ea, in
   const int pairs_max = (dev >= 0 && dev < 64) ? max_pairs[dev] : num_sms() / 2;
   const int tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kPairBN - 1) / kPairBN);
   const int pairs = tiles < pairs_max ? tiles : pairs_max;
-  kern<<<2 * pairs, kThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, ea, K);
-  return cudaGetLastError();
+  return launch_pdl(kern, 2 * pairs, kThreads, Cfg::SMEM_BYTES, stream, 0, ta, tb, ea, K);
 }
 
 // Kernel variant for an M x N problem: 0 = CTA pair (256 x 256 tiles),
@@ -751,6 +753,9 @@ template <typename T16>
 cudaError_t launch(const void* x, const void* w, const void* bias, const float* residual, void* y, int64_t M, int N,
                    int K, int64_t ldy, bool w_out_in, int epilogue, gpt2_dtype y_t, cudaStream_t stream) {
   if (M == 0) return cudaSuccess;
+  if (M <= kMaxRowsGemm)
+    return launch_gemm_rows_16(Type16<T16>::kFormat == 0 ? GPT2_F16 : GPT2_BF16, x, w, bias, residual, y, M, N, K,
+                               ldy, w_out_in, epilogue, y_t, stream);
   const int m = static_cast<int>(M);
   const int v = pick_variant(m, N);
   const T16* X = static_cast<const T16*>(x);

@@ -16,6 +16,33 @@ unsigned* device_error_word();
 // Number of SMs of the current device (cached per device).
 int num_sms();
 
+// Launches `kern` with programmatic stream serialisation (see griddep_wait in
+// common.cuh) and, when cluster_x > 0, thread-block clusters of cluster_x
+// CTAs along x (0: no cluster attribute).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       unsigned cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  unsigned n = 1;
+  if (cluster_x > 0) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // 2-D TMA map over a row-major [outer, inner] matrix with the given row pitch
 // in bytes; boxes of [box_outer, box_inner] elements, 128-byte swizzle,
 // out-of-range elements read as zero.  False if the driver rejects it.
@@ -38,6 +65,17 @@ cudaError_t launch_gemm_16(gpt2_dtype dt, const void* x, const void* w, const vo
                            void* y, int64_t M, int N, int K, int64_t ldy, bool w_out_in, int epilogue, gpt2_dtype y_t,
                            cudaStream_t stream);
 
+// The same GEMM for M <= kMaxRowsGemm rows (operands swapped, K split over a
+// thread-block cluster); launch_gemm_16 hands such calls to it.  With
+// argmax_cand (epilogue NONE, fp32 y, which may then be null) it also writes
+// per-row argmax candidates: argmax_cand[m * rows_argmax_candidates(N) + c]
+// = (value, index bits), to be reduced by launch_argmax_candidates.
+constexpr int64_t kMaxRowsGemm = 128;
+inline int rows_argmax_candidates(int N) { return 4 * ((N + 127) / 128); }
+cudaError_t launch_gemm_rows_16(gpt2_dtype dt, const void* x, const void* w, const void* bias, const float* residual,
+                                void* y, int64_t M, int N, int K, int64_t ldy, bool w_out_in, int epilogue,
+                                gpt2_dtype y_t, cudaStream_t stream, float2* argmax_cand = nullptr);
+
 // fp32 CUDA-core GEMM with the same epilogues.
 cudaError_t launch_gemm_f32(const float* x, const float* w, const float* bias, const float* residual, float* y,
                             int64_t M, int N, int K, int64_t ldy, bool w_out_in, int epilogue, cudaStream_t stream);
@@ -56,5 +94,8 @@ cudaError_t launch_decode_attention(gpt2_dtype dt, const void* qkv, void* kv_lay
                                     const int* valid, int B, int n_head, int T_max, cudaStream_t stream);
 cudaError_t launch_argmax_rows(const float* logits, int64_t ld, int B, int V, const int* valid, int32_t* next_tokens,
                                int32_t* past_len, cudaStream_t stream);
+// The same from the candidates of launch_gemm_rows_16 (n_cand per row).
+cudaError_t launch_argmax_candidates(const float2* cand, int n_cand, int B, const int* valid, int32_t* next_tokens,
+                                     int32_t* past_len, cudaStream_t stream);
 
 }  // namespace gpt2

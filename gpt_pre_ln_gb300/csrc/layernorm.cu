@@ -100,12 +100,11 @@ template <> struct Raw4<__half> {
 
 // Normalises the row held in v (NV groups of 4 per lane, lane-strided) and
 // writes it to yr.  Groups beyond D/4 hold zeros and are skipped.  gamma and
-// beta are loaded before the reductions so that their latency overlaps them.
+// beta (ln_load_affine) are loaded first, before the kernel's dependency
+// wait, so that their latency overlaps the previous kernel.
 template <typename YT, int NV>
-__device__ __forceinline__ void ln_finish(float (&v)[NV][4], int lane, int D, float eps, const YT* gamma,
-                                          const YT* beta, YT* yr) {
-  const int nvec = D >> 2;
-  Raw4<YT> g[NV], bb[NV];
+__device__ __forceinline__ void ln_load_affine(int lane, int D, const YT* gamma, const YT* beta, Raw4<YT> (&g)[NV],
+                                               Raw4<YT> (&bb)[NV]) {
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int c = (lane + i * 32) * 4;
@@ -114,6 +113,12 @@ __device__ __forceinline__ void ln_finish(float (&v)[NV][4], int lane, int D, fl
       bb[i].load(beta + c);
     }
   }
+}
+
+template <typename YT, int NV>
+__device__ __forceinline__ void ln_finish(float (&v)[NV][4], int lane, int D, float eps, const Raw4<YT> (&g)[NV],
+                                          const Raw4<YT> (&bb)[NV], YT* yr) {
+  const int nvec = D >> 2;
   float s = 0.f;
 #pragma unroll
   for (int i = 0; i < NV; ++i) s += (v[i][0] + v[i][1]) + (v[i][2] + v[i][3]);
@@ -148,8 +153,12 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_rows(const XT* __restric
                                                              const YT* __restrict__ beta, YT* __restrict__ y,
                                                              long long rows, int D, float eps) {
   const long long row = static_cast<long long>(blockIdx.x) * (kLnThreads / 32) + (threadIdx.x >> 5);
-  if (row >= rows) return;
   const int lane = threadIdx.x & 31;
+  Raw4<YT> g[NV], bb[NV];
+  ln_load_affine<YT, NV>(lane, D, gamma, beta, g, bb);
+  griddep_wait();
+  griddep_launch_dependents();
+  if (row >= rows) return;
   const XT* xr = x + row * D;
   const int nvec = D >> 2;
   float v[NV][4];
@@ -162,7 +171,7 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_rows(const XT* __restric
       v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.f;
     }
   }
-  ln_finish<YT, NV>(v, lane, D, eps, gamma, beta, y + row * D);
+  ln_finish<YT, NV>(v, lane, D, eps, g, bb, y + row * D);
 }
 
 // x[m] = wte[tokens[m]] + wpe[m % T]; y[m] = LN(x[m]).  A token id outside
@@ -173,8 +182,12 @@ __global__ void __launch_bounds__(kLnThreads)
                   const WT* __restrict__ gamma, const WT* __restrict__ beta, float* __restrict__ x,
                   WT* __restrict__ y, long long rows, int T, int D, int V, float eps, unsigned* err) {
   const long long row = static_cast<long long>(blockIdx.x) * (kLnThreads / 32) + (threadIdx.x >> 5);
-  if (row >= rows) return;
   const int lane = threadIdx.x & 31;
+  Raw4<WT> g[NV], bb[NV];
+  ln_load_affine<WT, NV>(lane, D, gamma, beta, g, bb);
+  griddep_wait();
+  griddep_launch_dependents();
+  if (row >= rows) return;
   const int pos = static_cast<int>(row % T);
   int tok = tokens[row];
   const bool tok_ok = tok >= 0 && tok < V;
@@ -201,7 +214,7 @@ __global__ void __launch_bounds__(kLnThreads)
       v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.f;
     }
   }
-  ln_finish<WT, NV>(v, lane, D, eps, gamma, beta, y + row * D);
+  ln_finish<WT, NV>(v, lane, D, eps, g, bb, y + row * D);
 }
 
 template <typename XT, typename YT>
@@ -213,17 +226,17 @@ cudaError_t ln_dispatch(const void* x, const void* g, const void* b, void* y, lo
   auto Bt = static_cast<const YT*>(b);
   auto Y = static_cast<YT*>(y);
   if (D <= 512)
-    layernorm_rows<XT, YT, 4><<<blocks, kLnThreads, 0, s>>>(X, G, Bt, Y, rows, D, eps);
+    return launch_pdl(layernorm_rows<XT, YT, 4>, blocks, kLnThreads, 0, s, 0, X, G, Bt, Y, rows, D, eps);
   else if (D <= 768)
-    layernorm_rows<XT, YT, 6><<<blocks, kLnThreads, 0, s>>>(X, G, Bt, Y, rows, D, eps);
+    return launch_pdl(layernorm_rows<XT, YT, 6>, blocks, kLnThreads, 0, s, 0, X, G, Bt, Y, rows, D, eps);
   else if (D <= 1024)
-    layernorm_rows<XT, YT, 8><<<blocks, kLnThreads, 0, s>>>(X, G, Bt, Y, rows, D, eps);
+    return launch_pdl(layernorm_rows<XT, YT, 8>, blocks, kLnThreads, 0, s, 0, X, G, Bt, Y, rows, D, eps);
   else if (D <= 1664)
-    layernorm_rows<XT, YT, 13><<<blocks, kLnThreads, 0, s>>>(X, G, Bt, Y, rows, D, eps);
+    return launch_pdl(layernorm_rows<XT, YT, 13>, blocks, kLnThreads, 0, s, 0, X, G, Bt, Y, rows, D, eps);
   else if (D <= 2048)
-    layernorm_rows<XT, YT, 16><<<blocks, kLnThreads, 0, s>>>(X, G, Bt, Y, rows, D, eps);
+    return launch_pdl(layernorm_rows<XT, YT, 16>, blocks, kLnThreads, 0, s, 0, X, G, Bt, Y, rows, D, eps);
   else
-    layernorm_rows<XT, YT, 32><<<blocks, kLnThreads, 0, s>>>(X, G, Bt, Y, rows, D, eps);
+    return launch_pdl(layernorm_rows<XT, YT, 32>, blocks, kLnThreads, 0, s, 0, X, G, Bt, Y, rows, D, eps);
   return cudaGetLastError();
 }
 
@@ -238,15 +251,20 @@ cudaError_t embed_dispatch(const int32_t* tokens, const void* wte, const void* w
   auto Y = static_cast<WT*>(y);
   unsigned* err = device_error_word();
   if (D <= 512)
-    embed_ln_rows<WT, 4><<<blocks, kLnThreads, 0, s>>>(tokens, E, P, G, Bt, x, Y, rows, T, D, V, eps, err);
+    return launch_pdl(embed_ln_rows<WT, 4>, blocks, kLnThreads, 0, s, 0, tokens, E, P, G, Bt, x, Y, rows, T, D,
+                      V, eps, err);
   else if (D <= 768)
-    embed_ln_rows<WT, 6><<<blocks, kLnThreads, 0, s>>>(tokens, E, P, G, Bt, x, Y, rows, T, D, V, eps, err);
+    return launch_pdl(embed_ln_rows<WT, 6>, blocks, kLnThreads, 0, s, 0, tokens, E, P, G, Bt, x, Y, rows, T, D,
+                      V, eps, err);
   else if (D <= 1024)
-    embed_ln_rows<WT, 8><<<blocks, kLnThreads, 0, s>>>(tokens, E, P, G, Bt, x, Y, rows, T, D, V, eps, err);
+    return launch_pdl(embed_ln_rows<WT, 8>, blocks, kLnThreads, 0, s, 0, tokens, E, P, G, Bt, x, Y, rows, T, D,
+                      V, eps, err);
   else if (D <= 2048)
-    embed_ln_rows<WT, 16><<<blocks, kLnThreads, 0, s>>>(tokens, E, P, G, Bt, x, Y, rows, T, D, V, eps, err);
+    return launch_pdl(embed_ln_rows<WT, 16>, blocks, kLnThreads, 0, s, 0, tokens, E, P, G, Bt, x, Y, rows, T, D,
+                      V, eps, err);
   else
-    embed_ln_rows<WT, 32><<<blocks, kLnThreads, 0, s>>>(tokens, E, P, G, Bt, x, Y, rows, T, D, V, eps, err);
+    return launch_pdl(embed_ln_rows<WT, 32>, blocks, kLnThreads, 0, s, 0, tokens, E, P, G, Bt, x, Y, rows, T, D,
+                      V, eps, err);
   return cudaGetLastError();
 }
 

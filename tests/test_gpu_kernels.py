@@ -80,6 +80,17 @@ LINEAR_CASES = [
     (1, 256, 64, G.W_IN_OUT),         # single row, single k-block
     (300, 1000, 768, G.W_OUT_IN),     # lm_head style, ragged N
     (130, 50257, 768, G.W_OUT_IN),    # full vocabulary
+    # few rows (one token per sequence of a decode step): the swapped-operand
+    # kernel with K split over a thread-block cluster
+    (16, 8, 64, G.W_IN_OUT),          # one partial tile, one k-block
+    (7, 2304, 768, G.W_IN_OUT),       # c_attn, 18 tiles
+    (33, 200, 192, G.W_IN_OUT),       # ragged N in the second tile, 3 k-blocks
+    (64, 768, 768, G.W_IN_OUT),       # attention c_proj at a decode batch of 64
+    (64, 768, 3072, G.W_IN_OUT),      # mlp c_proj
+    (64, 3072, 768, G.W_IN_OUT),      # c_fc
+    (100, 1000, 768, G.W_OUT_IN),     # wte layout, ragged N
+    (128, 768, 768, G.W_IN_OUT),      # the largest row count of this kernel
+    (64, 50257, 768, G.W_OUT_IN),     # lm_head of a decode step: persistent over 393 tiles
     (64, 4800, 1600, G.W_IN_OUT),     # XL c_attn: N not a multiple of 256
 ]
 
@@ -128,6 +139,24 @@ def test_linear_bf16(case, epi):
     if epi == G.EPI_BIAS_GELU:
         bound = bound + 2.0 ** -11 * np.abs(pre)
     assert_close_elementwise(got, ref, bound, f"linear epi={epi}")
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 768, 3072), (5, 2304, 768), (64, 50257, 768)])
+def test_linear_few_rows_is_deterministic(M, N, K):
+    """The split-K partial sums are added in a fixed order: two calls give
+    the same bits."""
+    r = rng(M + N)
+    layout = G.W_OUT_IN if N == 50257 else G.W_IN_OUT
+    x = to_t(bf16(r.standard_normal((M, K))), "bf16")
+    w = to_t(bf16(0.02 * r.standard_normal((K, N) if layout == G.W_IN_OUT else (N, K))), "bf16")
+    ld = (N + 3) // 4 * 4
+    ys = []
+    for _ in range(2):
+        y = torch.empty(M, ld, device="cuda", dtype=torch.float32)
+        G.gpt2_linear(x, w, None, None, y, M, N, K, ld, layout, G.EPI_NONE, G.BF16, G.F32)
+        ys.append(y)
+    torch.cuda.synchronize()
+    assert torch.equal(ys[0][:, :N], ys[1][:, :N])
 
 
 @pytest.mark.parametrize("epi", [G.EPI_BIAS, G.EPI_BIAS_GELU, G.EPI_BIAS_RESIDUAL])

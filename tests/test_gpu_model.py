@@ -281,3 +281,32 @@ def test_decode_position_out_of_range_is_reported():
     assert pl.cpu().tolist() == [4, 8]
     assert nxt.cpu().tolist()[1] == -7 and nxt.cpu().tolist()[0] >= 0
     del keep
+
+
+def test_decode_wide_batch_unfused_argmax():
+    """B = 130 sequences: past the few-row GEMM (128 rows), the lm_head
+    writes fp32 logits and a separate kernel takes the argmax; both paths
+    must pick the argmax of the step's own logits."""
+    dims = synth.Dims(n_layer=1, d_model=128, n_head=2, d_ff=512, vocab=300, n_pos=16)
+    B, T_max = 130, 8
+    past = (np.arange(B) % 5).astype(np.int32)
+    params, cache, tokens = _decode_setup(dims, B, T_max, past, 3)
+    dev = G.to_device(params, G.BF16)
+    mw, keep = G.model_weights(dev)
+    cd = _dims(dims, "bf16")
+    kv = to_t(cache, "bf16")
+    pl = torch.from_numpy(past.copy()).to("cuda")
+    tok = torch.from_numpy(tokens.copy()).to("cuda")
+    nxt = torch.empty_like(tok)
+    ld = 304
+    logits = torch.empty(B, ld, device="cuda")
+    wsb = G.gpt2_decode_workspace_bytes(cd, B)
+    ws = torch.empty(wsb, device="cuda", dtype=torch.uint8)
+    G.gpt2_decode_step(cd, mw, kv, B, T_max, pl, tok, nxt, logits, ld, ws, wsb)
+    torch.cuda.synchronize()
+    got = to_np(logits[:, :dims.vocab])
+    _, ref, _, opast = O.decode_step(params, dims, cache.astype(np.float64), past.copy(), tokens.copy())
+    _check_logits(got, ref)
+    assert np.array_equal(nxt.cpu().numpy(), np.argmax(got, -1))
+    assert np.array_equal(pl.cpu().numpy(), opast)
+    del keep
