@@ -268,15 +268,121 @@ int check_model(const gpt2_dims* dims, const gpt2_model_weights* w) {
   return GPT2_OK;
 }
 
-// Up to kMaxRowsGemm sequences the lm_head's epilogue makes argmax
-// candidates (no logits buffer); beyond, fp32 logits feed argmax_rows.
-size_t decode_ws_bytes(const gpt2_dims* d, int B) {
-  const size_t M = static_cast<size_t>(B);
+// The rows of a decode step: activations, then either the lm_head's argmax
+// candidates (up to kMaxRowsGemm rows) or a logits buffer for argmax_rows.
+size_t decode_group_ws(const gpt2_dims* d, int nb) {
+  const size_t M = static_cast<size_t>(nb);
   const size_t Vp = (static_cast<size_t>(d->vocab) + 3) & ~static_cast<size_t>(3);
-  const size_t head = B <= kMaxRowsGemm ? align256(M * rows_argmax_candidates(d->vocab) * sizeof(float2))
-                                        : align256(M * Vp * 4);
-  return acts_bytes(d, static_cast<int64_t>(M)) + head + align256(M * 4);
+  const size_t head = nb <= kMaxRowsGemm ? align256(M * rows_argmax_candidates(d->vocab) * sizeof(float2))
+                                         : align256(M * Vp * 4);
+  return acts_bytes(d, static_cast<int64_t>(M)) + head;
 }
+
+size_t decode_ws_bytes(const gpt2_dims* d, int B) {
+  return align256(static_cast<size_t>(B) * 4) + decode_group_ws(d, B);  // valid flags, then the group
+}
+
+// Buffers and phases of a decode step over rows b0 .. b0 + nb - 1 of the
+// cache's B_cache sequences.
+struct DecodeGroup {
+  const gpt2_dims* d;
+  const gpt2_model_weights* w;
+  void* kv_cache;
+  int B_cache, T_max, b0, nb;
+  int32_t* past_len;        // + b0
+  const int32_t* tokens;    // + b0
+  int32_t* next_tokens;     // + b0
+  float* logits;            // + b0 rows, or null
+  int64_t ld;
+  int* valid;               // + b0
+  Acts A;
+  float2* cand;             // fused argmax (nb <= kMaxRowsGemm)
+  float* lg;                // otherwise the logits for argmax_rows
+  cudaStream_t s;
+
+  void carve(char* base) {
+    Carve c(base);
+    const size_t M = static_cast<size_t>(nb);
+    const int D = d->d_model, F = d->d_ff, V = d->vocab;
+    A.x = c.take<float>(M * D, 4);
+    A.h = c.take<float>(M * D, 4);
+    A.a = c.take<char>(M * D, 2);
+    A.qkv = c.take<char>(M * 3 * D, 2);
+    A.o = c.take<char>(M * D, 2);
+    A.g = c.take<char>(M * F, 2);
+    cand = nullptr;
+    lg = nullptr;
+    if (nb <= kMaxRowsGemm)
+      cand = c.take<float2>(M * rows_argmax_candidates(V), sizeof(float2));
+    else
+      lg = c.take<float>(M * ((static_cast<size_t>(V) + 3) & ~static_cast<size_t>(3)), 4);
+  }
+
+  cudaError_t embed() {
+    const int D = d->d_model;
+    ProfScope prof("decode_embed_layernorm", 8.0 * nb * D, static_cast<double>(nb) * D * 10.0, s);
+    return launch_decode_embed_ln(d->dtype, tokens, past_len, w->wte, w->wpe, w->blocks[0].ln1_g,
+                                  w->blocks[0].ln1_b, A.x, A.a, nb, D, d->vocab, d->n_pos, T_max, d->eps, valid, s);
+  }
+
+  cudaError_t layer(int l) {
+    const gpt2_dtype dt = d->dtype;
+    const int D = d->d_model, F = d->d_ff, H = d->n_head;
+    const gpt2_block_weights* bw = &w->blocks[l];
+    cudaError_t e;
+    if (l > 0 && (e = layernorm(A.x, bw->ln1_g, bw->ln1_b, A.a, nb, D, d->eps, GPT2_F32, dt, s)) != cudaSuccess)
+      return e;
+    if ((e = linear(dt, A.a, bw->w_qkv, bw->b_qkv, nullptr, A.qkv, nb, 3 * D, D, 3 * D, false, GPT2_EPI_BIAS, dt,
+                    s)) != cudaSuccess)
+      return e;
+    const size_t layer_elems = static_cast<size_t>(2) * B_cache * H * static_cast<size_t>(T_max) * 64;
+    void* kv_layer = static_cast<char*>(kv_cache) + l * layer_elems * esize(dt);
+    {
+      // the cached lengths live on the device: the bytes of this kernel are
+      // left to the caller, who knows them
+      ProfScope prof("decode_attn", 0.0, 0.0, s);
+      if ((e = launch_decode_attention(dt, A.qkv, kv_layer, A.o, past_len, valid, nb, b0, B_cache, H, T_max, s)) !=
+          cudaSuccess)
+        return e;
+    }
+    if ((e = linear(dt, A.o, bw->w_o, bw->b_o, A.x, A.h, nb, D, D, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32, s)) !=
+        cudaSuccess)
+      return e;
+    if ((e = layernorm(A.h, bw->ln2_g, bw->ln2_b, A.a, nb, D, d->eps, GPT2_F32, dt, s)) != cudaSuccess) return e;
+    if ((e = linear(dt, A.a, bw->w_fc, bw->b_fc, nullptr, A.g, nb, F, D, F, false, GPT2_EPI_BIAS_GELU, dt, s)) !=
+        cudaSuccess)
+      return e;
+    return linear(dt, A.g, bw->w_proj, bw->b_proj, A.h, A.x, nb, D, F, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32, s);
+  }
+
+  cudaError_t head() {
+    const gpt2_dtype dt = d->dtype;
+    const int D = d->d_model, V = d->vocab;
+    cudaError_t e = layernorm(A.x, w->lnf_g, w->lnf_b, A.a, nb, D, d->eps, GPT2_F32, dt, s);
+    if (e != cudaSuccess) return e;
+    if (cand) {
+      const int n_cand = rows_argmax_candidates(V);
+      {
+        ProfScope prof(dt == GPT2_BF16 ? "gemm_rows_bf16_tcgen05" : "gemm_rows_f16_tcgen05", 2.0 * nb * V * D,
+                       (static_cast<double>(nb) + V) * D * esize(dt) + (logits ? 4.0 * nb * V : 0.0), s);
+        e = launch_gemm_rows_16(dt, A.a, w->wte, nullptr, nullptr, logits, nb, V, D, logits ? ld : V, true,
+                                GPT2_EPI_NONE, GPT2_F32, s, cand);
+        if (e != cudaSuccess) return e;
+      }
+      ProfScope prof("argmax_candidates", static_cast<double>(nb) * n_cand, static_cast<double>(nb) * n_cand * 8.0,
+                     s);
+      return launch_argmax_candidates(cand, n_cand, nb, valid, next_tokens, past_len, s);
+    }
+    const int64_t Vp = (static_cast<int64_t>(V) + 3) & ~static_cast<int64_t>(3);
+    float* out = logits ? logits : lg;
+    const int64_t lld = logits ? ld : Vp;
+    e = linear(dt, A.a, w->wte, nullptr, nullptr, out, nb, V, D, lld, true, GPT2_EPI_NONE, GPT2_F32, s);
+    if (e != cudaSuccess) return e;
+    ProfScope prof("argmax_rows", static_cast<double>(nb) * V, static_cast<double>(nb) * V * 4.0, s);
+    return launch_argmax_rows(out, lld, nb, V, valid, next_tokens, past_len, s);
+  }
+};
+
 
 }  // namespace
 
@@ -460,67 +566,28 @@ int gpt2_decode_step(const gpt2_dims* dims, const gpt2_model_weights* w, void* k
   if (logits_opt && ld % 4 != 0) return GPT2_ERR_UNSUPPORTED;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return GPT2_ERR_ARG;
   if (ws_bytes < decode_ws_bytes(dims, B)) return GPT2_ERR_WORKSPACE;
-  const int D = dims->d_model, F = dims->d_ff, H = dims->n_head, V = dims->vocab;
-  Carve c(ws);
-  Acts A;
-  A.x = c.take<float>(static_cast<size_t>(B) * D, 4);
-  A.h = c.take<float>(static_cast<size_t>(B) * D, 4);
-  A.a = c.take<char>(static_cast<size_t>(B) * D, 2);
-  A.qkv = c.take<char>(static_cast<size_t>(B) * 3 * D, 2);
-  A.o = c.take<char>(static_cast<size_t>(B) * D, 2);
-  A.g = c.take<char>(static_cast<size_t>(B) * F, 2);  // 16-bit paths only
-  const int64_t Vp = (static_cast<int64_t>(V) + 3) & ~static_cast<int64_t>(3);
-  const bool fused_argmax = B <= kMaxRowsGemm;
-  const int n_cand = rows_argmax_candidates(V);
-  float2* cand = nullptr;
-  float* lg = nullptr;
-  if (fused_argmax)
-    cand = c.take<float2>(static_cast<size_t>(B) * n_cand, sizeof(float2));
-  else
-    lg = c.take<float>(static_cast<size_t>(B) * Vp, 4);
-  int* valid = c.take<int>(static_cast<size_t>(B), 4);
   cudaStream_t s = cs(stream);
-  const gpt2_dtype dt = dims->dtype;
-  const size_t layer_elems = static_cast<size_t>(2) * B * H * static_cast<size_t>(T_max) * 64;
-  {
-    ProfScope prof("decode_embed_layernorm", 8.0 * B * D, static_cast<double>(B) * D * 10.0, s);
-    GPT2_CUDA(launch_decode_embed_ln(dt, tokens, past_len, w->wte, w->wpe, w->blocks[0].ln1_g, w->blocks[0].ln1_b,
-                                     A.x, A.a, B, D, V, dims->n_pos, T_max, dims->eps, valid, s));
-  }
-  for (int l = 0; l < dims->n_layer; ++l) {
-    const gpt2_block_weights* bw = &w->blocks[l];
-    if (l > 0) GPT2_CUDA(layernorm(A.x, bw->ln1_g, bw->ln1_b, A.a, B, D, dims->eps, GPT2_F32, dt, s));
-    GPT2_CUDA(linear(dt, A.a, bw->w_qkv, bw->b_qkv, nullptr, A.qkv, B, 3 * D, D, 3 * D, false, GPT2_EPI_BIAS, dt, s));
-    void* kv_layer = static_cast<char*>(kv_cache) + l * layer_elems * esize(dt);
-    {
-      // the cached lengths live on the device: the bytes of this kernel are
-      // left to the caller, who knows them
-      ProfScope prof("decode_attn", 0.0, 0.0, s);
-      GPT2_CUDA(launch_decode_attention(dt, A.qkv, kv_layer, A.o, past_len, valid, B, H, T_max, s));
-    }
-    GPT2_CUDA(linear(dt, A.o, bw->w_o, bw->b_o, A.x, A.h, B, D, D, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32, s));
-    GPT2_CUDA(layernorm(A.h, bw->ln2_g, bw->ln2_b, A.a, B, D, dims->eps, GPT2_F32, dt, s));
-    GPT2_CUDA(linear(dt, A.a, bw->w_fc, bw->b_fc, nullptr, A.g, B, F, D, F, false, GPT2_EPI_BIAS_GELU, dt, s));
-    GPT2_CUDA(linear(dt, A.g, bw->w_proj, bw->b_proj, A.h, A.x, B, D, F, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32,
-                     s));
-  }
-  GPT2_CUDA(layernorm(A.x, w->lnf_g, w->lnf_b, A.a, B, D, dims->eps, GPT2_F32, dt, s));
-  if (fused_argmax) {
-    {
-      ProfScope prof(dt == GPT2_BF16 ? "gemm_rows_bf16_tcgen05" : "gemm_rows_f16_tcgen05", 2.0 * B * V * D,
-                     (static_cast<double>(B) + V) * D * esize(dt) + (logits_opt ? 4.0 * B * V : 0.0), s);
-      GPT2_CUDA(launch_gemm_rows_16(dt, A.a, w->wte, nullptr, nullptr, logits_opt, B, V, D, logits_opt ? ld : V, true,
-                                    GPT2_EPI_NONE, GPT2_F32, s, cand));
-    }
-    ProfScope prof("argmax_candidates", static_cast<double>(B) * n_cand, static_cast<double>(B) * n_cand * 8.0, s);
-    GPT2_CUDA(launch_argmax_candidates(cand, n_cand, B, valid, next_tokens, past_len, s));
-  } else {
-    float* logits = logits_opt ? logits_opt : lg;
-    const int64_t lld = logits_opt ? ld : Vp;
-    GPT2_CUDA(linear(dt, A.a, w->wte, nullptr, nullptr, logits, B, V, D, lld, true, GPT2_EPI_NONE, GPT2_F32, s));
-    ProfScope prof("argmax_rows", static_cast<double>(B) * V, static_cast<double>(B) * V * 4.0, s);
-    GPT2_CUDA(launch_argmax_rows(logits, lld, B, V, valid, next_tokens, past_len, s));
-  }
+  char* base = static_cast<char*>(ws);
+  int* valid = reinterpret_cast<int*>(base);
+  DecodeGroup G;
+  G.d = dims;
+  G.w = w;
+  G.kv_cache = kv_cache;
+  G.B_cache = B;
+  G.T_max = T_max;
+  G.b0 = 0;
+  G.nb = B;
+  G.past_len = past_len;
+  G.tokens = tokens;
+  G.next_tokens = next_tokens;
+  G.logits = logits_opt;
+  G.ld = ld;
+  G.valid = valid;
+  G.carve(base + align256(static_cast<size_t>(B) * 4));
+  G.s = s;
+  GPT2_CUDA(G.embed());
+  for (int l = 0; l < dims->n_layer; ++l) GPT2_CUDA(G.layer(l));
+  GPT2_CUDA(G.head());
   return GPT2_OK;
 }
 

@@ -93,16 +93,17 @@ constexpr int kDaSmem = kDaWarps * kDaStages * kDaStageBytes + 1024;  // + slack
 template <typename T16>
 __global__ void __launch_bounds__(kDaWarps * 32, 6)
     decode_attn_tma(const __grid_constant__ CUtensorMap kv_map, const T16* __restrict__ qkv, T16* kv_layer,
-                    T16* __restrict__ out, const int32_t* __restrict__ past_len, const int* __restrict__ valid, int B,
-                    int H, int T_max, unsigned* err) {
+                    T16* __restrict__ out, const int32_t* __restrict__ past_len, const int* __restrict__ valid,
+                    int b_cache0, int B_cache, int H, int T_max, unsigned* err) {
   extern __shared__ uint8_t da_smem_raw[];
   __shared__ __align__(8) uint64_t bars[kDaWarps][kDaStages];
   __shared__ float s_q[kHd];
   __shared__ __align__(16) float s_p[kDaWarps][kDaChunk];  // key k at (k & 1) * 8 + (k >> 1)
   __shared__ float s_m[kDaWarps + 1], s_l[kDaWarps + 1];
   __shared__ __align__(16) float s_acc[kDaWarps + 1][kHd];
-  const int b = blockIdx.x / H;
+  const int b = blockIdx.x / H;  // sequence within this call's rows
   const int h = blockIdx.x % H;
+  const int bc = b_cache0 + b;   // and its index in the cache
   const int D = H * kHd;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -117,8 +118,8 @@ __global__ void __launch_bounds__(kDaWarps * 32, 6)
   uint8_t* wbuf = smem + warp * kDaStages * kDaStageBytes;
   const int n_chunks = (pos + kDaChunk - 1) / kDaChunk;
   const int my_chunks = n_chunks > warp ? (n_chunks - warp + kDaWarps - 1) / kDaWarps : 0;
-  const int row_k = (b * H + h) * T_max;  // row of slot 0 of this (b, h) in the K half
-  const int row_v = row_k + B * H * T_max;  // and in the V half
+  const int row_k = (bc * H + h) * T_max;      // row of slot 0 of this (b, h) in the K half
+  const int row_v = row_k + B_cache * H * T_max;  // and in the V half
   auto issue = [&](int i) {
     const int st = i % kDaStages;
     const int j0 = (warp + i * kDaWarps) * kDaChunk;
@@ -365,23 +366,27 @@ cudaError_t launch_decode_embed_ln(gpt2_dtype dt, const int32_t* tokens, const i
 namespace {
 template <typename T16>
 cudaError_t launch_decode_attn_t(const void* qkv, void* kv_layer, void* out, const int32_t* past_len, const int* valid,
-                                 int B, int n_head, int T_max, cudaStream_t stream) {
-  // the layer's K and V halves as one [2 * B * n_head * T_max, 64] matrix
-  const uint64_t rows = 2ull * B * n_head * static_cast<uint64_t>(T_max);
+                                 int B, int b_cache0, int B_cache, int n_head, int T_max, cudaStream_t stream) {
+  // the layer's K and V halves as one [2 * B_cache * n_head * T_max, 64] matrix
+  const uint64_t rows = 2ull * B_cache * n_head * static_cast<uint64_t>(T_max);
   if (rows >= (1ull << 31)) return cudaErrorInvalidValue;
   CUtensorMap map;
   if (!encode_tma_2d(&map, Type16<T16>::kTma, kv_layer, kHd, rows, kHd * 2, kHd, kDaChunk))
     return cudaErrorInvalidValue;
   return launch_pdl(decode_attn_tma<T16>, B * n_head, kDaWarps * 32, kDaSmem, stream, 0, map,
                     static_cast<const T16*>(qkv), static_cast<T16*>(kv_layer), static_cast<T16*>(out), past_len,
-                    valid, B, n_head, T_max, device_error_word());
+                    valid, b_cache0, B_cache, n_head, T_max, device_error_word());
 }
 }  // namespace
 
 cudaError_t launch_decode_attention(gpt2_dtype dt, const void* qkv, void* kv_layer, void* out, const int32_t* past_len,
-                                    const int* valid, int B, int n_head, int T_max, cudaStream_t stream) {
-  if (dt == GPT2_F16) return launch_decode_attn_t<__half>(qkv, kv_layer, out, past_len, valid, B, n_head, T_max, stream);
-  return launch_decode_attn_t<__nv_bfloat16>(qkv, kv_layer, out, past_len, valid, B, n_head, T_max, stream);
+                                    const int* valid, int B, int b_cache0, int B_cache, int n_head, int T_max,
+                                    cudaStream_t stream) {
+  if (dt == GPT2_F16)
+    return launch_decode_attn_t<__half>(qkv, kv_layer, out, past_len, valid, B, b_cache0, B_cache, n_head, T_max,
+                                        stream);
+  return launch_decode_attn_t<__nv_bfloat16>(qkv, kv_layer, out, past_len, valid, B, b_cache0, B_cache, n_head,
+                                             T_max, stream);
 }
 
 cudaError_t launch_argmax_candidates(const float2* cand, int n_cand, int B, const int* valid, int32_t* next_tokens,

@@ -90,8 +90,11 @@ cudaError_t launch_attention_f32(const float* qkv, float* out, int B, int T, int
 cudaError_t launch_decode_embed_ln(gpt2_dtype dt, const int32_t* tokens, const int32_t* past_len, const void* wte,
                                    const void* wpe, const void* gamma, const void* beta, float* x, void* y, int B,
                                    int D, int V, int n_pos, int T_max, float eps, int* valid, cudaStream_t stream);
+// Rows 0..B-1 of qkv / out / past_len / valid are sequences b_cache0 ..
+// b_cache0 + B - 1 of a cache laid out for B_cache sequences.
 cudaError_t launch_decode_attention(gpt2_dtype dt, const void* qkv, void* kv_layer, void* out, const int32_t* past_len,
-                                    const int* valid, int B, int n_head, int T_max, cudaStream_t stream);
+                                    const int* valid, int B, int b_cache0, int B_cache, int n_head, int T_max,
+                                    cudaStream_t stream);
 cudaError_t launch_argmax_rows(const float* logits, int64_t ld, int B, int V, const int* valid, int32_t* next_tokens,
                                int32_t* past_len, cudaStream_t stream);
 // The same from the candidates of launch_gemm_rows_16 (n_cand per row).

@@ -253,7 +253,10 @@ size_t gpt2_decode_workspace_bytes(const gpt2_dims *dims, int B);
  *   (they may be the same buffer); logits_opt: NULL or fp32 [B, ld] device
  *   receiving the step's logits (ld >= vocab, a multiple of 4); ws of
  *   gpt2_decode_workspace_bytes(dims, B) bytes.  16-bit paths only (BF16,
- *   F16: GPT2_ERR_UNSUPPORTED for F32), and 2 * B * n_head * T_max < 2^31. */
+ *   F16: GPT2_ERR_UNSUPPORTED for F32), and 2 * B * n_head * T_max < 2^31.
+ *   Everything runs on `stream` and allocates nothing, so after a first call
+ *   on a device (which sets kernel attributes) the call may be captured into
+ *   a CUDA graph and replayed. */
 int gpt2_decode_step(const gpt2_dims *dims, const gpt2_model_weights *w, void *kv_cache, int B, int T_max,
                      int32_t *past_len, const int32_t *tokens, int32_t *next_tokens, float *logits_opt, int64_t ld,
                      void *ws, size_t ws_bytes, gpt2_stream_t stream);

@@ -283,13 +283,16 @@ def test_decode_position_out_of_range_is_reported():
     del keep
 
 
-def test_decode_wide_batch_unfused_argmax():
-    """B = 130 sequences: past the few-row GEMM (128 rows), the lm_head
-    writes fp32 logits and a separate kernel takes the argmax; both paths
-    must pick the argmax of the step's own logits."""
-    dims = synth.Dims(n_layer=1, d_model=128, n_head=2, d_ff=512, vocab=300, n_pos=16)
-    B, T_max = 130, 8
-    past = (np.arange(B) % 5).astype(np.int32)
+@pytest.mark.parametrize("B", [20, 130])
+def test_decode_batches(B):
+    """Sequences with mixed cache lengths.  At B = 130 the batch is past the
+    few-row GEMM (128 rows), so the lm_head writes fp32 logits and a separate
+    kernel takes the argmax; below, the lm_head's epilogue makes argmax
+    candidates.  Both must pick the argmax of the step's own logits and
+    match the oracle."""
+    dims = synth.Dims(n_layer=2, d_model=128, n_head=2, d_ff=512, vocab=300, n_pos=16)
+    T_max = 8
+    past = (np.arange(B) % 7).astype(np.int32)
     params, cache, tokens = _decode_setup(dims, B, T_max, past, 3)
     dev = G.to_device(params, G.BF16)
     mw, keep = G.model_weights(dev)
@@ -305,8 +308,13 @@ def test_decode_wide_batch_unfused_argmax():
     G.gpt2_decode_step(cd, mw, kv, B, T_max, pl, tok, nxt, logits, ld, ws, wsb)
     torch.cuda.synchronize()
     got = to_np(logits[:, :dims.vocab])
-    _, ref, _, opast = O.decode_step(params, dims, cache.astype(np.float64), past.copy(), tokens.copy())
+    _, ref, ocache, opast = O.decode_step(params, dims, cache.astype(np.float64), past.copy(), tokens.copy())
     _check_logits(got, ref)
     assert np.array_equal(nxt.cpu().numpy(), np.argmax(got, -1))
     assert np.array_equal(pl.cpu().numpy(), opast)
+    kv_np = to_np(kv)
+    for b in range(B):  # the new slot of every sequence, in its own cache rows
+        s_ = past[b]
+        assert rel_l2(kv_np[:, :, b, :, s_], ocache[:, :, b, :, s_]) < 2e-2, b
+        assert np.all(kv_np[:, :, b, :, s_ + 1:] == 0)
     del keep
