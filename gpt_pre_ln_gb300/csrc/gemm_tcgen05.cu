@@ -53,6 +53,14 @@ constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kWarpStageBytes = 4096;   // 32 rows x 128 bytes per epilogue warp
 constexpr int kSmemLimit = 232448;      // 227 KB opt-in maximum per block
+#ifndef GPT2_GEMM_1SM_CLUSTER
+#define GPT2_GEMM_1SM_CLUSTER 1
+#endif
+// 1 or 2.  Clusters of two cut each SM's operand bytes per k-block by a
+// third on the D-wide GEMMs, but measured slightly slower on the GPT-2 small
+// forward (the pairs' lock step and fewer resident CTAs), so one is the
+// default; 2 builds and passes the same tests.
+constexpr int kOneSmCluster = GPT2_GEMM_1SM_CLUSTER;
 
 enum Epi : int { EPI_NONE = 0, EPI_BIAS = 1, EPI_GELU = 2, EPI_RES = 3 };
 
@@ -131,10 +139,19 @@ struct EpiArgs {
 
 // Epilogue role (warps 2-9).  Tiles tile_begin, tile_begin + tile_stride, ...
 // < num_tiles; tile t covers rows (t % m_units) * unit_rows + row_off
-// .. + 127 and columns (t / m_units) * BN .. + BN - 1.  After reading its last
-// accumulator columns of a tile, every thread arrives once on the tile's
-// accumulator-empty barrier: locally, or at a cluster address when
-// CLUSTER_ARRIVE (the barrier of the pair's even CTA).
+// .. + 127 and columns (t / m_units) * BN .. + BN - 1.  Every thread arrives
+// once per tile on the accumulator-empty barrier of the tile's accumulator:
+// locally, or at a cluster address when CLUSTER_ARRIVE (the barrier of the
+// pair's even CTA).
+//   Other epilogues: the arrival comes after the thread's last read of the
+//   tile's accumulator, and means "free for the tile after next".
+//   EPI_RES: the accumulator of a tile starts from residual + bias (fp32),
+//   written into tensor memory by these warps before the tile's MMAs, which
+//   then accumulate on top of it.  Each warp preloads its 32 rows of the
+//   first two tiles up front and, after reading out tile t, those of tile
+//   t + 2 into the same accumulator; the arrival follows each preload.  The
+//   residual loads thus run while the MMAs of the other accumulator do, and
+//   the read-out has no global loads left.
 template <int BN, int EPI, typename OutT, typename T16, bool CLUSTER_ARRIVE>
 __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, int warp, int lane, uint32_t stage_base,
                                               uint32_t tmem_base, uint32_t tfull0, uint32_t tfull1, uint32_t tempty0,
@@ -146,50 +163,104 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, int w
   const int half = (warp - 2) >> 2;
   const uint32_t stage_w = stage_base + (warp - 2) * kWarpStageBytes;
   const int M = a.M, N = a.N;
+  auto arrive_empty = [&](int acc) {
+    tc_fence_before();
+    const uint32_t tempty = acc ? tempty1 : tempty0;
+    if (CLUSTER_ARRIVE)
+      mbar_arrive_cluster(tempty);
+    else
+      mbar_arrive(tempty);
+  };
+
+  // ---- EPI_RES: residual + bias into the accumulator of `tile`
+  // residual chunk (fp32, 32 columns) of rows row0..row0+31: coalesced
+  // loads, 4 rows of 128 B per instruction
+  auto load_res = [&](float4 (&r)[8], int row0, int col0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = i * 4 + (lane >> 3);
+      const int cc = col0 + (lane & 7) * 4;
+      r[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (row0 + rr < M && cc < N)
+        r[i] = *reinterpret_cast<const float4*>(a.residual + static_cast<long long>(row0 + rr) * N + cc);
+    }
+  };
+  // transpose a chunk through the staging area (row = lane), add the bias
+  // of its columns and store it into tensor memory
+  auto put_res = [&](const float4 (&r)[8], uint32_t t_col, int col0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(stage_w + swz(i * 4 + (lane >> 3), lane & 7)),
+                   "f"(r[i].x), "f"(r[i].y), "f"(r[i].z), "f"(r[i].w)
+                   : "memory");
+    __syncwarp();
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float4 q;
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(q.x), "=f"(q.y), "=f"(q.z), "=f"(q.w)
+                   : "r"(stage_w + swz(lane, j)));
+      v[4 * j] = q.x;
+      v[4 * j + 1] = q.y;
+      v[4 * j + 2] = q.z;
+      v[4 * j + 3] = q.w;
+    }
+    __syncwarp();
+    apply_bias_act<EPI_BIAS, float, T16>(v, a.bias, col0, N);
+    tmem_st_32x32b_x32(t_col, v);
+  };
+  auto preload = [&](int tile, int acc) {
+    const int m0 = (tile % m_units) * unit_rows + row_off;
+    const int n0 = (tile / m_units) * BN;
+    const int row0 = m0 + quad * 32;
+    const int valid_cols = N - n0 < BN ? N - n0 : BN;
+    const int nch = (valid_cols + CW - 1) / CW;
+    const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+    // two chunks in flight (chunks c and c + 2 of this half), no copies
+    float4 ra[8], rb[8];
+    int c = half;
+    if (c < nch) load_res(ra, row0, n0 + c * CW);
+    while (c < nch) {
+      if (c + 2 < nch) load_res(rb, row0, n0 + (c + 2) * CW);
+      put_res(ra, t_addr + c * CW, n0 + c * CW);
+      c += 2;
+      if (c >= nch) break;
+      if (c + 2 < nch) load_res(ra, row0, n0 + (c + 2) * CW);
+      put_res(rb, t_addr + c * CW, n0 + c * CW);
+      c += 2;
+    }
+    tmem_st_wait();
+    arrive_empty(acc);
+  };
+  if constexpr (EPI == EPI_RES) {
+    if (tile_begin < num_tiles) preload(tile_begin, 0);
+    if (tile_begin + tile_stride < num_tiles) preload(tile_begin + tile_stride, 1);
+  }
+
   int t_local = 0;
   for (int tile = tile_begin; tile < num_tiles; tile += tile_stride, ++t_local) {
     const int acc = t_local & 1;
     const uint32_t acc_par = (t_local >> 1) & 1;
-    const uint32_t tempty = acc ? tempty1 : tempty0;
+    const int m0 = (tile % m_units) * unit_rows + row_off;
+    const int n0 = (tile / m_units) * BN;
+    const int row0 = m0 + quad * 32;  // first row of this warp
+    const int valid_cols = N - n0 < BN ? N - n0 : BN;
+    const int nch = (valid_cols + CW - 1) / CW;
     const bool got = mbar_wait(acc ? tfull1 : tfull0, acc_par);
     if (!__all_sync(0xffffffffu, got)) {
       if (lane == 0) record_error(a.err, kErrTimeout, kSiteGemmEpilogue);
       return;
     }
     tc_fence_after();
-    const int m0 = (tile % m_units) * unit_rows + row_off;
-    const int n0 = (tile / m_units) * BN;
-    const int row0 = m0 + quad * 32;  // first row of this warp
-    const int valid_cols = N - n0 < BN ? N - n0 : BN;
-    const int nch = (valid_cols + CW - 1) / CW;
     // the last chunk of this half in the tile, after which its accumulator
     // columns are no longer read (-1: none)
     const int last_c = (nch - 1 - half) >= 0 ? nch - 1 - ((nch - 1 - half) & 1) : -1;
     const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
-    auto release = [&]() {
-      tc_fence_before();
-      if (CLUSTER_ARRIVE)
-        mbar_arrive_cluster(tempty);
-      else
-        mbar_arrive(tempty);
-    };
-    if (last_c < 0) release();
+    if (EPI != EPI_RES && last_c < 0) arrive_empty(acc);
 #pragma unroll 1
     for (int c = half; c < nch; c += 2) {
       const int col0 = n0 + c * CW;
-      // residual chunk (fp32, 32 columns): coalesced loads, 4 rows of 128 B
-      // per instruction, issued before the tensor-memory reads
-      float4 res[8];
-      if (EPI == EPI_RES) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = i * 4 + (lane >> 3);
-          const int cc = col0 + (lane & 7) * 4;
-          res[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (row0 + rr < M && cc < N)
-            res[i] = *reinterpret_cast<const float4*>(a.residual + static_cast<long long>(row0 + rr) * N + cc);
-        }
-      }
       float v[CW];
       {
         uint32_t raw[32];
@@ -201,29 +272,8 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, int w
           for (int i = 0; i < 32; ++i) v[l * 32 + i] = __uint_as_float(raw[i]);
         }
       }
-      if (c == last_c) release();  // this half has read its last columns
-      apply_bias_act<EPI, OutT, T16>(v, a.bias, col0, N);
-      if (EPI == EPI_RES) {
-        // transpose the residual through the staging area: row = lane
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(stage_w + swz(i * 4 + (lane >> 3), lane & 7)),
-                       "f"(res[i].x), "f"(res[i].y), "f"(res[i].z), "f"(res[i].w)
-                       : "memory");
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float4 q;
-          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                       : "=f"(q.x), "=f"(q.y), "=f"(q.z), "=f"(q.w)
-                       : "r"(stage_w + swz(lane, j)));
-          v[4 * j] += q.x;
-          v[4 * j + 1] += q.y;
-          v[4 * j + 2] += q.z;
-          v[4 * j + 3] += q.w;
-        }
-        __syncwarp();
-      }
+      if (EPI != EPI_RES && c == last_c) arrive_empty(acc);  // this half has read its last columns
+      if constexpr (EPI != EPI_RES) apply_bias_act<EPI, OutT, T16>(v, a.bias, col0, N);
       // this lane's row (128 bytes) into the staging area
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -263,6 +313,10 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, int w
       }
       __syncwarp();
     }
+    if constexpr (EPI == EPI_RES) {
+      const int next = tile + 2 * tile_stride;  // the next tile on this accumulator
+      if (next < num_tiles) preload(next, acc);
+    }
   }
 }
 
@@ -282,6 +336,13 @@ __device__ __forceinline__ void drain_loads(long long issued, FullBar full_bar, 
 }
 
 // ------------------------------------------------------------------ 1 SM
+// Launched alone (a cluster of one) or as clusters of C = 2 CTAs that work
+// on vertically adjacent tiles of the same column block: each CTA loads half
+// of the k-rows (or columns) of the shared W tile and multicasts it into both
+// CTAs' shared memory, which cuts the operand bytes each SM takes in per
+// k-block from A + W to A + W/2.  A stage is refilled only when the MMAs of
+// both CTAs have read it (each MMA commit arrives on the empty barriers of
+// both), and neither CTA leaves before the other is done.
 template <int BN, bool B_MN, int EPI, typename OutT, typename T16>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_1sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -305,9 +366,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int M = ea.M, N = ea.N;
+  const int C = static_cast<int>(cluster_nctarank());  // 1 or 2
+  const int rank = static_cast<int>(cluster_ctarank());
+  const uint16_t cmask = static_cast<uint16_t>((1u << C) - 1u);
   const int m_tiles = (M + kBM - 1) / kBM;
   const int n_tiles = (N + BN - 1) / BN;
-  const int num_tiles = m_tiles * n_tiles;
+  const int m_groups = (m_tiles + C - 1) / C;  // C vertically adjacent tiles per cluster tile
+  const int num_tiles = m_groups * n_tiles;     // cluster tiles
+  const int tile0 = blockIdx.x / C, tile_step = gridDim.x / C;
   const int k_blocks = K / kBK;
 
   if (threadIdx.x == 0) {
@@ -315,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), C);  // the MMA commits of every CTA of the cluster
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -342,9 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int m0 = (tile % m_tiles) * kBM;
-        const int n0 = (tile / m_tiles) * BN;
+      for (int tile = tile0; tile < num_tiles && ok; tile += tile_step) {
+        const int m0 = ((tile % m_groups) * C + rank) * kBM;
+        const int n0 = (tile / m_groups) * BN;
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1)) {
             record_error(err, kErrTimeout, kSiteGemmProducer);
@@ -354,13 +420,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
           tma_load_2d(smem_u32(sA + stage * Cfg::A_BYTES), &tmA, full_bar(stage), kb * kBK, m0);
           const uint32_t b_dst = smem_u32(sB + stage * Cfg::B_BYTES);
-          if constexpr (B_MN) {
-            // W [K, N]: one box of 64 N-columns x 64 K-rows per 64-wide atom
+          if (C == 1) {
+            if constexpr (B_MN) {
+              // W [K, N]: one box of 64 N-columns x 64 K-rows per 64-wide atom
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(b_dst + j * (kBK * 128), &tmB, full_bar(stage), n0 + j * 64, kb * kBK);
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(b_dst + j * (kBK * 128), &tmB, full_bar(stage), n0 + j * 64, kb * kBK);
+            } else {
+              tma_load_2d(b_dst, &tmB, full_bar(stage), kb * kBK, n0);
+            }
           } else {
-            tma_load_2d(b_dst, &tmB, full_bar(stage), kb * kBK, n0);
+            // this CTA's half of W, into both CTAs: k-rows rank*32.. of each
+            // [64 x 64] atom (W [K, N]), or rows rank*BN/2.. (W [N, K])
+            if constexpr (B_MN) {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d_multicast(b_dst + j * (kBK * 128) + rank * (kBK / 2) * 128, &tmB, full_bar(stage),
+                                      n0 + j * 64, kb * kBK + rank * (kBK / 2), cmask);
+            } else {
+              tma_load_2d_multicast(b_dst + rank * (BN / 2) * 128, &tmB, full_bar(stage), kb * kBK,
+                                    n0 + rank * (BN / 2), cmask);
+            }
           }
           ++issued;
           if (++stage == STAGES) {
@@ -380,10 +460,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int t_local = 0;
       bool ok = true;
       bool any = false;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++t_local) {
+      for (int tile = tile0; tile < num_tiles && ok; tile += tile_step, ++t_local) {
         const int acc = t_local & 1;
         const uint32_t acc_par = (t_local >> 1) & 1;
-        if (!mbar_wait(tempty_bar(acc), acc_par ^ 1)) {
+        // EPI_RES: wait for this tile's residual preload (every use);
+        // otherwise for the read-out of the tile before last (none at first)
+        if (!mbar_wait(tempty_bar(acc), EPI == EPI_RES ? acc_par : acc_par ^ 1)) {
           record_error(err, kErrTimeout, kSiteGemmMma);
           break;
         }
@@ -410,10 +492,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               bdesc = sdesc_sw128(b_base + k * 32, 16, 1024);
             }
-            umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_bf16(d_tmem, adesc, bdesc, idesc, (EPI == EPI_RES || (kb | k) != 0) ? 1u : 0u);
             any = true;
           }
-          umma_commit(empty_bar(stage));
+          if (C == 1)
+            umma_commit(empty_bar(stage));
+          else
+            umma_commit_multicast(empty_bar(stage), cmask);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -430,12 +515,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     epilogue_role<BN, EPI, OutT, T16, false>(ea, warp, lane, smem_u32(sOut), tmem_base, tfull_bar(0), tfull_bar(1),
-                                         tempty_bar(0), tempty_bar(1), blockIdx.x, gridDim.x, num_tiles, m_tiles, kBM,
-                                         0);
+                                         tempty_bar(0), tempty_bar(1), tile0, tile_step, num_tiles, m_groups, C * kBM,
+                                         rank * kBM);
   }
 
   tc_fence_before();
   __syncthreads();
+  // no CTA leaves while the other may still multicast into its shared memory
+  // or arrive on its barriers
+  if (C > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
@@ -551,7 +639,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int tile = pair; tile < num_tiles && ok; tile += num_pairs, ++t_local) {
         const int acc = t_local & 1;
         const uint32_t acc_par = (t_local >> 1) & 1;
-        if (!mbar_wait(tempty_bar(acc), acc_par ^ 1)) {
+        // EPI_RES: wait for this tile's residual preload (every use);
+        // otherwise for the read-out of the tile before last (none at first)
+        if (!mbar_wait(tempty_bar(acc), EPI == EPI_RES ? acc_par : acc_par ^ 1)) {
           record_error(err, kErrTimeout, kSiteGemmMma);
           break;
         }
@@ -575,7 +665,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             } else {
               bdesc = sdesc_sw128(b_base + k * 32, 16, 1024);
             }
-            umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (EPI == EPI_RES || (kb | k) != 0) ? 1u : 0u);
             any = true;
           }
           umma_commit_pair_multicast(empty_bar(stage), kBoth);
@@ -637,12 +727,41 @@ cudaError_t run_1sm(const T16* x, const T16* w, const EpiArgs<OutT, T16>& ea, in
   cudaError_t e = set_smem_once(kern, Cfg::SMEM_BYTES, configured);
   if (e != cudaSuccess) return e;
   const int M = ea.M, N = ea.N;
+  const int m_tiles = (M + kBM - 1) / kBM;
+  // clusters of kOneSmCluster (W shared by multicast) when there are two row tiles
+  const int C = m_tiles >= 2 ? kOneSmCluster : 1;
   CUtensorMap ta, tb;
   if (!make_map(&ta, dt, x, K, M, kBM)) return cudaErrorInvalidValue;
-  if (!(B_MN ? make_map(&tb, dt, w, N, K, kBK) : make_map(&tb, dt, w, K, N, BN))) return cudaErrorInvalidValue;
-  const int tiles = ((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
-  const int grid = tiles < num_sms() ? tiles : num_sms();
-  return launch_pdl(kern, grid, kThreads, Cfg::SMEM_BYTES, stream, 0, ta, tb, ea, K);
+  if (!(B_MN ? make_map(&tb, dt, w, N, K, kBK / C) : make_map(&tb, dt, w, K, N, BN / C)))
+    return cudaErrorInvalidValue;
+  const int cluster_tiles = ((m_tiles + C - 1) / C) * ((N + BN - 1) / BN);
+  int max_clusters = num_sms() / C;
+  if (C > 1) {
+    // clusters resident at once (the two CTAs need two SMs of one GPC)
+    static int known[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64) {
+      if (known[dev] == 0) {
+        cudaLaunchConfig_t qc = {};
+        qc.gridDim = dim3(C * (num_sms() / C), 1, 1);
+        qc.blockDim = dim3(kThreads, 1, 1);
+        qc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        cudaLaunchAttribute qa;
+        qa.id = cudaLaunchAttributeClusterDimension;
+        qa.val.clusterDim.x = C;
+        qa.val.clusterDim.y = 1;
+        qa.val.clusterDim.z = 1;
+        qc.attrs = &qa;
+        qc.numAttrs = 1;
+        int n = 0;
+        known[dev] = (cudaOccupancyMaxActiveClusters(&n, kern, &qc) == cudaSuccess && n > 0) ? n : num_sms() / C;
+      }
+      max_clusters = std::min(known[dev], num_sms() / C);
+    }
+  }
+  const int clusters = cluster_tiles < max_clusters ? cluster_tiles : max_clusters;
+  return launch_pdl(kern, C * clusters, kThreads, Cfg::SMEM_BYTES, stream, static_cast<unsigned>(C), ta, tb, ea, K);
 }
 
 template <bool B_MN, int EPI, typename OutT, typename T16>
