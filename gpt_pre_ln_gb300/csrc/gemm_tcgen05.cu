@@ -98,25 +98,35 @@ __device__ __forceinline__ void apply_bias_act(float (&v)[OutTraits<OutT>::CW], 
                                                int col0, int N) {
   constexpr int CW = OutTraits<OutT>::CW;
   if constexpr (EPI != EPI_NONE) {
+    // all 16-byte bias loads first (independent, so their latencies
+    // overlap), then the adds; a group that crosses column N is read
+    // element by element
+    uint4 raw[CW / 8];
 #pragma unroll
     for (int q = 0; q < CW / 8; ++q) {
       const int c = col0 + q * 8;
-      float b[8];
-      if (c + 8 <= N) {
-        uint4 u = __ldg(reinterpret_cast<const uint4*>(bias + c));
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      raw[q] = c + 8 <= N ? __ldg(reinterpret_cast<const uint4*>(bias + c)) : make_uint4(0u, 0u, 0u, 0u);
+    }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float2 f = Type16<T16>::unpack2(w[e]);
-          b[2 * e] = f.x;
-          b[2 * e + 1] = f.y;
-        }
-      } else {
+    for (int q = 0; q < CW / 8; ++q) {
+      const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) b[e] = (c + e < N) ? to_f32<T16>(bias[c + e]) : 0.f;
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = Type16<T16>::unpack2(w[e]);
+        v[q * 8 + 2 * e] += f.x;
+        v[q * 8 + 2 * e + 1] += f.y;
       }
+    }
+    if (col0 + CW > N) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) v[q * 8 + e] += b[e];
+      for (int q = 0; q < CW / 8; ++q) {
+        const int c = col0 + q * 8;
+        if (c < N && c + 8 > N) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (c + e < N) v[q * 8 + e] += to_f32<T16>(bias[c + e]);
+        }
+      }
     }
   }
   // 16-bit outputs: one hardware tanh per element (absolute error below
@@ -153,7 +163,8 @@ struct EpiArgs {
 //   residual loads thus run while the MMAs of the other accumulator do, and
 //   the read-out has no global loads left.
 template <int BN, int EPI, typename OutT, typename T16, bool CLUSTER_ARRIVE>
-__device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, int warp, int lane, uint32_t stage_base,
+__device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const CUtensorMap* tmY, int warp, int lane,
+                                              uint32_t stage_base,
                                               uint32_t tmem_base, uint32_t tfull0, uint32_t tfull1, uint32_t tempty0,
                                               uint32_t tempty1, int tile_begin, int tile_stride, int num_tiles,
                                               int m_units, int unit_rows, int row_off) {
@@ -163,6 +174,12 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, int w
   const int half = (warp - 2) >> 2;
   const uint32_t stage_w = stage_base + (warp - 2) * kWarpStageBytes;
   const int M = a.M, N = a.N;
+  // the staging area is rewritten only once the TMA store of its previous
+  // contents has read it
+  auto staging_free = [&]() {
+    if (lane == 0) bulk_wait_group_read<0>();
+    __syncwarp();
+  };
   auto arrive_empty = [&](int acc) {
     tc_fence_before();
     const uint32_t tempty = acc ? tempty1 : tempty0;
@@ -188,6 +205,7 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, int w
   // transpose a chunk through the staging area (row = lane), add the bias
   // of its columns and store it into tensor memory
   auto put_res = [&](const float4 (&r)[8], uint32_t t_col, int col0) {
+    staging_free();
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(stage_w + swz(i * 4 + (lane >> 3), lane & 7)),
@@ -247,9 +265,20 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, int w
     const int row0 = m0 + quad * 32;  // first row of this warp
     const int valid_cols = N - n0 < BN ? N - n0 : BN;
     const int nch = (valid_cols + CW - 1) / CW;
+    if constexpr (EPI != EPI_NONE && EPI != EPI_RES) {
+      // bring the bias of this warp's chunks into L1 while the MMAs run
+      constexpr int kLines = CW * static_cast<int>(sizeof(T16)) / 128 > 0 ? CW * static_cast<int>(sizeof(T16)) / 128 : 1;
+      const int k = lane / kLines;  // chunk half + 2k
+      const int c = half + 2 * k;
+      const int col = n0 + c * CW + (lane % kLines) * (128 / static_cast<int>(sizeof(T16)));
+      if (c < nch && col < N) asm volatile("prefetch.global.L1 [%0];" ::"l"(a.bias + col));
+    }
     const bool got = mbar_wait(acc ? tfull1 : tfull0, acc_par);
     if (!__all_sync(0xffffffffu, got)) {
-      if (lane == 0) record_error(a.err, kErrTimeout, kSiteGemmEpilogue);
+      if (lane == 0) {
+        record_error(a.err, kErrTimeout, kSiteGemmEpilogue);
+        bulk_wait_group<0>();
+      }
       return;
     }
     tc_fence_after();
@@ -263,18 +292,20 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, int w
       const int col0 = n0 + c * CW;
       float v[CW];
       {
-        uint32_t raw[32];
+        uint32_t raw[OT::LD][32];
 #pragma unroll
-        for (int l = 0; l < OT::LD; ++l) {
-          tmem_ld_32x32b_x32(t_addr + c * CW + l * 32, raw);
-          tmem_ld_wait();
+        for (int l = 0; l < OT::LD; ++l) tmem_ld_32x32b_x32(t_addr + c * CW + l * 32, raw[l]);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[l * 32 + i] = __uint_as_float(raw[i]);
-        }
+        for (int l = 0; l < OT::LD; ++l)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[l * 32 + i] = __uint_as_float(raw[l][i]);
       }
       if (EPI != EPI_RES && c == last_c) arrive_empty(acc);  // this half has read its last columns
       if constexpr (EPI != EPI_RES) apply_bias_act<EPI, OutT, T16>(v, a.bias, col0, N);
-      // this lane's row (128 bytes) into the staging area
+      // this lane's row (128 bytes) into the staging area (the 128-byte
+      // swizzled layout of a [32 x 128 B] TMA box)
+      staging_free();
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         uint32_t w0, w1, w2, w3;
@@ -293,31 +324,22 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, int w
                      "r"(w2), "r"(w3)
                      : "memory");
       }
+      // and out to global memory by one TMA store of the warp's 32 rows; the
+      // tensor map ends at the 16-byte boundary after column N (that padding
+      // receives the zeros computed there) and at row M
+      fence_proxy_async_smem();
       __syncwarp();
-      // and out to global memory, 4 rows x 128 B per instruction; a 16-byte
-      // piece is stored if it starts before column N (the padding up to the
-      // next 16-byte boundary receives the zeros computed there)
-      constexpr int kPer16 = 16 / static_cast<int>(sizeof(OutT));
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int rr = i * 4 + (lane >> 3);
-        const int cc = col0 + (lane & 7) * kPer16;
-        uint32_t w0, w1, w2, w3;
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                     : "r"(stage_w + swz(rr, lane & 7)));
-        if (row0 + rr < M && cc < N) {
-          uint4* dst = reinterpret_cast<uint4*>(a.out + static_cast<long long>(row0 + rr) * a.ldo + cc);
-          *dst = make_uint4(w0, w1, w2, w3);
-        }
+      if (lane == 0 && row0 < M) {  // (a box wholly below row M writes nothing)
+        tma_store_2d(tmY, stage_w, col0, row0);
+        bulk_commit_group();
       }
-      __syncwarp();
     }
     if constexpr (EPI == EPI_RES) {
       const int next = tile + 2 * tile_stride;  // the next tile on this accumulator
       if (next < num_tiles) preload(next, acc);
     }
   }
+  if (lane == 0) bulk_wait_group<0>();  // this warp's stores are complete
 }
 
 // Producer drain: wait for the copies still in flight (the last STAGES
@@ -346,7 +368,7 @@ __device__ __forceinline__ void drain_loads(long long issued, FullBar full_bar, 
 template <int BN, bool B_MN, int EPI, typename OutT, typename T16>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_1sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-             const EpiArgs<OutT, T16> ea, int K) {
+             const __grid_constant__ CUtensorMap tmY, const EpiArgs<OutT, T16> ea, int K) {
   using Cfg = GemmCfg<BN, BN>;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -379,6 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmY);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), C);  // the MMA commits of every CTA of the cluster
@@ -514,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    epilogue_role<BN, EPI, OutT, T16, false>(ea, warp, lane, smem_u32(sOut), tmem_base, tfull_bar(0), tfull_bar(1),
+    epilogue_role<BN, EPI, OutT, T16, false>(ea, &tmY, warp, lane, smem_u32(sOut), tmem_base, tfull_bar(0), tfull_bar(1),
                                          tempty_bar(0), tempty_bar(1), tile0, tile_step, num_tiles, m_groups, C * kBM,
                                          rank * kBM);
   }
@@ -536,7 +559,7 @@ constexpr int kPairBN = 256;
 template <bool B_MN, int EPI, typename OutT, typename T16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-             const EpiArgs<OutT, T16> ea, int K) {
+             const __grid_constant__ CUtensorMap tmY, const EpiArgs<OutT, T16> ea, int K) {
   using Cfg = GemmCfg<kPairBN, kPairBN / 2>;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -567,6 +590,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmY);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);   // the even CTA's expect_tx; both CTAs' bytes
       mbar_init(empty_bar(s), 1);  // the pair MMA commit
@@ -683,7 +707,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    epilogue_role<kPairBN, EPI, OutT, T16, true>(ea, warp, lane, smem_u32(sOut), tmem_base, tfull_bar(0), tfull_bar(1),
+    epilogue_role<kPairBN, EPI, OutT, T16, true>(ea, &tmY, warp, lane, smem_u32(sOut), tmem_base, tfull_bar(0), tfull_bar(1),
                                             mapa_shared(tempty_bar(0), 0), mapa_shared(tempty_bar(1), 0), pair,
                                             num_pairs, num_tiles, m_units, 2 * kBM, static_cast<int>(rank) * kBM);
   }
@@ -704,6 +728,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 bool make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
               uint32_t box_outer) {
   return encode_tma_2d(map, dt, base, inner, outer, inner * 2, 64, box_outer);
+}
+
+// Output y [M, ldo] as the target of the epilogue warps' TMA stores: boxes
+// of 32 rows x 128 bytes, 128-byte swizzle; the map ends at the 16-byte
+// boundary after column N and at row M.
+template <typename OutT>
+constexpr CUtensorMapDataType out_tma_type() {
+  if constexpr (sizeof(OutT) == 4)
+    return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  else
+    return Type16<OutT>::kTma;
+}
+template <typename OutT, typename T16>
+bool make_out_map(CUtensorMap* map, const EpiArgs<OutT, T16>& ea) {
+  constexpr int esz = static_cast<int>(sizeof(OutT));
+  const uint64_t n16 = (static_cast<uint64_t>(ea.N) * esz + 15) / 16 * 16 / esz;
+  return encode_tma_2d(map, out_tma_type<OutT>(), ea.out, n16, static_cast<uint64_t>(ea.M),
+                       static_cast<uint64_t>(ea.ldo) * esz, 128 / esz, 32);
 }
 
 template <typename Kern>
@@ -761,7 +803,10 @@ cudaError_t run_1sm(const T16* x, const T16* w, const EpiArgs<OutT, T16>& ea, in
     }
   }
   const int clusters = cluster_tiles < max_clusters ? cluster_tiles : max_clusters;
-  return launch_pdl(kern, C * clusters, kThreads, Cfg::SMEM_BYTES, stream, static_cast<unsigned>(C), ta, tb, ea, K);
+  CUtensorMap ty;
+  if (!make_out_map(&ty, ea)) return cudaErrorInvalidValue;
+  return launch_pdl(kern, C * clusters, kThreads, Cfg::SMEM_BYTES, stream, static_cast<unsigned>(C), ta, tb, ty, ea,
+                    K);
 }
 
 template <bool B_MN, int EPI, typename OutT, typename T16>
@@ -800,7 +845,9 @@ cudaError_t run_2sm(const T16* x, const T16* w, const EpiArgs<OutT, T16>& ea, in
   const int pairs_max = (dev >= 0 && dev < 64) ? max_pairs[dev] : num_sms() / 2;
   const int tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kPairBN - 1) / kPairBN);
   const int pairs = tiles < pairs_max ? tiles : pairs_max;
-  return launch_pdl(kern, 2 * pairs, kThreads, Cfg::SMEM_BYTES, stream, 0, ta, tb, ea, K);
+  CUtensorMap ty;
+  if (!make_out_map(&ty, ea)) return cudaErrorInvalidValue;
+  return launch_pdl(kern, 2 * pairs, kThreads, Cfg::SMEM_BYTES, stream, 0, ta, tb, ty, ea, K);
 }
 
 // Kernel variant for an M x N problem: 0 = CTA pair (256 x 256 tiles),
