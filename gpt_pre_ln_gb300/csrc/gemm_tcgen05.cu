@@ -71,15 +71,17 @@ struct GemmCfg {
   static constexpr int A_BYTES = kBM * kBK * 2;
   static constexpr int B_BYTES = B_COLS * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int BAR_BYTES = 256;
-  static constexpr int FIXED = 1024 + kEpiWarps * kWarpStageBytes + BAR_BYTES;
+  // the bias of a tile, 16-bit, one buffer per accumulator
+  static constexpr int BIAS_BYTES = 2 * BN * 2;
+  static constexpr int BAR_BYTES = 192;
+  static constexpr int FIXED = 1024 + kEpiWarps * kWarpStageBytes + BIAS_BYTES + BAR_BYTES;
   static constexpr int STAGES_FIT = (kSmemLimit - FIXED) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
   static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;  // power of two >= 2 * BN
   static constexpr int SMEM_BYTES = FIXED + STAGES * STAGE_BYTES;
   static_assert(STAGES >= 3, "pipeline too shallow");
   static_assert(SMEM_BYTES <= kSmemLimit, "shared memory");
-  static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+  static_assert((2 * STAGES + 9) * 8 + 8 <= BAR_BYTES, "barrier area");
   static_assert(BN % 64 == 0 && BN <= 256 && B_COLS % 64 == 0, "tile width");
 };
 
@@ -137,6 +139,33 @@ __device__ __forceinline__ void apply_bias_act(float (&v)[OutTraits<OutT>::CW], 
   }
 }
 
+// The same with the bias of the chunk read from shared memory (16-bit, zero
+// beyond column N), where the epilogue stages each tile's bias once.
+template <int EPI, typename OutT, typename T16>
+__device__ __forceinline__ void apply_bias_act_smem(float (&v)[OutTraits<OutT>::CW], uint32_t bias_addr) {
+  constexpr int CW = OutTraits<OutT>::CW;
+  uint4 raw[CW / 8];
+#pragma unroll
+  for (int q = 0; q < CW / 8; ++q)
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(raw[q].x), "=r"(raw[q].y), "=r"(raw[q].z), "=r"(raw[q].w)
+                 : "r"(bias_addr + q * 16));
+#pragma unroll
+  for (int q = 0; q < CW / 8; ++q) {
+    const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = Type16<T16>::unpack2(w[e]);
+      v[q * 8 + 2 * e] += f.x;
+      v[q * 8 + 2 * e + 1] += f.y;
+    }
+  }
+  if constexpr (EPI == EPI_GELU) {
+#pragma unroll
+    for (int i = 0; i < CW; ++i) v[i] = (sizeof(OutT) == 2) ? gelu_new_fast(v[i]) : gelu_new_accurate(v[i]);
+  }
+}
+
 template <typename OutT, typename T16>
 struct EpiArgs {
   const T16* bias;
@@ -164,7 +193,8 @@ struct EpiArgs {
 //   the read-out has no global loads left.
 template <int BN, int EPI, typename OutT, typename T16, bool CLUSTER_ARRIVE>
 __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const CUtensorMap* tmY, int warp, int lane,
-                                              uint32_t stage_base,
+                                              uint32_t stage_base, uint32_t bias_s, uint32_t bias_full0,
+                                              uint32_t bias_full1, uint32_t bias_empty0, uint32_t bias_empty1,
                                               uint32_t tmem_base, uint32_t tfull0, uint32_t tfull1, uint32_t tempty0,
                                               uint32_t tempty1, int tile_begin, int tile_stride, int num_tiles,
                                               int m_units, int unit_rows, int row_off) {
@@ -265,13 +295,42 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
     const int row0 = m0 + quad * 32;  // first row of this warp
     const int valid_cols = N - n0 < BN ? N - n0 : BN;
     const int nch = (valid_cols + CW - 1) / CW;
-    if constexpr (EPI != EPI_NONE && EPI != EPI_RES) {
-      // bring the bias of this warp's chunks into L1 while the MMAs run
-      constexpr int kLines = CW * static_cast<int>(sizeof(T16)) / 128 > 0 ? CW * static_cast<int>(sizeof(T16)) / 128 : 1;
-      const int k = lane / kLines;  // chunk half + 2k
-      const int c = half + 2 * k;
-      const int col = n0 + c * CW + (lane % kLines) * (128 / static_cast<int>(sizeof(T16)));
-      if (c < nch && col < N) asm volatile("prefetch.global.L1 [%0];" ::"l"(a.bias + col));
+    // EPI_BIAS / EPI_GELU: the tile's bias into the shared buffer of this
+    // accumulator (loaded by warp 2 while the MMAs run; the buffer is free
+    // once all eight warps have released it after its previous tile)
+    constexpr bool kBiasSmem = EPI == EPI_BIAS || EPI == EPI_GELU;
+    const uint32_t bias_b = bias_s + acc * (BN * 2);
+    if constexpr (kBiasSmem) {
+      if (warp == 2) {
+        const bool free_ok = t_local < 2 || __all_sync(0xffffffffu, mbar_wait(acc ? bias_empty1 : bias_empty0,
+                                                                                acc_par ^ 1));
+        if (!free_ok) {
+          if (lane == 0) {
+            record_error(a.err, kErrTimeout, kSiteGemmEpilogue);
+            bulk_wait_group<0>();
+          }
+          return;
+        }
+        for (int i = lane; i < BN / 8; i += 32) {
+          const int col = n0 + i * 8;
+          uint4 u = make_uint4(0u, 0u, 0u, 0u);
+          if (col + 8 <= N) {
+            u = __ldg(reinterpret_cast<const uint4*>(a.bias + col));
+          } else if (col < N) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = Type16<T16>::pack2(col + 2 * e < N ? to_f32<T16>(a.bias[col + 2 * e]) : 0.f,
+                                        col + 2 * e + 1 < N ? to_f32<T16>(a.bias[col + 2 * e + 1]) : 0.f);
+            u = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(bias_b + i * 16), "r"(u.x), "r"(u.y),
+                       "r"(u.z), "r"(u.w)
+                       : "memory");
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc ? bias_full1 : bias_full0);
+      }
     }
     const bool got = mbar_wait(acc ? tfull1 : tfull0, acc_par);
     if (!__all_sync(0xffffffffu, got)) {
@@ -282,6 +341,15 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
       return;
     }
     tc_fence_after();
+    if constexpr (kBiasSmem) {
+      if (!__all_sync(0xffffffffu, mbar_wait(acc ? bias_full1 : bias_full0, acc_par))) {
+        if (lane == 0) {
+          record_error(a.err, kErrTimeout, kSiteGemmEpilogue);
+          bulk_wait_group<0>();
+        }
+        return;
+      }
+    }
     // the last chunk of this half in the tile, after which its accumulator
     // columns are no longer read (-1: none)
     const int last_c = (nch - 1 - half) >= 0 ? nch - 1 - ((nch - 1 - half) & 1) : -1;
@@ -302,7 +370,10 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
           for (int i = 0; i < 32; ++i) v[l * 32 + i] = __uint_as_float(raw[l][i]);
       }
       if (EPI != EPI_RES && c == last_c) arrive_empty(acc);  // this half has read its last columns
-      if constexpr (EPI != EPI_RES) apply_bias_act<EPI, OutT, T16>(v, a.bias, col0, N);
+      if constexpr (kBiasSmem)
+        apply_bias_act_smem<EPI, OutT, T16>(v, bias_b + static_cast<uint32_t>(c * CW * 2));
+      else if constexpr (EPI == EPI_NONE)
+        apply_bias_act<EPI, OutT, T16>(v, a.bias, col0, N);
       // this lane's row (128 bytes) into the staging area (the 128-byte
       // swizzled layout of a [32 x 128 B] TMA box)
       staging_free();
@@ -333,6 +404,10 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
         tma_store_2d(tmY, stage_w, col0, row0);
         bulk_commit_group();
       }
+    }
+    if constexpr (kBiasSmem) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc ? bias_empty1 : bias_empty0);  // this warp has read the tile's bias
     }
     if constexpr (EPI == EPI_RES) {
       const int next = tile + 2 * tile_stride;  // the next tile on this accumulator
@@ -376,8 +451,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
   uint8_t* sOut = sB + STAGES * Cfg::B_BYTES;  // per-warp staging areas, 1024-aligned
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + kEpiWarps * kWarpStageBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  uint8_t* sBias = sOut + kEpiWarps * kWarpStageBytes;  // two tiles' bias
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sBias + Cfg::BIAS_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 9);
+  auto bias_full_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + 5 + a); };
+  auto bias_empty_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + 7 + a); };
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + STAGES + s); };
   auto tfull_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + a); };
@@ -409,6 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
       mbar_init(tempty_bar(a), kEpiThreads);  // every epilogue thread, once per tile
+      mbar_init(bias_full_bar(a), 1);
+      mbar_init(bias_empty_bar(a), kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     fence_barrier_init();
@@ -537,7 +617,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    epilogue_role<BN, EPI, OutT, T16, false>(ea, &tmY, warp, lane, smem_u32(sOut), tmem_base, tfull_bar(0), tfull_bar(1),
+    epilogue_role<BN, EPI, OutT, T16, false>(ea, &tmY, warp, lane, smem_u32(sOut), smem_u32(sBias), bias_full_bar(0),
+                                         bias_full_bar(1), bias_empty_bar(0), bias_empty_bar(1), tmem_base,
+                                         tfull_bar(0), tfull_bar(1),
                                          tempty_bar(0), tempty_bar(1), tile0, tile_step, num_tiles, m_groups, C * kBM,
                                          rank * kBM);
   }
@@ -567,8 +649,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
   uint8_t* sOut = sB + STAGES * Cfg::B_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + kEpiWarps * kWarpStageBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  uint8_t* sBias = sOut + kEpiWarps * kWarpStageBytes;  // two tiles' bias
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sBias + Cfg::BIAS_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 9);
+  auto bias_full_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + 5 + a); };
+  auto bias_empty_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + 7 + a); };
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + STAGES + s); };
   auto tfull_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + a); };
@@ -598,6 +683,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
       mbar_init(tempty_bar(a), 2 * kEpiThreads);  // both CTAs' epilogue threads
+      mbar_init(bias_full_bar(a), 1);
+      mbar_init(bias_empty_bar(a), kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     fence_barrier_init();
@@ -707,7 +794,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    epilogue_role<kPairBN, EPI, OutT, T16, true>(ea, &tmY, warp, lane, smem_u32(sOut), tmem_base, tfull_bar(0), tfull_bar(1),
+    epilogue_role<kPairBN, EPI, OutT, T16, true>(ea, &tmY, warp, lane, smem_u32(sOut), smem_u32(sBias),
+                                            bias_full_bar(0), bias_full_bar(1), bias_empty_bar(0), bias_empty_bar(1),
+                                            tmem_base, tfull_bar(0), tfull_bar(1),
                                             mapa_shared(tempty_bar(0), 0), mapa_shared(tempty_bar(1), 0), pair,
                                             num_pairs, num_tiles, m_units, 2 * kBM, static_cast<int>(rank) * kBM);
   }
