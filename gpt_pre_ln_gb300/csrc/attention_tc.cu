@@ -11,10 +11,14 @@
 //   S = Q K^T          tcgen05.mma M=128 N=128 K=64 -> tensor memory (fp32)
 //   softmax            4 warps, thread = query row = tensor-memory lane: the
 //                      row maximum and sum need no cross-thread exchange;
-//                      P = exp2(S * log2(e)/8 - m) written back as bf16 over
-//                      the S columns (tcgen05.st)
+//                      P = exp2(S * log2(e)/8 - m) written as bf16 into its
+//                      own 64 tensor-memory columns (tcgen05.st)
 //   O += P V           tcgen05.mma M=128 N=64 K=128 with A = P read from
 //                      tensor memory and V from shared memory (MN-major)
+// Tensor memory: S columns 0-127, O 128-191, P 192-255.  As soon as the
+// softmax of tile j has published P (and so finished reading S), the MMA
+// warp issues P.V for tile j and then S for tile j + 1, which overlap; the
+// softmax waits for that P.V before it rescales O or writes the next P.
 // The running maximum m is only raised (and O, l rescaled) when a row's new
 // maximum exceeds it by more than 8 in the log2 domain; otherwise P may reach
 // 2^8, harmless in fp32 sums and bf16.  Key tiles entirely above the
@@ -38,8 +42,9 @@ constexpr int kTk = 128;  // keys per tile
 constexpr int kAttnThreads = 192;
 constexpr int kTileBytes = kTq * kHd * 2;  // 16 KB, 128-byte rows, swizzled
 constexpr int kSmemBytes = 1024 + 5 * kTileBytes + 256;
-constexpr uint32_t kTmemCols = 256;  // S: 128 columns, O: 64 columns
+constexpr uint32_t kTmemCols = 256;  // S: 128 columns, O: 64, P: 64
 constexpr uint32_t kOCol = 128;
+constexpr uint32_t kPCol = 192;
 constexpr float kRescaleLog2 = 8.f;
 
 // D[tmem] (+)= A[tmem] * B[smem], kind::f16.
@@ -142,8 +147,6 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       for (int j = 0; j < n_kv && ok; ++j) {
         const int st = j & 1;
         ok = mbar_wait(kv_full(st), (j >> 1) & 1);
-        // the previous P.V has read P (which lies over S) before S is rewritten
-        if (ok && j > 0) ok = mbar_wait(pv_done, (j - 1) & 1);
         if (!ok) break;
         tc_fence_after();
         const uint32_t kb = sK0 + st * kTileBytes;
@@ -161,7 +164,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         const uint32_t vb = sV0 + st * kTileBytes;
 #pragma unroll
         for (int k = 0; k < kTk / 16; ++k)  // P: 8 tensor-memory columns (16 bf16) per K=16
-          umma_bf16_ts(tmem + kOCol, tmem + k * 8, sdesc_sw128(vb + k * 2048, 8192, 1024), idesc_pv,
+          umma_bf16_ts(tmem + kOCol, tmem + kPCol + k * 8, sdesc_sw128(vb + k * 2048, 8192, 1024), idesc_pv,
                        (j | k) != 0 ? 1u : 0u);
         umma_commit(pv_done);
         umma_commit(kv_empty(st));
@@ -180,6 +183,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off;
     const uint32_t tO = tmem + lane_off + kOCol;
+    const uint32_t tP = tmem + lane_off + kPCol;
     const float scale = 1.4426950408889634f * 0.125f;  // log2(e) / sqrt(64)
     float m_run = -INFINITY;
     float l = 0.f;
@@ -192,29 +196,50 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       }
       tc_fence_after();
       const bool diag = (j == qt);
-      const int k0 = j * kTk;
-      // pass 1: row maximum of the raw scores (8 independent partial maxima;
-      // the scale is positive, so it is applied once to the maximum)
+      // pass 1: row maximum of the raw scores (8 independent partial maxima,
+      // three-input max; the scale is positive, so it is applied once to the
+      // maximum).  In the diagonal tile, key chunk c holds keys
+      // c*32 .. c*32+31 of the tile against rows quad*32 + lane: chunks
+      // c > quad are above the diagonal for the whole warp and are skipped,
+      // chunk c == quad is masked per lane.
       float pm[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) pm[e] = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kTk / 32; ++c) {
-        uint32_t raw[32];
-        tmem_ld_32x32b_x32(tS + c * 32, raw);
+      for (int c2 = 0; c2 < kTk / 64; ++c2) {
+        if (diag && 2 * c2 > quad) break;
+        uint32_t raw[2][32];
+        tmem_ld_32x32b_x32(tS + c2 * 64, raw[0]);
+        tmem_ld_32x32b_x32(tS + c2 * 64 + 32, raw[1]);
         tmem_ld_wait();
-        if (diag) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (k0 + c * 32 + i <= q) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(raw[i]));
-        } else {
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int c = 2 * c2 + h2;
+          if (diag && c >= quad) {
+            if (c == quad) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(raw[i]));
+              for (int i = 0; i < 32; ++i)
+                if (i <= lane) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(raw[h2][i]));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pm[i & 7] = max3f(pm[i & 7], __uint_as_float(raw[h2][2 * i]), __uint_as_float(raw[h2][2 * i + 1]));
+          }
         }
       }
       const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                              fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * scale;
       const bool raise = mx > m_run + kRescaleLog2;
+      // the previous P.V has read P and updated O
+      if (j > 0) {
+        const bool pv_ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1));
+        if (!pv_ok) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
       // tcgen05.ld / tcgen05.st are warp-collective: the whole warp takes
       // the rescale branch if any of its rows needs it (alpha = 1 for the
       // others)
@@ -233,35 +258,40 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         }
       }
       if (raise) m_run = mx;
-      // pass 2: P = exp2(s * scale - m_run) as bf16 over the S columns;
-      // 8 independent partial sums
-      float ps[8];
+      // pass 2: P = exp2(s * scale - m_run) as 16-bit values into the P
+      // columns, paired fp32 arithmetic; 4 independent pair sums.  Chunks of
+      // the diagonal tile above the diagonal are written as zeros.
+      float2 ps[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) ps[e] = 0.f;
-      const float neg_m = -m_run;
+      for (int e = 0; e < 4; ++e) ps[e] = make_float2(0.f, 0.f);
+      const float2 scale2 = make_float2(scale, scale);
+      const float2 neg_m2 = make_float2(-m_run, -m_run);
 #pragma unroll
       for (int c = 0; c < kTk / 32; ++c) {
-        uint32_t raw[32];
-        tmem_ld_32x32b_x32(tS + c * 32, raw);
-        tmem_ld_wait();
-        float pv[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pv[i] = ex2_approx(fmaf(__uint_as_float(raw[i]), scale, neg_m));
-        if (diag) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (k0 + c * 32 + i > q) pv[i] = 0.f;
-        }
         uint32_t pk[16];
+        if (diag && c > quad) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          ps[(2 * i) & 7] += pv[2 * i];
-          ps[(2 * i + 1) & 7] += pv[2 * i + 1];
-          pk[i] = Type16<T16>::pack2(pv[2 * i], pv[2 * i + 1]);
+          for (int i = 0; i < 16; ++i) pk[i] = 0u;
+        } else {
+          uint32_t raw[32];
+          tmem_ld_32x32b_x32(tS + c * 32, raw);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 x = fma_f32x2(make_float2(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])),
+                                       scale2, neg_m2);
+            float2 p2 = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            if (diag && c == quad) {
+              if (2 * i > lane) p2.x = 0.f;
+              if (2 * i + 1 > lane) p2.y = 0.f;
+            }
+            ps[i & 3] = add_f32x2(ps[i & 3], p2);
+            pk[i] = Type16<T16>::pack2(p2.x, p2.y);
+          }
         }
-        tmem_st_32x32b_x16(tS + c * 16, pk);
+        tmem_st_32x32b_x16(tP + c * 16, pk);
       }
-      l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      l += ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y)) + ((ps[2].x + ps[2].y) + (ps[3].x + ps[3].y));
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_ready);
