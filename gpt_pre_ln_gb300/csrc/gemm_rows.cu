@@ -12,7 +12,8 @@
 //     accumulator in tensor memory holds y transposed, lane = feature,
 //     column = row.  W [K, N] is read MN-major straight from its Conv1D
 //     layout, wte [N, K] K-major; x K-major.
-//   * split K across a thread-block cluster of S CTAs (S <= 8), one
+//   * split K across a thread-block cluster of S CTAs (S <= 16; more than 8
+//     is a non-portable cluster size, all CTAs in one GPC), one
 //     128-feature tile per cluster: each CTA multiplies its share of the 64-
 //     wide k-blocks; the partial sums are reduce-scattered through
 //     distributed shared memory (CTA r of the cluster receives the partials
@@ -41,7 +42,11 @@ constexpr int kRF = 128;  // output features per tile (MMA M)
 constexpr int kRK = 64;   // K per k-block: one 128-byte swizzle atom of 16-bit values
 constexpr int kRThreads = 192;
 constexpr int kRStages = 3;
-constexpr int kRMaxCluster = 8;
+#ifndef GPT2_ROWS_MAX_CLUSTER
+#define GPT2_ROWS_MAX_CLUSTER 16
+#endif
+constexpr int kRMaxCluster = 16;                      // receive-area sizing
+constexpr int kRClusterCap = GPT2_ROWS_MAX_CLUSTER;  // largest K split launched (<= kRMaxCluster)
 
 enum RowsEpi : int { R_NONE = 0, R_BIAS = 1, R_GELU = 2, R_RES = 3 };
 
@@ -52,8 +57,8 @@ struct RowsCfg {
   static constexpr int B_BYTES = MP * kRK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // receive area of the split-K reduction: S sources x cw rows x 128 features
-  // (S * cw <= MP + S - 1 rows in all)
-  static constexpr int RECV_BYTES = kRF * (MP + kRMaxCluster) * 4;
+  // (S * cw <= M + S - 1 <= MP + kRMaxCluster - 1 rows in all)
+  static constexpr int RECV_BYTES = kRF * (MP + kRMaxCluster - 1) * 4;
   static constexpr int BAR_BYTES = 128;
   static constexpr int SMEM_BYTES = 1024 + kRStages * STAGE_BYTES + RECV_BYTES + BAR_BYTES;
   static constexpr int TMEM_COLS = 2 * MP < 64 ? 64 : 2 * MP;  // two accumulators; x32 loads stay inside
@@ -451,13 +456,18 @@ cudaError_t run_rows(const T16* x, const T16* w, const RowsArgs<OutT, T16>& ea, 
   using Cfg = RowsCfg<MP>;
   auto kern = gemm_rows<MP, W_MN, EPI, OutT, T16>;
   static int configured[64] = {0};
-  static int cluster_ok[64][kRMaxCluster + 1] = {{0}};  // 1 = fits, -1 = does not, per cluster size
+  static int cluster_ok[64][kRMaxCluster + 1] = {{0}};  // resident clusters per cluster size (-1: none)
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    // clusters beyond the portable 8 CTAs (all 16 in one GPC)
+    if (kRClusterCap > 8) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
     configured[dev] = 1;
   }
   constexpr CUtensorMapDataType dt = Type16<T16>::kTma;
@@ -474,7 +484,7 @@ cudaError_t run_rows(const T16* x, const T16* w, const RowsArgs<OutT, T16>& ea, 
   const int per_sm = std::max(1, std::min(2, 232448 / (Cfg::SMEM_BYTES + 1024)));
   int S = 1;
   if (2 * tiles < sms && !ea.cand) {  // argmax candidates are made by the single-CTA epilogue
-    S = std::min(kRMaxCluster, std::min(KB, std::max(1, per_sm * sms / tiles)));
+    S = std::min(kRClusterCap, std::min(KB, std::max(1, per_sm * sms / tiles)));
     // the largest cluster size whose clusters all fit at once
     for (; S > 1; --S) {
       int& known = cluster_ok[dev][S];
