@@ -41,7 +41,8 @@ namespace {
 constexpr int kRF = 128;  // output features per tile (MMA M)
 constexpr int kRK = 64;   // K per k-block: one 128-byte swizzle atom of 16-bit values
 constexpr int kRThreads = 192;
-constexpr int kRStages = 3;
+constexpr int kRStages = 3;      // ring depth with a K split (two CTAs per SM)
+constexpr int kRStagesMax = 8;   // ring depth of the persistent form (one CTA per SM, no receive area)
 #ifndef GPT2_ROWS_MAX_CLUSTER
 #define GPT2_ROWS_MAX_CLUSTER 16
 #endif
@@ -59,10 +60,16 @@ struct RowsCfg {
   // receive area of the split-K reduction: S sources x cw rows x 128 features
   // (S * cw <= M + S - 1 <= MP + kRMaxCluster - 1 rows in all)
   static constexpr int RECV_BYTES = kRF * (MP + kRMaxCluster - 1) * 4;
-  static constexpr int BAR_BYTES = 128;
+  // layout: ring (A stages, B stages), receive area (split-K form only),
+  // barriers
+  static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = 1024 + kRStages * STAGE_BYTES + RECV_BYTES + BAR_BYTES;
+  static constexpr int NST_PERSIST_FIT = (232448 - 1024 - BAR_BYTES) / STAGE_BYTES;
+  static constexpr int NST_PERSIST = NST_PERSIST_FIT < kRStagesMax ? NST_PERSIST_FIT : kRStagesMax;
+  static constexpr int SMEM_BYTES_PERSIST = 1024 + NST_PERSIST * STAGE_BYTES + BAR_BYTES;
   static constexpr int TMEM_COLS = 2 * MP < 64 ? 64 : 2 * MP;  // two accumulators; x32 loads stay inside
-  static_assert((2 * kRStages + 6) * 8 + 8 <= BAR_BYTES, "barrier area");
+  static_assert((2 * kRStagesMax + 6) * 8 + 8 <= BAR_BYTES, "barrier area");
+  static_assert(NST_PERSIST >= kRStages, "persistent ring");
   static_assert(kRStages * STAGE_BYTES >= MP * kRF * 4, "the partial fits over the ring");
 };
 
@@ -137,26 +144,27 @@ __global__ void __launch_bounds__(kRThreads, 1)
   using Cfg = RowsCfg<MP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = static_cast<int>(cluster_nctarank());  // K split; 1 = persistent over tiles
+  const int nst = S == 1 ? Cfg::NST_PERSIST : kRStages;  // ring depth
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kRStages * Cfg::A_BYTES;
+  uint8_t* sB = sA + nst * Cfg::A_BYTES;
   // split K: this CTA's partial, rows x 128 features fp32, staged over the
   // operand ring once every MMA has completed
   float* part = reinterpret_cast<float*>(smem);
-  float* recv = reinterpret_cast<float*>(sB + kRStages * Cfg::B_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(recv) + Cfg::RECV_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kRStages + 6);
+  float* recv = reinterpret_cast<float*>(sB + nst * Cfg::B_BYTES);  // split-K form only
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(recv) + (S > 1 ? Cfg::RECV_BYTES : 0));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kRStagesMax + 6);
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
-  auto empty_bar = [&](int s) { return smem_u32(bars + kRStages + s); };
-  auto tfull_bar = [&](int a) { return smem_u32(bars + 2 * kRStages + a); };
-  auto tempty_bar = [&](int a) { return smem_u32(bars + 2 * kRStages + 2 + a); };
-  const uint32_t drain_bar = smem_u32(bars + 2 * kRStages + 4);
-  const uint32_t recv_bar = smem_u32(bars + 2 * kRStages + 5);
+  auto empty_bar = [&](int s) { return smem_u32(bars + kRStagesMax + s); };
+  auto tfull_bar = [&](int a) { return smem_u32(bars + 2 * kRStagesMax + a); };
+  auto tempty_bar = [&](int a) { return smem_u32(bars + 2 * kRStagesMax + 2 + a); };
+  const uint32_t drain_bar = smem_u32(bars + 2 * kRStagesMax + 4);
+  const uint32_t recv_bar = smem_u32(bars + 2 * kRStagesMax + 5);
   unsigned* err = ea.err;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int M = ea.M, N = ea.N;
-  const int S = static_cast<int>(cluster_nctarank());  // K split; 1 = persistent over tiles
   const int rank = static_cast<int>(cluster_ctarank());
   const int n_tiles = (N + kRF - 1) / kRF;
   const int KB = ea.K / kRK;
@@ -188,7 +196,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   };
   auto advance = [&]() {
     ++issued;
-    if (++p_stage == kRStages) {
+    if (++p_stage == nst) {
       p_stage = 0;
       p_phase ^= 1;
     }
@@ -198,12 +206,11 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
   };
 
-  int pro_kb[kRStages];  // k-blocks of the stages loaded before the wait
-  int n_pro = 0;
+  int n_pro = 0;  // stages whose W boxes were loaded before the wait
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
-    for (int s = 0; s < kRStages; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
@@ -216,17 +223,16 @@ __global__ void __launch_bounds__(kRThreads, 1)
     fence_barrier_init();
     // the partials of this CTA's rows from all S CTAs (none when S = 1)
     mbar_arrive_expect_tx(recv_bar, S > 1 ? static_cast<uint32_t>(S * (own1 - own0) * kRF * 4) : 0u);
-    for (; n_pro < kRStages && p_tile < n_tiles; ++n_pro) {  // fresh ring: no waits
+    for (; n_pro < nst && p_tile < n_tiles; ++n_pro) {  // fresh ring: no waits
       mbar_arrive_expect_tx(full_bar(p_stage), Cfg::STAGE_BYTES);
       load_w(p_stage, p_tile, p_kb);
-      pro_kb[n_pro] = p_kb;
       advance();
     }
   }
   griddep_wait();  // x and the residual come from earlier kernels; tensor memory only after they completed
   griddep_launch_dependents();
   if (threadIdx.x == 0)
-    for (int i = 0; i < n_pro; ++i) load_x(i, pro_kb[i]);
+    for (int i = 0; i < n_pro; ++i) load_x(i, kb0 + i % (kb1 - kb0));  // stage i holds k-block kb0 + i mod (kb1 - kb0)
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
     tmem_relinquish();
@@ -254,9 +260,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
         advance();
       }
       // wait for the copies still in flight
-      const long long first = issued > kRStages ? issued - kRStages : 0;
+      const long long first = issued > nst ? issued - nst : 0;
       for (long long i = first; i < issued; ++i)
-        if (!mbar_wait(full_bar(static_cast<int>(i % kRStages)), static_cast<uint32_t>((i / kRStages) & 1))) {
+        if (!mbar_wait(full_bar(static_cast<int>(i % nst)), static_cast<uint32_t>((i / nst) & 1))) {
           record_error(err, kErrTimeout, kSiteRowsProducer);
           break;
         }
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
             any = true;
           }
           umma_commit(empty_bar(stage));
-          if (++stage == kRStages) {
+          if (++stage == nst) {
             stage = 0;
             phase ^= 1;
           }
@@ -461,7 +467,8 @@ cudaError_t run_rows(const T16* x, const T16* w, const RowsArgs<OutT, T16>& ea, 
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         std::max(Cfg::SMEM_BYTES, Cfg::SMEM_BYTES_PERSIST));
     if (e != cudaSuccess) return e;
     // clusters beyond the portable 8 CTAs (all 16 in one GPC)
     if (kRClusterCap > 8) {
@@ -507,7 +514,8 @@ cudaError_t run_rows(const T16* x, const T16* w, const RowsArgs<OutT, T16>& ea, 
     }
   }
   const unsigned grid = S > 1 ? S * tiles : std::min(tiles, sms);
-  return launch_pdl(kern, grid, kRThreads, Cfg::SMEM_BYTES, stream, static_cast<unsigned>(S), tw, tx, ea);
+  const int smem = S > 1 ? Cfg::SMEM_BYTES : Cfg::SMEM_BYTES_PERSIST;
+  return launch_pdl(kern, grid, kRThreads, smem, stream, static_cast<unsigned>(S), tw, tx, ea);
 }
 
 template <int MP, bool W_MN, typename T16>
