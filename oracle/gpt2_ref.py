@@ -194,6 +194,48 @@ def argmax_lowest(logits):
     return np.argmax(_f64(logits), axis=-1)  # numpy returns the first maximum
 
 
+# ------------------------------------------------------------------- loss
+def logsumexp(z):
+    """log sum_v exp(z_v) over the last axis, with the row maximum taken out
+    first so that no exponential overflows (llm.c notes section 2.3, the
+    max subtraction of the softmax)."""
+    z = _f64(z)
+    m = z.max(axis=-1, keepdims=True)
+    return (m + np.log(np.exp(z - m).sum(axis=-1, keepdims=True)))[..., 0]
+
+
+def shifted_cross_entropy(logits, labels):
+    """The language-model loss of GPT2LMHeadModel.
+
+    "逐行拆GPT-2源码", GPT2LMHeadModel section: the logits of positions
+    0 .. T-2 are scored against the labels of positions 1 .. T-1 (the shift
+    happens inside, so the labels may be the input ids themselves), each
+    position by the cross-entropy -log softmax(z)[label] = lse(z) - z[label],
+    and the mean is taken over all B (T-1) positions (the default reduction
+    of CrossEntropyLoss).  Labels must lie in [0, V).
+
+    Returns (token_loss [B, T-1], lse [B, T], mean).
+    """
+    logits = _f64(logits)
+    labels = np.asarray(labels)
+    B, T, V = logits.shape
+    if T < 2:
+        raise ValueError("the shifted loss needs T >= 2")
+    if labels.shape != (B, T) or labels.min() < 0 or labels.max() >= V:
+        raise ValueError("labels must be [B, T] ids in [0, V)")
+    lse = logsumexp(logits)
+    nxt = labels[:, 1:]
+    z_t = np.take_along_axis(logits[:, :-1, :], nxt[..., None], axis=-1)[..., 0]
+    token_loss = lse[:, :-1] - z_t
+    return token_loss, lse, float(token_loss.mean())
+
+
+def forward_loss(tokens, labels, params, dims):
+    """Forward over [B, T] tokens, then the shifted cross-entropy against
+    labels (labels = tokens for the usual next-token loss)."""
+    return shifted_cross_entropy(forward_logits(tokens, params, dims), labels)
+
+
 # ----------------------------------------------------------------- decode
 def decode_step(params, dims, cache, past_len, tokens):
     """One KV-cache decode step for every sequence of the batch.

@@ -417,3 +417,107 @@ def test_embed_positions_continue_at_offset():
     full = O.embed(tokens, wte, wpe)
     for p in (1, 7, 19):
         np.testing.assert_array_equal(O.embed(tokens[:, p:], wte, wpe, pos0=p), full[:, p:])
+
+
+# ------------------------------------------------------------------ loss
+def test_loss_uniform_logits_is_log_vocab():
+    """All logits equal: every position's loss and lse are ln V exactly.
+
+    Catches: a missing log, a sum where a mean belongs, lse without the
+    maximum added back.
+    """
+    for V in (3, 50257):
+        z = np.full((2, 5, V), 0.37)
+        lab = RNG.integers(0, V, size=(2, 5))
+        tl, lse, mean = O.shifted_cross_entropy(z, lab)
+        np.testing.assert_allclose(tl, math.log(V), rtol=1e-14)
+        np.testing.assert_allclose(lse, 0.37 + math.log(V), rtol=1e-14)
+        assert tl.shape == (2, 4) and lse.shape == (2, 5)
+        assert abs(mean - math.log(V)) < 1e-12
+
+
+def test_loss_one_hot_margin_closed_form():
+    """Target logit L above V-1 others at 0: loss = ln(1 + (V-1) e^-L).
+
+    Catches: the sign of the target term, the target taken from the wrong
+    column, overflow without the max shift (L = 800).
+    """
+    V = 11
+    for L in (0.0, 2.5, 30.0, 800.0):
+        z = np.zeros((1, 2, V))
+        lab = np.array([[4, 7]])
+        z[0, 0, 7] = L
+        tl, lse, _ = O.shifted_cross_entropy(z, lab)
+        assert np.isfinite(lse).all()
+        # lse - L cancels: the absolute error is a few ulp of L
+        np.testing.assert_allclose(tl[0, 0], math.log1p((V - 1) * math.exp(-L)), rtol=1e-12, atol=8 * np.spacing(max(L, 1.0)))
+
+
+def test_loss_shift_uses_next_label():
+    """Position t is scored against labels[t + 1]; labels[0] never counts.
+
+    Catches: an unshifted loss, a shift the wrong way, scoring the last
+    position.
+    """
+    V, T = 13, 6
+    z = RNG.standard_normal((2, T, V)) * 3
+    lab = RNG.integers(0, V, size=(2, T))
+    tl, _, m0 = O.shifted_cross_entropy(z, lab)
+    lab2 = lab.copy()
+    lab2[:, 0] = (lab[:, 0] + 5) % V
+    assert np.array_equal(O.shifted_cross_entropy(z, lab2)[0], tl)
+    lab3 = lab.copy()
+    lab3[1, 3] = (lab[1, 3] + 1) % V
+    tl3 = O.shifted_cross_entropy(z, lab3)[0]
+    changed = np.argwhere(tl3 != tl)
+    assert changed.tolist() == [[1, 2]]
+    z2 = z.copy()
+    z2[:, -1] += 100.0  # the last position's logits are not scored
+    assert O.shifted_cross_entropy(z2, lab)[2] == m0
+
+
+def test_loss_matches_torch_cross_entropy_fp64():
+    """The shifted mean equals torch's cross_entropy on the shifted tensors
+    (float64), and lse equals torch.logsumexp."""
+    V, B, T = 50, 3, 7
+    z = RNG.standard_normal((B, T, V)) * 4
+    lab = RNG.integers(0, V, size=(B, T))
+    tl, lse, mean = O.shifted_cross_entropy(z, lab)
+    zt = torch.from_numpy(z)
+    ref = Fn.cross_entropy(zt[:, :-1].reshape(-1, V), torch.from_numpy(lab[:, 1:]).reshape(-1), reduction="none")
+    np.testing.assert_allclose(tl.reshape(-1), ref.numpy(), rtol=1e-13)
+    np.testing.assert_allclose(mean, ref.mean().item(), rtol=1e-13)
+    np.testing.assert_allclose(lse, torch.logsumexp(zt, -1).numpy(), rtol=1e-13)
+
+
+def test_loss_row_shift_invariance():
+    """Adding c to every logit of a row leaves its loss unchanged and moves
+    its lse by c (softmax is shift-invariant)."""
+    V = 17
+    z = RNG.standard_normal((1, 4, V))
+    lab = RNG.integers(0, V, size=(1, 4))
+    tl, lse, _ = O.shifted_cross_entropy(z, lab)
+    c = np.array([5.0, -3.0, 40.0, 0.25])[None, :, None]
+    tl2, lse2, _ = O.shifted_cross_entropy(z + c, lab)
+    np.testing.assert_allclose(tl2, tl, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse2, lse + c[..., 0], rtol=1e-13)
+
+
+def test_forward_loss_zero_wte_is_log_vocab():
+    """wte = 0 makes every logit 0 whatever the blocks compute (the head is
+    tied to wte): the loss is ln V at every position."""
+    dims = Dims(n_layer=2, d_model=8, n_head=2, d_ff=32, vocab=19, n_pos=6, eps=1e-5)
+    params, d = synth.draw_model(dims, "f32", 5)
+    params["wte"] = np.zeros_like(params["wte"])
+    tok = RNG.integers(0, dims.vocab, size=(2, 6))
+    tl, lse, mean = O.forward_loss(tok, tok, params, dims)
+    np.testing.assert_allclose(tl, math.log(19), rtol=1e-14)
+    assert abs(mean - math.log(19)) < 1e-13
+
+
+def test_loss_rejects_bad_labels():
+    z = np.zeros((1, 3, 5))
+    with pytest.raises(ValueError):
+        O.shifted_cross_entropy(z, np.array([[0, 5, 1]]))
+    with pytest.raises(ValueError):
+        O.shifted_cross_entropy(np.zeros((1, 1, 5)), np.array([[0]]))
