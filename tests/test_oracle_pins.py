@@ -521,3 +521,23 @@ def test_loss_rejects_bad_labels():
         O.shifted_cross_entropy(z, np.array([[0, 5, 1]]))
     with pytest.raises(ValueError):
         O.shifted_cross_entropy(np.zeros((1, 1, 5)), np.array([[0]]))
+
+
+def test_prefill_cache_equals_token_by_token_decode():
+    """The cache of a forward over T positions equals the cache that T decode
+    steps from an empty cache build one token at a time ("逐行拆GPT-2源码":
+    `present` is the concatenation of every step's K and V).
+
+    Catches: K and V swapped, a head or position transposed, the cache of
+    the wrong layer.
+    """
+    dims = Dims(n_layer=2, d_model=128, n_head=2, d_ff=512, vocab=29, n_pos=12)
+    p = _toy_params(dims, seed=6)
+    tokens = RNG.integers(0, dims.vocab, size=(2, 9)).astype(np.int32)
+    ref = O.prefill_cache(tokens, p, dims, T_max=12)
+    cache = np.zeros_like(ref)
+    past = np.zeros(2, np.int32)
+    for t in range(9):
+        _, _, cache, past = O.decode_step(p, dims, cache, past, tokens[:, t])
+    np.testing.assert_allclose(cache, ref, rtol=1e-11, atol=1e-12)
+    assert np.all(ref[:, :, :, :, 9:] == 0)
