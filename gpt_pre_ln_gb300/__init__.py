@@ -17,7 +17,8 @@ __all__ = [
     "W_OUT_IN", "Dims", "BlockWeights", "ModelWeights", "lib", "library_path", "gpt2_abi_version",
     "gpt2_status_string", "gpt2_last_error", "gpt2_layernorm", "gpt2_linear", "gpt2_attention_causal",
     "gpt2_mlp_workspace_bytes", "gpt2_mlp", "gpt2_mlp_noalloc", "gpt2_mlp_noalloc_max_scratch_bytes",
-    "gpt2_workspace_bytes", "gpt2_block_forward", "gpt2_forward_logits",
+    "gpt2_workspace_bytes", "gpt2_block_forward", "gpt2_forward_logits", "gpt2_loss_workspace_bytes",
+    "gpt2_forward_loss", "gpt2_prefill_workspace_bytes", "gpt2_prefill",
     "gpt2_kv_cache_bytes", "gpt2_decode_workspace_bytes", "gpt2_decode_step", "gpt2_profile_begin",
     "gpt2_profile_end", "gpt2_profile_read", "ProfileEntry",
 ]
@@ -80,8 +81,14 @@ _SIGS = {
                                   _VP]),
     "gpt2_forward_logits": (_I32, [ctypes.POINTER(Dims), ctypes.POINTER(ModelWeights), _VP, _VP, _I64, _I32, _I32,
                                    _I32, _VP, _SZ, _VP]),
+    "gpt2_loss_workspace_bytes": (_SZ, [ctypes.POINTER(Dims), _I32, _I32]),
+    "gpt2_forward_loss": (_I32, [ctypes.POINTER(Dims), ctypes.POINTER(ModelWeights), _VP, _VP, _VP, _VP, _VP, _I32,
+                                 _I32, _VP, _SZ, _VP]),
     "gpt2_kv_cache_bytes": (_SZ, [ctypes.POINTER(Dims), _I32, _I32]),
     "gpt2_decode_workspace_bytes": (_SZ, [ctypes.POINTER(Dims), _I32]),
+    "gpt2_prefill_workspace_bytes": (_SZ, [ctypes.POINTER(Dims), _I32, _I32]),
+    "gpt2_prefill": (_I32, [ctypes.POINTER(Dims), ctypes.POINTER(ModelWeights), _VP, _I32, _I32, _VP, _I32, _VP, _VP,
+                            _VP, _I64, _VP, _SZ, _VP]),
     "gpt2_decode_step": (_I32, [ctypes.POINTER(Dims), ctypes.POINTER(ModelWeights), _VP, _I32, _I32, _VP, _VP, _VP,
                                 _VP, _I64, _VP, _SZ, _VP]),
     "gpt2_mlp_noalloc_max_scratch_bytes": (_SZ, []),
@@ -193,12 +200,34 @@ def gpt2_forward_logits(dims: Dims, w: ModelWeights, tokens, logits, ld, logits_
                                      B, T, _ptr(ws), ws_bytes, _stream(stream)), "gpt2_forward_logits")
 
 
+def gpt2_loss_workspace_bytes(dims: Dims, B: int, T: int) -> int:
+    return lib().gpt2_loss_workspace_bytes(ctypes.byref(dims), B, T)
+
+
+def gpt2_forward_loss(dims: Dims, w: ModelWeights, tokens, labels, token_loss, lse, mean_loss, B, T, ws, ws_bytes,
+                      stream=None):
+    _check(lib().gpt2_forward_loss(ctypes.byref(dims), ctypes.byref(w), _ptr(tokens), _ptr(labels), _ptr(token_loss),
+                                   _ptr(lse), _ptr(mean_loss), B, T, _ptr(ws), ws_bytes, _stream(stream)),
+           "gpt2_forward_loss")
+
+
 def gpt2_kv_cache_bytes(dims: Dims, B: int, T_max: int) -> int:
     return lib().gpt2_kv_cache_bytes(ctypes.byref(dims), B, T_max)
 
 
 def gpt2_decode_workspace_bytes(dims: Dims, B: int) -> int:
     return lib().gpt2_decode_workspace_bytes(ctypes.byref(dims), B)
+
+
+def gpt2_prefill_workspace_bytes(dims: Dims, B: int, T: int) -> int:
+    return lib().gpt2_prefill_workspace_bytes(ctypes.byref(dims), B, T)
+
+
+def gpt2_prefill(dims: Dims, w: ModelWeights, tokens, B, T, kv_cache, T_max, past_len, next_tokens, logits_opt, ld,
+                 ws, ws_bytes, stream=None):
+    _check(lib().gpt2_prefill(ctypes.byref(dims), ctypes.byref(w), _ptr(tokens), B, T, _ptr(kv_cache), T_max,
+                              _ptr(past_len), _ptr(next_tokens), _ptr(logits_opt), ld, _ptr(ws), ws_bytes,
+                              _stream(stream)), "gpt2_prefill")
 
 
 def gpt2_decode_step(dims: Dims, w: ModelWeights, kv_cache, B, T_max, past_len, tokens, next_tokens, logits_opt, ld,

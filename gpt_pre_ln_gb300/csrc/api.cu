@@ -72,7 +72,7 @@ using namespace gpt2;
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 
 // ------------------------------------------------------------- profiler
 struct ProfRec {
@@ -243,13 +243,19 @@ Acts carve_acts(void* ws, const gpt2_dims* d, int64_t M) {
   return a;
 }
 
-// The block body from `a = LN_1(x)` already computed; x -> x_out.
+// The block body from `a = LN_1(x)` already computed; x -> x_out.  With
+// kv_layer (16-bit paths), the layer's K and V of all B T positions are
+// also written to cache slots 0..T-1 of a [2, B, n_head, T_max, 64] layer.
 int block_body(const gpt2_dims* d, const gpt2_block_weights* w, const float* x, float* x_out, int B, int T,
-               const Acts& A, cudaStream_t s) {
+               const Acts& A, cudaStream_t s, void* kv_layer = nullptr, int T_max = 0) {
   const gpt2_dtype dt = d->dtype;
   const int64_t M = static_cast<int64_t>(B) * T;
   const int D = d->d_model, F = d->d_ff, H = d->n_head;
   GPT2_CUDA(linear(dt, A.a, w->w_qkv, w->b_qkv, nullptr, A.qkv, M, 3 * D, D, 3 * D, false, GPT2_EPI_BIAS, dt, s));
+  if (kv_layer) {
+    ProfScope prof("kv_from_qkv", 0.0, 2.0 * M * 2 * D * esize(dt), s);
+    GPT2_CUDA(launch_kv_from_qkv(dt, A.qkv, kv_layer, B, T, H, T_max, s));
+  }
   GPT2_CUDA(attention(dt, A.qkv, A.o, B, T, H, s));
   GPT2_CUDA(linear(dt, A.o, w->w_o, w->b_o, x, A.h, M, D, D, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32, s));
   GPT2_CUDA(layernorm(A.h, w->ln2_g, w->ln2_b, A.a, M, D, d->eps, GPT2_F32, dt, s));
@@ -383,6 +389,58 @@ struct DecodeGroup {
   }
 };
 
+
+// Embedding, the n_layer blocks and ln_f: A.a = LN_f(x_L) (type dims.dtype).
+// With kv_cache ([n_layer, 2, B, n_head, T_max, 64]) every layer's K and V
+// are kept in it; with lnf = false the ln_f step is left out.
+int forward_to_lnf(const gpt2_dims* dims, const gpt2_model_weights* w, const int32_t* tokens, int B, int T,
+                   const Acts& A, cudaStream_t s, void* kv_cache = nullptr, int T_max = 0, bool lnf = true) {
+  const int64_t M = static_cast<int64_t>(B) * T;
+  const gpt2_dtype dt = dims->dtype;
+  const int D = dims->d_model;
+  {
+    ProfScope prof("embed_layernorm", 8.0 * M * D, static_cast<double>(M) * (4.0 + D * (2.0 * esize(dt) + 4.0 + esize(dt))),
+                   s);
+    GPT2_CUDA(launch_embed_ln(tokens, w->wte, w->wpe, w->blocks[0].ln1_g, w->blocks[0].ln1_b, A.x, A.a, B, T, D,
+                              dims->vocab, dims->eps, dt, s));
+  }
+  for (int l = 0; l < dims->n_layer; ++l) {
+    const gpt2_block_weights* bw = &w->blocks[l];
+    if (l > 0) GPT2_CUDA(layernorm(A.x, bw->ln1_g, bw->ln1_b, A.a, M, D, dims->eps, GPT2_F32, dt, s));
+    void* kv_layer = nullptr;
+    if (kv_cache)
+      kv_layer = static_cast<char*>(kv_cache) +
+                 static_cast<size_t>(l) * 2 * B * dims->n_head * static_cast<size_t>(T_max) * 64 * esize(dt);
+    GPT2_TRY(block_body(dims, bw, A.x, A.x, B, T, A, s, kv_layer, T_max));
+  }
+  if (lnf) GPT2_CUDA(layernorm(A.x, w->lnf_g, w->lnf_b, A.a, M, D, dims->eps, GPT2_F32, dt, s));
+  return GPT2_OK;
+}
+
+// Prefill workspace after the [B T]-row activations: valid flags, the last
+// rows (fp32 and 16-bit) and the head's argmax candidates or logits.
+size_t prefill_extra_bytes(const gpt2_dims* d, int B) {
+  const size_t b = static_cast<size_t>(B);
+  const size_t Vp = (static_cast<size_t>(d->vocab) + 3) & ~static_cast<size_t>(3);
+  size_t n = align256(b * 4) + align256(b * d->d_model * 4) + align256(b * d->d_model * 2);
+  n += B <= kMaxRowsGemm ? align256(b * rows_argmax_candidates(d->vocab) * sizeof(float2)) : align256(b * Vp * 4);
+  return n;
+}
+
+// The loss path fuses log-sum-exp into the lm_head GEMM (16-bit, more than
+// kMaxRowsGemm rows); otherwise it writes fp32 logits into the workspace and
+// reduces them.
+bool loss_fused(const gpt2_dims* d, int64_t M) { return is16(d->dtype) && M > kMaxRowsGemm; }
+int64_t loss_ld(const gpt2_dims* d) { return (static_cast<int64_t>(d->vocab) + 3) / 4 * 4; }
+size_t loss_extra_bytes(const gpt2_dims* d, int64_t M) {
+  const size_t m = static_cast<size_t>(M);
+  size_t b = align256(m * 4) * 2;  // target logits, per-position loss scratch
+  if (loss_fused(d, M))
+    b += align256(m * lse_max_partials(d->vocab) * sizeof(float2));
+  else
+    b += align256(m * sizeof(float2)) + align256(m * loss_ld(d) * 4);
+  return b;
+}
 
 }  // namespace
 
@@ -523,22 +581,61 @@ int gpt2_forward_logits(const gpt2_dims* dims, const gpt2_model_weights* w, cons
   if (ws_bytes < gpt2_workspace_bytes(dims, B, T)) return GPT2_ERR_WORKSPACE;
   const int64_t M = static_cast<int64_t>(B) * T;
   const gpt2_dtype dt = dims->dtype;
-  const int D = dims->d_model;
   Acts A = carve_acts(ws, dims, M);
   cudaStream_t s = cs(stream);
-  {
-    ProfScope prof("embed_layernorm", 8.0 * M * D, static_cast<double>(M) * (4.0 + D * (2.0 * esize(dt) + 4.0 + esize(dt))),
-                   s);
-    GPT2_CUDA(launch_embed_ln(tokens, w->wte, w->wpe, w->blocks[0].ln1_g, w->blocks[0].ln1_b, A.x, A.a, B, T, D,
-                              dims->vocab, dims->eps, dt, s));
+  GPT2_TRY(forward_to_lnf(dims, w, tokens, B, T, A, s));
+  GPT2_CUDA(linear(dt, A.a, w->wte, nullptr, nullptr, logits, M, dims->vocab, dims->d_model, ld, true, GPT2_EPI_NONE,
+                   logits_t, s));
+  return GPT2_OK;
+}
+
+
+size_t gpt2_loss_workspace_bytes(const gpt2_dims* dims, int B, int T) {
+  if (check_dims(dims, true) != GPT2_OK || B < 0 || T < 0) return 0;
+  const int64_t M = static_cast<int64_t>(B) * T;
+  return acts_bytes(dims, M) + loss_extra_bytes(dims, M);
+}
+
+int gpt2_forward_loss(const gpt2_dims* dims, const gpt2_model_weights* w, const int32_t* tokens,
+                      const int32_t* labels, float* token_loss, float* lse, float* mean_loss, int B, int T, void* ws,
+                      size_t ws_bytes, gpt2_stream_t stream) {
+  GPT2_TRY(check_model(dims, w));
+  if (B < 0 || T < 0 || static_cast<int64_t>(B) * T > INT_MAX) return GPT2_ERR_ARG;
+  if (T > dims->n_pos) return GPT2_ERR_ARG;
+  if (B == 0) return GPT2_OK;
+  if (T < 2 || !tokens) return GPT2_ERR_ARG;
+  if (!token_loss && !lse && !mean_loss) return GPT2_ERR_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return GPT2_ERR_ARG;
+  if (ws_bytes < gpt2_loss_workspace_bytes(dims, B, T)) return GPT2_ERR_WORKSPACE;
+  const int64_t M = static_cast<int64_t>(B) * T;
+  const gpt2_dtype dt = dims->dtype;
+  const int D = dims->d_model, V = dims->vocab;
+  if (!labels) labels = tokens;
+  Acts A = carve_acts(ws, dims, M);
+  Carve c(static_cast<char*>(ws) + acts_bytes(dims, M));
+  float* tgt = c.take<float>(M, 4);
+  float* tl_scratch = c.take<float>(M, 4);
+  cudaStream_t s = cs(stream);
+  GPT2_TRY(forward_to_lnf(dims, w, tokens, B, T, A, s));
+  float2* part;
+  int n_part = 1;
+  if (loss_fused(dims, M)) {
+    part = c.take<float2>(M * lse_max_partials(V), sizeof(float2));
+    const double e = static_cast<double>(esize(dt));
+    ProfScope prof(dt == GPT2_BF16 ? "gemm_lse_bf16_tcgen05" : "gemm_lse_f16_tcgen05", 2.0 * M * V * D,
+                   (static_cast<double>(M) + V) * D * e, s);
+    GPT2_CUDA(launch_gemm_lse_16(dt, A.a, w->wte, M, V, D, labels, T, part, tgt, &n_part, s));
+  } else {
+    part = c.take<float2>(M, sizeof(float2));
+    float* logits = c.take<float>(M * loss_ld(dims), 4);
+    GPT2_CUDA(linear(dt, A.a, w->wte, nullptr, nullptr, logits, M, V, D, loss_ld(dims), true, GPT2_EPI_NONE,
+                     GPT2_F32, s));
+    ProfScope prof("lse_from_logits", 3.0 * M * V, 4.0 * M * V, s);
+    GPT2_CUDA(launch_lse_from_logits(logits, loss_ld(dims), M, V, labels, T, part, tgt, s));
   }
-  for (int l = 0; l < dims->n_layer; ++l) {
-    const gpt2_block_weights* bw = &w->blocks[l];
-    if (l > 0) GPT2_CUDA(layernorm(A.x, bw->ln1_g, bw->ln1_b, A.a, M, D, dims->eps, GPT2_F32, dt, s));
-    GPT2_TRY(block_body(dims, bw, A.x, A.x, B, T, A, s));
-  }
-  GPT2_CUDA(layernorm(A.x, w->lnf_g, w->lnf_b, A.a, M, D, dims->eps, GPT2_F32, dt, s));
-  GPT2_CUDA(linear(dt, A.a, w->wte, nullptr, nullptr, logits, M, dims->vocab, D, ld, true, GPT2_EPI_NONE, logits_t, s));
+  ProfScope prof("loss_reduce", 4.0 * M * n_part, 8.0 * M * n_part + 12.0 * M, s);
+  GPT2_CUDA(launch_loss_rows(part, n_part, tgt, labels, B, T, V, lse, token_loss ? token_loss : tl_scratch,
+                             mean_loss, s));
   return GPT2_OK;
 }
 
@@ -588,6 +685,63 @@ int gpt2_decode_step(const gpt2_dims* dims, const gpt2_model_weights* w, void* k
   GPT2_CUDA(G.embed());
   for (int l = 0; l < dims->n_layer; ++l) GPT2_CUDA(G.layer(l));
   GPT2_CUDA(G.head());
+  return GPT2_OK;
+}
+
+size_t gpt2_prefill_workspace_bytes(const gpt2_dims* dims, int B, int T) {
+  if (check_dims(dims, true) != GPT2_OK || B < 0 || T < 0) return 0;
+  return acts_bytes(dims, static_cast<int64_t>(B) * T) + prefill_extra_bytes(dims, B);
+}
+
+int gpt2_prefill(const gpt2_dims* dims, const gpt2_model_weights* w, const int32_t* tokens, int B, int T,
+                 void* kv_cache, int T_max, int32_t* past_len, int32_t* next_tokens, float* logits_opt, int64_t ld,
+                 void* ws, size_t ws_bytes, gpt2_stream_t stream) {
+  GPT2_TRY(check_model(dims, w));
+  if (!is16(dims->dtype)) return GPT2_ERR_UNSUPPORTED;
+  if (B < 0 || T < 0 || static_cast<int64_t>(B) * T > INT_MAX) return GPT2_ERR_ARG;
+  if (B == 0) return GPT2_OK;
+  if (T < 1 || T > dims->n_pos || T > T_max) return GPT2_ERR_ARG;
+  if (2ll * B * dims->n_head * T_max >= (1ll << 31)) return GPT2_ERR_UNSUPPORTED;
+  if (!tokens || !kv_cache || !past_len || !next_tokens || !aligned16(kv_cache)) return GPT2_ERR_ARG;
+  if (logits_opt && (ld < dims->vocab || !aligned16(logits_opt))) return GPT2_ERR_ARG;
+  if (logits_opt && ld % 4 != 0) return GPT2_ERR_UNSUPPORTED;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return GPT2_ERR_ARG;
+  if (ws_bytes < gpt2_prefill_workspace_bytes(dims, B, T)) return GPT2_ERR_WORKSPACE;
+  const int64_t M = static_cast<int64_t>(B) * T;
+  const gpt2_dtype dt = dims->dtype;
+  const int D = dims->d_model, V = dims->vocab;
+  cudaStream_t s = cs(stream);
+  Acts A = carve_acts(ws, dims, M);
+  Carve c(static_cast<char*>(ws) + acts_bytes(dims, M));
+  int* valid = c.take<int>(B, 4);
+  float* x_last = c.take<float>(static_cast<size_t>(B) * D, 4);
+  void* a_last = c.take<char>(static_cast<size_t>(B) * D, 2);
+  GPT2_TRY(forward_to_lnf(dims, w, tokens, B, T, A, s, kv_cache, T_max, false));
+  {
+    ProfScope prof("prefill_last_rows", 0.0, 8.0 * B * D, s);
+    GPT2_CUDA(launch_prefill_last_rows(A.x, B, T, D, x_last, valid, past_len, s));
+  }
+  GPT2_CUDA(layernorm(x_last, w->lnf_g, w->lnf_b, a_last, B, D, dims->eps, GPT2_F32, dt, s));
+  if (B <= kMaxRowsGemm) {
+    float2* cand = c.take<float2>(static_cast<size_t>(B) * rows_argmax_candidates(V), sizeof(float2));
+    const int n_cand = rows_argmax_candidates(V);
+    {
+      ProfScope prof(dt == GPT2_BF16 ? "gemm_rows_bf16_tcgen05" : "gemm_rows_f16_tcgen05", 2.0 * B * V * D,
+                     (static_cast<double>(B) + V) * D * esize(dt) + (logits_opt ? 4.0 * B * V : 0.0), s);
+      GPT2_CUDA(launch_gemm_rows_16(dt, a_last, w->wte, nullptr, nullptr, logits_opt, B, V, D, logits_opt ? ld : V,
+                                    true, GPT2_EPI_NONE, GPT2_F32, s, cand));
+    }
+    ProfScope prof("argmax_candidates", static_cast<double>(B) * n_cand, static_cast<double>(B) * n_cand * 8.0, s);
+    GPT2_CUDA(launch_argmax_candidates(cand, n_cand, B, valid, next_tokens, nullptr, s));
+    return GPT2_OK;
+  }
+  const int64_t Vp = (static_cast<int64_t>(V) + 3) & ~static_cast<int64_t>(3);
+  float* lg = c.take<float>(static_cast<size_t>(B) * Vp, 4);
+  float* out = logits_opt ? logits_opt : lg;
+  const int64_t lld = logits_opt ? ld : Vp;
+  GPT2_CUDA(linear(dt, a_last, w->wte, nullptr, nullptr, out, B, V, D, lld, true, GPT2_EPI_NONE, GPT2_F32, s));
+  ProfScope prof("argmax_rows", static_cast<double>(B) * V, static_cast<double>(B) * V * 4.0, s);
+  GPT2_CUDA(launch_argmax_rows(out, lld, B, V, valid, next_tokens, nullptr, s));
   return GPT2_OK;
 }
 

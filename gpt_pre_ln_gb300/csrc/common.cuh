@@ -35,6 +35,7 @@ enum ErrSite : unsigned {
   kSiteRowsProducer = 14,
   kSiteRowsMma = 15,
   kSiteRowsEpilogue = 16,
+  kSiteLossLabel = 17,
 };
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait

@@ -290,7 +290,8 @@ __device__ __forceinline__ void block_argmax(float& best, int& bi) {
   }
 }
 
-// One CTA per row: lowest index of the maximum; then past_len[b] += 1.
+// One CTA per row: lowest index of the maximum; then past_len[b] += 1
+// (unless past_len is null).
 __global__ void __launch_bounds__(1024) argmax_rows(const float* __restrict__ logits, long long ld, int V,
                                                     const int* __restrict__ valid, int32_t* __restrict__ next_tokens,
                                                     int32_t* __restrict__ past_len) {
@@ -310,7 +311,7 @@ __global__ void __launch_bounds__(1024) argmax_rows(const float* __restrict__ lo
   block_argmax(best, bi);
   if (threadIdx.x == 0 && valid[b]) {
     next_tokens[b] = bi;
-    past_len[b] += 1;
+    if (past_len) past_len[b] += 1;
   }
 }
 
@@ -339,11 +340,69 @@ __global__ void __launch_bounds__(256) argmax_candidates(const float2* __restric
   block_argmax(best, bi);
   if (threadIdx.x == 0 && valid[b]) {
     next_tokens[b] = bi;
-    past_len[b] += 1;
+    if (past_len) past_len[b] += 1;
+  }
+}
+
+// The prompt's K and V into the cache (the `present` of GPT2Attention after
+// a forward over positions 0..T-1): row m = b T + t of qkv [M, 3D] holds
+// k at columns D + h 64 + d and v at 2D + h 64 + d; they go to slots
+// [0|1][b_cache][h][t][d] of the layer's [2, B_cache, n_head, T_max, 64]
+// cache.  One CTA per row, one 16-byte chunk (8 elements) per thread.
+template <typename T16>
+__global__ void kv_from_qkv(const T16* __restrict__ qkv, T16* __restrict__ kv_layer, int T, int n_head, int T_max,
+                            int B_cache) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long m = blockIdx.x;
+  const int D = n_head * kHd;
+  const int j = threadIdx.x;  // chunk of the row's 2D k|v elements
+  if (j >= 2 * D / 8) return;
+  const int b = static_cast<int>(m / T), t = static_cast<int>(m % T);
+  const int kv = j * 8 >= D ? 1 : 0;
+  const int c = j * 8 - kv * D;  // column within k or v
+  const int h = c / kHd, d = c % kHd;
+  const uint4 u = *reinterpret_cast<const uint4*>(qkv + m * 3 * D + D + j * 8);
+  const long long dst = ((static_cast<long long>(kv) * B_cache + b) * n_head + h) * T_max * kHd +
+                        static_cast<long long>(t) * kHd + d;
+  *reinterpret_cast<uint4*>(kv_layer + dst) = u;
+}
+
+// After the prompt: x_last[b] = x[b T + T - 1] (the residual stream of each
+// sequence's last position), valid[b] = 1, past_len[b] = T.
+__global__ void prefill_last_rows(const float* __restrict__ x, int T, int D, float* __restrict__ x_last,
+                                  int* __restrict__ valid, int32_t* __restrict__ past_len) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int b = blockIdx.x;
+  const float* src = x + (static_cast<long long>(b) * T + T - 1) * D;
+  for (int i = threadIdx.x * 4; i < D; i += blockDim.x * 4)
+    *reinterpret_cast<float4*>(x_last + static_cast<long long>(b) * D + i) =
+        *reinterpret_cast<const float4*>(src + i);
+  if (threadIdx.x == 0) {
+    valid[b] = 1;
+    past_len[b] = T;
   }
 }
 
 }  // namespace
+
+cudaError_t launch_kv_from_qkv(gpt2_dtype dt, const void* qkv, void* kv_layer, int B, int T, int n_head, int T_max,
+                               cudaStream_t stream) {
+  const unsigned rows = static_cast<unsigned>(static_cast<long long>(B) * T);
+  const int threads = (2 * n_head * kHd / 8 + 31) / 32 * 32;
+  if (dt == GPT2_F16)
+    return launch_pdl(kv_from_qkv<__half>, rows, threads, 0, stream, 0, static_cast<const __half*>(qkv),
+                      static_cast<__half*>(kv_layer), T, n_head, T_max, B);
+  return launch_pdl(kv_from_qkv<__nv_bfloat16>, rows, threads, 0, stream, 0,
+                    static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(kv_layer), T, n_head, T_max,
+                    B);
+}
+
+cudaError_t launch_prefill_last_rows(const float* x, int B, int T, int D, float* x_last, int* valid,
+                                     int32_t* past_len, cudaStream_t stream) {
+  return launch_pdl(prefill_last_rows, B, 256, 0, stream, 0, x, T, D, x_last, valid, past_len);
+}
 
 cudaError_t launch_decode_embed_ln(gpt2_dtype dt, const int32_t* tokens, const int32_t* past_len, const void* wte,
                                    const void* wpe, const void* gamma, const void* beta, float* x, void* y, int B,

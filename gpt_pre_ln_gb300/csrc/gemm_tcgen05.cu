@@ -5,6 +5,7 @@
 //   y[M, N] = epilogue( x[M, K] . W )      W = [K, N] ("in, out", Conv1D)
 //                                          or  [N, K] (wte as the lm_head)
 //   epilogues: none | + bias | gelu_new(+ bias) | + bias + residual (fp32)
+//              | log-sum-exp partials (the lm_head of the loss: no output)
 //
 // Two persistent kernels share one design (10 warps per CTA):
 //   warp 0      TMA producer: 128-byte-swizzled A and B tiles of 64 K per
@@ -62,7 +63,7 @@ constexpr int kSmemLimit = 232448;      // 227 KB opt-in maximum per block
 // default; 2 builds and passes the same tests.
 constexpr int kOneSmCluster = GPT2_GEMM_1SM_CLUSTER;
 
-enum Epi : int { EPI_NONE = 0, EPI_BIAS = 1, EPI_GELU = 2, EPI_RES = 3 };
+enum Epi : int { EPI_NONE = 0, EPI_BIAS = 1, EPI_GELU = 2, EPI_RES = 3, EPI_LSE = 4 };
 
 // BN: output columns per CTA tile; B_COLS: columns of B staged per CTA
 // (BN for one CTA, BN / 2 for a pair).
@@ -174,7 +175,50 @@ struct EpiArgs {
   long long ldo;
   int M, N;
   unsigned* err;
+  // EPI_LSE: row r's target column is labels[r + 1] unless r % T == T - 1
+  // (the next token of the same sequence); part[p * M + r] = (max, sum of
+  // exp(z - max)) of row r over column slice p; tgt[r] = z at the target
+  const int32_t* labels;
+  int T;
+  float2* part;
+  float* tgt;
 };
+
+// EPI_LSE: one 32-column chunk of a row's logits into the running (m, s) of
+// a log-sum-exp (s = sum of exp(z - m) over the columns seen so far;
+// columns >= N lie outside the vocabulary and are left out), and the target
+// logit when its column falls in the chunk.  exp(z - m) = 2^((z - m) log2 e)
+// on the hardware exp2.
+__device__ __forceinline__ void lse_chunk(float (&v)[32], int col0, int N, int lbl, float& m, float& s,
+                                          float* tgt_row) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  if (col0 + 32 > N) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (col0 + i >= N) v[i] = -INFINITY;
+  }
+  if (lbl >= col0 && lbl < col0 + 32) {
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) t = (col0 + i == lbl) ? v[i] : t;
+    *tgt_row = t;
+  }
+  float cm = v[0];
+#pragma unroll
+  for (int i = 1; i < 31; i += 2) cm = max3f(cm, v[i], v[i + 1]);
+  cm = fmaxf(cm, v[31]);
+  const float nm = fmaxf(m, cm);  // finite: column col0 < N is in the chunk
+  const float nml = -nm * kLog2e;
+  float2 acc = make_float2(s * ex2_approx(fmaf(m, kLog2e, nml)), 0.f);  // m = -inf at first: 0
+  const float2 l2 = make_float2(kLog2e, kLog2e), sh = make_float2(nml, nml);
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const float2 e = fma_f32x2(make_float2(v[i], v[i + 1]), l2, sh);
+    acc = add_f32x2(acc, make_float2(ex2_approx(e.x), ex2_approx(e.y)));
+  }
+  m = nm;
+  s = acc.x + acc.y;
+}
 
 // Epilogue role (warps 2-9).  Tiles tile_begin, tile_begin + tile_stride, ...
 // < num_tiles; tile t covers rows (t % m_units) * unit_rows + row_off
@@ -355,6 +399,14 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
     const int last_c = (nch - 1 - half) >= 0 ? nch - 1 - ((nch - 1 - half) & 1) : -1;
     const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
     if (EPI != EPI_RES && last_c < 0) arrive_empty(acc);
+    // EPI_LSE: this lane's row, its target column (-1: none) and running
+    // log-sum-exp over this half's chunks
+    const int row = row0 + lane;
+    int lbl = -1;
+    float lse_m = -INFINITY, lse_s = 0.f;
+    if constexpr (EPI == EPI_LSE) {
+      if (row < M && row % a.T != a.T - 1) lbl = __ldg(a.labels + row + 1);
+    }
 #pragma unroll 1
     for (int c = half; c < nch; c += 2) {
       const int col0 = n0 + c * CW;
@@ -370,6 +422,10 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
           for (int i = 0; i < 32; ++i) v[l * 32 + i] = __uint_as_float(raw[l][i]);
       }
       if (EPI != EPI_RES && c == last_c) arrive_empty(acc);  // this half has read its last columns
+      if constexpr (EPI == EPI_LSE) {
+        lse_chunk(v, col0, N, lbl, lse_m, lse_s, a.tgt + row);
+        continue;
+      }
       if constexpr (kBiasSmem)
         apply_bias_act_smem<EPI, OutT, T16>(v, bias_b + static_cast<uint32_t>(c * CW * 2));
       else if constexpr (EPI == EPI_NONE)
@@ -408,6 +464,10 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
     if constexpr (kBiasSmem) {
       __syncwarp();
       if (lane == 0) mbar_arrive(acc ? bias_empty1 : bias_empty0);  // this warp has read the tile's bias
+    }
+    if constexpr (EPI == EPI_LSE) {
+      // slice (n0 / BN) * 2 + half; lanes write consecutive rows
+      if (row < M) a.part[static_cast<long long>((n0 / BN) * 2 + half) * M + row] = make_float2(lse_m, lse_s);
     }
     if constexpr (EPI == EPI_RES) {
       const int next = tile + 2 * tile_stride;  // the next tile on this accumulator
@@ -892,8 +952,8 @@ cudaError_t run_1sm(const T16* x, const T16* w, const EpiArgs<OutT, T16>& ea, in
     }
   }
   const int clusters = cluster_tiles < max_clusters ? cluster_tiles : max_clusters;
-  CUtensorMap ty;
-  if (!make_out_map(&ty, ea)) return cudaErrorInvalidValue;
+  CUtensorMap ty = ta;  // EPI_LSE stores no tile (a valid map, never used)
+  if (EPI != EPI_LSE && !make_out_map(&ty, ea)) return cudaErrorInvalidValue;
   return launch_pdl(kern, C * clusters, kThreads, Cfg::SMEM_BYTES, stream, static_cast<unsigned>(C), ta, tb, ty, ea,
                     K);
 }
@@ -934,8 +994,8 @@ cudaError_t run_2sm(const T16* x, const T16* w, const EpiArgs<OutT, T16>& ea, in
   const int pairs_max = (dev >= 0 && dev < 64) ? max_pairs[dev] : num_sms() / 2;
   const int tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kPairBN - 1) / kPairBN);
   const int pairs = tiles < pairs_max ? tiles : pairs_max;
-  CUtensorMap ty;
-  if (!make_out_map(&ty, ea)) return cudaErrorInvalidValue;
+  CUtensorMap ty = ta;  // EPI_LSE stores no tile (a valid map, never used)
+  if (EPI != EPI_LSE && !make_out_map(&ty, ea)) return cudaErrorInvalidValue;
   return launch_pdl(kern, 2 * pairs, kThreads, Cfg::SMEM_BYTES, stream, 0, ta, tb, ty, ea, K);
 }
 
@@ -1020,7 +1080,27 @@ cudaError_t launch(const void* x, const void* w, const void* bias, const float* 
                   : dispatch<true, T16>(v, X, W, Bv, residual, y, m, N, K, ldy, epilogue, y_t, stream);
 }
 
+template <typename T16>
+cudaError_t launch_lse(const void* x, const void* w, int64_t M, int N, int K, const int32_t* labels, int T,
+                       float2* part, float* tgt, int* n_part, cudaStream_t stream) {
+  const int m = static_cast<int>(M);
+  const int v = pick_variant(m, N);
+  const int bn = v == 0 ? kPairBN : v;
+  *n_part = 2 * ((N + bn - 1) / bn);
+  EpiArgs<float, T16> ea{nullptr, nullptr, nullptr, 0, m, N, device_error_word(), labels, T, part, tgt};
+  return run_variant<false, EPI_LSE, float, T16>(v, static_cast<const T16*>(x), static_cast<const T16*>(w), ea, K,
+                                                 stream);
+}
+
 }  // namespace
+
+cudaError_t launch_gemm_lse_16(gpt2_dtype dt, const void* x, const void* w, int64_t M, int N, int K,
+                               const int32_t* labels, int T, float2* part, float* tgt, int* n_part,
+                               cudaStream_t stream) {
+  if (M <= kMaxRowsGemm) return cudaErrorNotSupported;
+  if (dt == GPT2_F16) return launch_lse<__half>(x, w, M, N, K, labels, T, part, tgt, n_part, stream);
+  return launch_lse<__nv_bfloat16>(x, w, M, N, K, labels, T, part, tgt, n_part, stream);
+}
 
 cudaError_t launch_gemm_16(gpt2_dtype dt, const void* x, const void* w, const void* bias, const float* residual,
                            void* y, int64_t M, int N, int K, int64_t ldy, bool w_out_in, int epilogue, gpt2_dtype y_t,

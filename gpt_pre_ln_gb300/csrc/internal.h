@@ -65,6 +65,16 @@ cudaError_t launch_gemm_16(gpt2_dtype dt, const void* x, const void* w, const vo
                            void* y, int64_t M, int N, int K, int64_t ldy, bool w_out_in, int epilogue, gpt2_dtype y_t,
                            cudaStream_t stream);
 
+// The lm_head of the loss: z = x . w^T (w [N, K], K-major), never stored.
+// Per row r and column slice p: part[p * M + r] = (max_z, sum exp(z - max_z))
+// over the slice; tgt[r] = z at column labels[r + 1] when r % T != T - 1 and
+// that label is in [0, N) (not written otherwise).  *n_part = slices per
+// row (at most lse_max_partials(N)).  M > kMaxRowsGemm only.
+inline int lse_max_partials(int N) { return 2 * ((N + 127) / 128); }
+cudaError_t launch_gemm_lse_16(gpt2_dtype dt, const void* x, const void* w, int64_t M, int N, int K,
+                               const int32_t* labels, int T, float2* part, float* tgt, int* n_part,
+                               cudaStream_t stream);
+
 // The same GEMM for M <= kMaxRowsGemm rows (operands swapped, K split over a
 // thread-block cluster); launch_gemm_16 hands such calls to it.  With
 // argmax_cand (epilogue NONE, fp32 y, which may then be null) it also writes
@@ -95,9 +105,28 @@ cudaError_t launch_decode_embed_ln(gpt2_dtype dt, const int32_t* tokens, const i
 cudaError_t launch_decode_attention(gpt2_dtype dt, const void* qkv, void* kv_layer, void* out, const int32_t* past_len,
                                     const int* valid, int B, int b_cache0, int B_cache, int n_head, int T_max,
                                     cudaStream_t stream);
+// Prefill: K and V of rows b T + t of qkv [B T, 3D] into cache slots t of
+// sequences b (layer layout [2, B, n_head, T_max, 64]).
+cudaError_t launch_kv_from_qkv(gpt2_dtype dt, const void* qkv, void* kv_layer, int B, int T, int n_head, int T_max,
+                               cudaStream_t stream);
+// x_last[b] = x[b T + T - 1] (fp32 [B, D]), valid[b] = 1, past_len[b] = T.
+cudaError_t launch_prefill_last_rows(const float* x, int B, int T, int D, float* x_last, int* valid,
+                                     int32_t* past_len, cudaStream_t stream);
+// past_len may be null in the two argmax launchers (no increment).
 cudaError_t launch_argmax_rows(const float* logits, int64_t ld, int B, int V, const int* valid, int32_t* next_tokens,
                                int32_t* past_len, cudaStream_t stream);
 // The same from the candidates of launch_gemm_rows_16 (n_cand per row).
+// Loss from log-sum-exp partials (n_part per row, layout of
+// launch_gemm_lse_16) and target logits: lse[r] (nullable), token_loss
+// [B, T-1] = lse - z_target (nullable), mean over the B (T-1) positions
+// into *mean_loss (nullable).  A label outside [0, V) records kErrRange and
+// gives a NaN loss.
+cudaError_t launch_loss_rows(const float2* part, int n_part, const float* tgt, const int32_t* labels, int B, int T,
+                             int V, float* lse, float* token_loss, float* mean_loss, cudaStream_t stream);
+// Log-sum-exp partials (n_part = 1) and target logits from stored fp32 logits
+// [M, ld], for the paths that write logits.
+cudaError_t launch_lse_from_logits(const float* logits, int64_t ld, int64_t M, int V, const int32_t* labels, int T,
+                                   float2* part, float* tgt, cudaStream_t stream);
 cudaError_t launch_argmax_candidates(const float2* cand, int n_cand, int B, const int* valid, int32_t* next_tokens,
                                      int32_t* past_len, cudaStream_t stream);
 

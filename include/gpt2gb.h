@@ -231,9 +231,57 @@ int gpt2_forward_logits(const gpt2_dims *dims, const gpt2_model_weights *w, cons
                         int64_t ld, gpt2_dtype logits_t, int B, int T, void *ws, size_t ws_bytes,
                         gpt2_stream_t stream);
 
+/* Workspace needed by gpt2_forward_loss for a [B, T] batch (0 if the dims
+ * are invalid). */
+size_t gpt2_loss_workspace_bytes(const gpt2_dims *dims, int B, int T);
+
+/* Whole forward to the language-model loss ("逐行拆GPT-2源码",
+ * GPT2LMHeadModel.forward with labels): the forward of gpt2_forward_logits,
+ * then position t of each sequence is scored against labels[b, t + 1] (the
+ * shift happens here, so labels may be the input ids themselves) by the
+ * cross-entropy lse(z) - z[label], lse(z) = log sum_v exp(z_v) over the
+ * vocabulary, and the mean is taken over all B (T - 1) positions.  The
+ * [B, T, vocab] logits are never written: on the 16-bit paths with
+ * B T > 128 the lm_head GEMM reduces each row to log-sum-exp partials and
+ * the target logit in its epilogue.
+ *   tokens: int32 [B, T] device (as gpt2_forward_logits); labels: NULL
+ *   (= tokens) or int32 [B, T] device, each used label in [0, vocab) (else
+ *   GPT2_ERR_RANGE on the device and a NaN loss at that position);
+ *   token_loss: NULL or fp32 [B, T - 1] device; lse: NULL or fp32 [B, T]
+ *   device (log-sum-exp of every position's logits, so that
+ *   p(v) = exp(z_v - lse)); mean_loss: NULL or one fp32 on the device, the
+ *   mean of the B (T - 1) losses summed in a fixed order (deterministic).
+ *   At least one output must be given.  2 <= T <= n_pos; ws of
+ *   gpt2_loss_workspace_bytes(dims, B, T) bytes, 256-byte aligned. */
+int gpt2_forward_loss(const gpt2_dims *dims, const gpt2_model_weights *w, const int32_t *tokens,
+                      const int32_t *labels, float *token_loss, float *lse, float *mean_loss, int B, int T, void *ws,
+                      size_t ws_bytes, gpt2_stream_t stream);
+
 /* Bytes of a KV cache laid out [n_layer, 2 (K, V), B, n_head, T_max, 64] in
  * the path's element type (2 bytes for BF16 and F16, 4 for F32). */
 size_t gpt2_kv_cache_bytes(const gpt2_dims *dims, int B, int T_max);
+
+/* Workspace needed by gpt2_prefill for a [B, T] prompt batch. */
+size_t gpt2_prefill_workspace_bytes(const gpt2_dims *dims, int B, int T);
+
+/* Prompt processing ahead of gpt2_decode_step ("逐行拆GPT-2源码",
+ * GPT2Attention with use_cache: `present` keeps each layer's K and V of the
+ * positions processed so far; GPT2Model: positions start at 0 without a
+ * cache): the forward of gpt2_forward_logits over tokens [B, T], which also
+ * writes every layer's K and V of positions 0..T-1 into cache slots 0..T-1
+ * of each sequence; then LN_f and the tied lm_head on each sequence's last
+ * position only, argmax (lowest index on ties) -> next_tokens[b], and
+ * past_len[b] = T.  A following gpt2_decode_step with tokens = next_tokens
+ * continues the greedy sequence at position T.
+ *   kv_cache: [n_layer, 2, B, n_head, T_max, 64] (gpt2_kv_cache_bytes; slots
+ *   >= T are not touched); past_len, next_tokens: int32 [B] device (written);
+ *   logits_opt: NULL or fp32 [B, ld] device receiving the last position's
+ *   logits (ld >= vocab, a multiple of 4); 1 <= T <= min(n_pos, T_max);
+ *   ws of gpt2_prefill_workspace_bytes(dims, B, T) bytes.  16-bit paths
+ *   only, and 2 * B * n_head * T_max < 2^31. */
+int gpt2_prefill(const gpt2_dims *dims, const gpt2_model_weights *w, const int32_t *tokens, int B, int T,
+                 void *kv_cache, int T_max, int32_t *past_len, int32_t *next_tokens, float *logits_opt, int64_t ld,
+                 void *ws, size_t ws_bytes, gpt2_stream_t stream);
 
 /* Workspace needed by gpt2_decode_step for a batch of B sequences. */
 size_t gpt2_decode_workspace_bytes(const gpt2_dims *dims, int B);

@@ -198,6 +198,21 @@ def test_forward_logits_gpt2_small_full_size():
         _check_logits(got, ref)
 
 
+@pytest.mark.parametrize("name,seqs", [("gpt2_medium_fwd_b16_t1024", (15,)), ("gpt2_xl_fwd_b4_t1024", (3,))],
+                         ids=["gpt2-medium-b16", "gpt2-xl-b4"])
+def test_forward_logits_larger_models_full_size(name, seqs):
+    """GPT-2 medium (24 x 1024, 16 heads; B=16) and XL (48 x 1600, 25 heads;
+    B=4) at T=1024: the GPU runs the whole batch, the oracle checks the last
+    sequence at every position."""
+    inp = synth.workload_inputs(name)
+    dims, params, tokens = inp["dims"], inp["params"], inp["tokens"]
+    logits = _forward(dims, "bf16", params, tokens, G.F32)
+    for b in seqs:
+        got = to_np(logits[b:b + 1])
+        ref = O.forward_logits(tokens[b:b + 1], params, dims)
+        _check_logits(got, ref)
+
+
 def test_embedding_token_out_of_range_is_reported():
     dims = synth.Dims(n_layer=1, d_model=128, n_head=2, d_ff=512, vocab=100, n_pos=16)
     params, _ = synth.draw_model(dims, "bf16", 1)
