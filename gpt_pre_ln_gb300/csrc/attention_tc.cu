@@ -6,8 +6,11 @@
 // ``_merge_heads``; llm.c notes 2.2-2.3: scale 1/sqrt(d_k), future positions
 // masked before the softmax, row maximum subtracted.)
 //
-// One CTA per (batch, head, tile of 128 queries), two CTAs per SM so that one
-// CTA's softmax overlaps the other's tensor-core work.  Per key tile of 128:
+// Persistent CTAs, two per SM so that one CTA's softmax overlaps the other's
+// tensor-core work; each walks a list of (batch, head, tile of 128 queries)
+// items, heaviest first, keeping its tensor memory and barriers, so that
+// one item's last softmax and output store overlap the next item's loads
+// and first S = Q K^T.  Per key tile of 128:
 //   S = Q K^T          tcgen05.mma M=128 N=128 K=64 -> tensor memory (fp32)
 //   softmax            4 warps, thread = query row = tensor-memory lane: the
 //                      row maximum and sum need no cross-thread exchange;
@@ -58,9 +61,18 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// Work item w of a launch (heaviest first): query tile n_qt - 1 - w / BH of
+// (batch, head) w % BH.  CTA c takes items c, then 2G - 1 - c, 2G + c, ...
+// (G CTAs; a snake order, so that the CTAs that took the heaviest items of
+// one round take the lightest of the next).
+__device__ __forceinline__ int attn_item(int k, int c, int G) {
+  return k * G + ((k & 1) ? G - 1 - c : c);
+}
+
 template <typename T16>
 __global__ void __launch_bounds__(kAttnThreads, 2)
-    attn_causal_tc(const __grid_constant__ CUtensorMap tm_qkv, T16* __restrict__ out, int T, int H, unsigned* err) {
+    attn_causal_tc(const __grid_constant__ CUtensorMap tm_qkv, T16* __restrict__ out, int B, int T, int H,
+                   unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(smem);
@@ -74,23 +86,21 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   const uint32_t p_ready = smem_u32(bars + 6);
   const uint32_t pv_done = smem_u32(bars + 7);
   const uint32_t drain = smem_u32(bars + 8);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
+  const uint32_t q_empty = smem_u32(bars + 9);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int b = bh / H;
-  const int h = bh % H;
   const int D = H * kHd;
+  const int BH = B * H;
   const int n_qt = (T + kTq - 1) / kTq;
-  const int qt = n_qt - 1 - static_cast<int>(blockIdx.y);  // heaviest tiles first
-  const int q0 = qt * kTq;
-  const int n_kv = qt + 1;  // key tiles 0..qt; later ones are fully masked
-  const int row_base = b * T;  // first row of this sequence in [B*T, 3D]
+  const int n_items = BH * n_qt;
+  const int G = gridDim.x, cta = blockIdx.x;
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_qkv);
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(kv_full(s), 1);
       mbar_init(kv_empty(s), 1);
@@ -112,27 +122,45 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Barrier phases run on across items: key tile g (counted over all items
+  // of this CTA) uses K/V stage g & 1 in its (g >> 1)-th round and the g-th
+  // phase of s_full / p_ready / pv_done; item i the i-th phase of q_full /
+  // q_empty.
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
-      mbar_arrive_expect_tx(q_full, kTileBytes);
-      tma_load_2d(sQ, &tm_qkv, q_full, h * kHd, row_base + q0);
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(kv_empty(st), ((j >> 1) & 1) ^ 1)) {
+      long long g = 0;
+      bool ok = true;
+      int it = 0;
+      for (int k = 0; ok; ++k, ++it) {
+        const int w = attn_item(k, cta, G);
+        if (w >= n_items) break;
+        const int qt = n_qt - 1 - w / BH, bh = w % BH;
+        const int b = bh / H, h = bh % H;
+        const int row_base = b * T;
+        // the Q tile is free once the last S of the item before has been computed
+        if (it > 0 && !mbar_wait(q_empty, (it - 1) & 1)) {
           record_error(err, kErrTimeout, kSiteAttnProducer);
           break;
         }
-        mbar_arrive_expect_tx(kv_full(st), 2 * kTileBytes);
-        tma_load_2d(sK0 + st * kTileBytes, &tm_qkv, kv_full(st), D + h * kHd, row_base + j * kTk);
-        tma_load_2d(sV0 + st * kTileBytes, &tm_qkv, kv_full(st), 2 * D + h * kHd, row_base + j * kTk);
-        ++issued;
+        mbar_arrive_expect_tx(q_full, kTileBytes);
+        tma_load_2d(sQ, &tm_qkv, q_full, h * kHd, row_base + qt * kTq);
+        for (int j = 0; j <= qt; ++j, ++g) {
+          const int st = static_cast<int>(g & 1);
+          if (!mbar_wait(kv_empty(st), static_cast<uint32_t>((g >> 1) & 1) ^ 1)) {
+            record_error(err, kErrTimeout, kSiteAttnProducer);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(kv_full(st), 2 * kTileBytes);
+          tma_load_2d(sK0 + st * kTileBytes, &tm_qkv, kv_full(st), D + h * kHd, row_base + j * kTk);
+          tma_load_2d(sV0 + st * kTileBytes, &tm_qkv, kv_full(st), 2 * D + h * kHd, row_base + j * kTk);
+        }
       }
-      // copies still in flight: the Q tile and the last (up to two) stages
-      if (!mbar_wait(q_full, 0)) record_error(err, kErrTimeout, kSiteAttnProducer);
-      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
-        if (!mbar_wait(kv_full(j & 1), (j >> 1) & 1)) {
+      // copies still in flight: the last Q tile and the last (up to two) stages
+      if (it > 0 && !mbar_wait(q_full, (it - 1) & 1)) record_error(err, kErrTimeout, kSiteAttnProducer);
+      for (long long x = g > 2 ? g - 2 : 0; x < g; ++x)
+        if (!mbar_wait(kv_full(static_cast<int>(x & 1)), static_cast<uint32_t>((x >> 1) & 1))) {
           record_error(err, kErrTimeout, kSiteAttnProducer);
           break;
         }
@@ -142,32 +170,41 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       // ------------------------------------------------ MMA issuer
       constexpr uint32_t idesc_s = idesc_f16kind_f32(kTq, kTk, false, false, Type16<T16>::kFormat);
       constexpr uint32_t idesc_pv = idesc_f16kind_f32(kTq, kHd, false, true, Type16<T16>::kFormat);
-      bool ok = mbar_wait(q_full, 0);
+      bool ok = true;
       bool any = false;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int st = j & 1;
-        ok = mbar_wait(kv_full(st), (j >> 1) & 1);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kb = sK0 + st * kTileBytes;
+      long long g = 0;
+      int it = 0;
+      for (int k = 0; ok; ++k, ++it) {
+        const int w = attn_item(k, cta, G);
+        if (w >= n_items) break;
+        const int qt = n_qt - 1 - w / BH;
+        ok = mbar_wait(q_full, it & 1);
+        for (int j = 0; j <= qt && ok; ++j, ++g) {
+          const int st = static_cast<int>(g & 1);
+          ok = mbar_wait(kv_full(st), static_cast<uint32_t>((g >> 1) & 1));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t kb = sK0 + st * kTileBytes;
 #pragma unroll
-        for (int k = 0; k < kHd / 16; ++k)
-          umma_bf16(tmem, sdesc_sw128(sQ + k * 32, 16, 1024), sdesc_sw128(kb + k * 32, 16, 1024), idesc_s,
-                    k > 0 ? 1u : 0u);
-        umma_commit(s_full);
-        any = true;
-        if (!mbar_wait(p_ready, j & 1)) {
-          ok = false;
-          break;
+          for (int kk = 0; kk < kHd / 16; ++kk)
+            umma_bf16(tmem, sdesc_sw128(sQ + kk * 32, 16, 1024), sdesc_sw128(kb + kk * 32, 16, 1024), idesc_s,
+                      kk > 0 ? 1u : 0u);
+          umma_commit(s_full);
+          if (j == qt) umma_commit(q_empty);  // the item's last read of Q
+          any = true;
+          if (!mbar_wait(p_ready, static_cast<uint32_t>(g & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t vb = sV0 + st * kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kTk / 16; ++kk)  // P: 8 tensor-memory columns (16 bf16) per K=16
+            umma_bf16_ts(tmem + kOCol, tmem + kPCol + kk * 8, sdesc_sw128(vb + kk * 2048, 8192, 1024), idesc_pv,
+                         (j | kk) != 0 ? 1u : 0u);
+          umma_commit(pv_done);
+          umma_commit(kv_empty(st));
         }
-        tc_fence_after();
-        const uint32_t vb = sV0 + st * kTileBytes;
-#pragma unroll
-        for (int k = 0; k < kTk / 16; ++k)  // P: 8 tensor-memory columns (16 bf16) per K=16
-          umma_bf16_ts(tmem + kOCol, tmem + kPCol + k * 8, sdesc_sw128(vb + k * 2048, 8192, 1024), idesc_pv,
-                       (j | k) != 0 ? 1u : 0u);
-        umma_commit(pv_done);
-        umma_commit(kv_empty(st));
       }
       if (!ok) record_error(err, kErrTimeout, kSiteAttnMma);
       if (any) {
@@ -179,134 +216,138 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     // ------------------------------------------------ softmax (warps 2..5)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // query row within the tile
-    const int q = q0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off;
     const uint32_t tO = tmem + lane_off + kOCol;
     const uint32_t tP = tmem + lane_off + kPCol;
     const float scale = 1.4426950408889634f * 0.125f;  // log2(e) / sqrt(64)
-    float m_run = -INFINITY;
-    float l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const bool got = mbar_wait(s_full, j & 1);
-      if (!__all_sync(0xffffffffu, got)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const bool diag = (j == qt);
-      // pass 1: row maximum of the raw scores (8 independent partial maxima,
-      // three-input max; the scale is positive, so it is applied once to the
-      // maximum).  In the diagonal tile, key chunk c holds keys
-      // c*32 .. c*32+31 of the tile against rows quad*32 + lane: chunks
-      // c > quad are above the diagonal for the whole warp and are skipped,
-      // chunk c == quad is masked per lane.
-      float pm[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) pm[e] = -INFINITY;
-#pragma unroll
-      for (int c2 = 0; c2 < kTk / 64; ++c2) {
-        if (diag && 2 * c2 > quad) break;
-        uint32_t raw[2][32];
-        tmem_ld_32x32b_x32(tS + c2 * 64, raw[0]);
-        tmem_ld_32x32b_x32(tS + c2 * 64 + 32, raw[1]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int c = 2 * c2 + h2;
-          if (diag && c >= quad) {
-            if (c == quad) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (i <= lane) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(raw[h2][i]));
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pm[i & 7] = max3f(pm[i & 7], __uint_as_float(raw[h2][2 * i]), __uint_as_float(raw[h2][2 * i + 1]));
-          }
-        }
-      }
-      const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * scale;
-      const bool raise = mx > m_run + kRescaleLog2;
-      // the previous P.V has read P and updated O
-      if (j > 0) {
-        const bool pv_ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1));
-        if (!pv_ok) {
+    long long g = 0;
+    for (int k = 0; ok; ++k) {
+      const int w = attn_item(k, cta, G);
+      if (w >= n_items) break;
+      const int qt = n_qt - 1 - w / BH, bh = w % BH;
+      const int b = bh / H, h = bh % H;
+      const int q = qt * kTq + r;
+      float m_run = -INFINITY;
+      float l = 0.f;
+      for (int j = 0; j <= qt; ++j, ++g) {
+        const bool got = mbar_wait(s_full, static_cast<uint32_t>(g & 1));
+        if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
         tc_fence_after();
-      }
-      // tcgen05.ld / tcgen05.st are warp-collective: the whole warp takes
-      // the rescale branch if any of its rows needs it (alpha = 1 for the
-      // others)
-      if (j > 0 && __any_sync(0xffffffffu, raise)) {
-        // O and l were accumulated against m_run: bring them to mx
-        const float alpha = raise ? ex2_approx(m_run - mx) : 1.f;
-        l *= alpha;
+        const bool diag = (j == qt);
+        // pass 1: row maximum of the raw scores (8 independent partial
+        // maxima, three-input max; the scale is positive, so it is applied
+        // once to the maximum).  In the diagonal tile, key chunk c holds
+        // keys c*32 .. c*32+31 of the tile against rows quad*32 + lane:
+        // chunks c > quad are above the diagonal for the whole warp and are
+        // skipped, chunk c == quad is masked per lane.
+        float pm[8];
 #pragma unroll
-        for (int c = 0; c < kHd / 32; ++c) {
-          uint32_t raw[32];
-          tmem_ld_32x32b_x32(tO + c * 32, raw);
+        for (int e = 0; e < 8; ++e) pm[e] = -INFINITY;
+#pragma unroll
+        for (int c2 = 0; c2 < kTk / 64; ++c2) {
+          if (diag && 2 * c2 > quad) break;
+          uint32_t raw[2][32];
+          tmem_ld_32x32b_x32(tS + c2 * 64, raw[0]);
+          tmem_ld_32x32b_x32(tS + c2 * 64 + 32, raw[1]);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) raw[i] = __float_as_uint(__uint_as_float(raw[i]) * alpha);
-          tmem_st_32x32b_x32(tO + c * 32, raw);
-        }
-      }
-      if (raise) m_run = mx;
-      // pass 2: P = exp2(s * scale - m_run) as 16-bit values into the P
-      // columns, paired fp32 arithmetic; 4 independent pair sums.  Chunks of
-      // the diagonal tile above the diagonal are written as zeros.
-      float2 ps[4];
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int c = 2 * c2 + h2;
+            if (diag && c >= quad) {
+              if (c == quad) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) ps[e] = make_float2(0.f, 0.f);
-      const float2 scale2 = make_float2(scale, scale);
-      const float2 neg_m2 = make_float2(-m_run, -m_run);
+                for (int i = 0; i < 32; ++i)
+                  if (i <= lane) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(raw[h2][i]));
+              }
+            } else {
 #pragma unroll
-      for (int c = 0; c < kTk / 32; ++c) {
-        uint32_t pk[16];
-        if (diag && c > quad) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = 0u;
-        } else {
-          uint32_t raw[32];
-          tmem_ld_32x32b_x32(tS + c * 32, raw);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 x = fma_f32x2(make_float2(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])),
-                                       scale2, neg_m2);
-            float2 p2 = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            if (diag && c == quad) {
-              if (2 * i > lane) p2.x = 0.f;
-              if (2 * i + 1 > lane) p2.y = 0.f;
+              for (int i = 0; i < 16; ++i)
+                pm[i & 7] = max3f(pm[i & 7], __uint_as_float(raw[h2][2 * i]), __uint_as_float(raw[h2][2 * i + 1]));
             }
-            ps[i & 3] = add_f32x2(ps[i & 3], p2);
-            pk[i] = Type16<T16>::pack2(p2.x, p2.y);
           }
         }
-        tmem_st_32x32b_x16(tP + c * 16, pk);
+        const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                               fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * scale;
+        const bool raise = mx > m_run + kRescaleLog2;
+        // the previous P.V of this item has read P and updated O
+        if (j > 0) {
+          const bool pv_ok = __all_sync(0xffffffffu, mbar_wait(pv_done, static_cast<uint32_t>((g - 1) & 1)));
+          if (!pv_ok) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        // tcgen05.ld / tcgen05.st are warp-collective: the whole warp takes
+        // the rescale branch if any of its rows needs it (alpha = 1 for the
+        // others)
+        if (j > 0 && __any_sync(0xffffffffu, raise)) {
+          // O and l were accumulated against m_run: bring them to mx
+          const float alpha = raise ? ex2_approx(m_run - mx) : 1.f;
+          l *= alpha;
+#pragma unroll
+          for (int c = 0; c < kHd / 32; ++c) {
+            uint32_t raw[32];
+            tmem_ld_32x32b_x32(tO + c * 32, raw);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) raw[i] = __float_as_uint(__uint_as_float(raw[i]) * alpha);
+            tmem_st_32x32b_x32(tO + c * 32, raw);
+          }
+        }
+        if (raise) m_run = mx;
+        // pass 2: P = exp2(s * scale - m_run) as 16-bit values into the P
+        // columns, paired fp32 arithmetic; 4 independent pair sums.  Chunks
+        // of the diagonal tile above the diagonal are written as zeros.
+        float2 ps[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ps[e] = make_float2(0.f, 0.f);
+        const float2 scale2 = make_float2(scale, scale);
+        const float2 neg_m2 = make_float2(-m_run, -m_run);
+#pragma unroll
+        for (int c = 0; c < kTk / 32; ++c) {
+          uint32_t pk[16];
+          if (diag && c > quad) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = 0u;
+          } else {
+            uint32_t raw[32];
+            tmem_ld_32x32b_x32(tS + c * 32, raw);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 x = fma_f32x2(make_float2(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])),
+                                         scale2, neg_m2);
+              float2 p2 = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              if (diag && c == quad) {
+                if (2 * i > lane) p2.x = 0.f;
+                if (2 * i + 1 > lane) p2.y = 0.f;
+              }
+              ps[i & 3] = add_f32x2(ps[i & 3], p2);
+              pk[i] = Type16<T16>::pack2(p2.x, p2.y);
+            }
+          }
+          tmem_st_32x32b_x16(tP + c * 16, pk);
+        }
+        l += ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y)) + ((ps[2].x + ps[2].y) + (ps[3].x + ps[3].y));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_ready);
       }
-      l += ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y)) + ((ps[2].x + ps[2].y) + (ps[3].x + ps[3].y));
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(p_ready);
-    }
-    // the last P.V has completed when pv_done reaches its n_kv-th phase
-    if (ok) {
-      const bool got = mbar_wait(pv_done, (n_kv - 1) & 1);
-      ok = __all_sync(0xffffffffu, got);
-    }
-    if (!ok) {
-      if (lane == 0) record_error(err, kErrTimeout, kSiteAttnSoftmax);
-    } else {
+      if (!ok) break;
+      // the item's last P.V has completed when pv_done reaches phase g - 1
+      if (!__all_sync(0xffffffffu, mbar_wait(pv_done, static_cast<uint32_t>((g - 1) & 1)))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const float inv = 1.f / l;
-      T16* orow = out + (static_cast<long long>(row_base) + q) * D + h * kHd;
+      T16* orow = out + (static_cast<long long>(b) * T + q) * D + h * kHd;
 #pragma unroll
       for (int c = 0; c < kHd / 32; ++c) {
         uint32_t raw[32];
@@ -315,16 +356,20 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         if (q < T) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            uint32_t w[4];
+            uint32_t wv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              w[e] = Type16<T16>::pack2(__uint_as_float(raw[v * 8 + 2 * e]) * inv,
-                                        __uint_as_float(raw[v * 8 + 2 * e + 1]) * inv);
-            *reinterpret_cast<uint4*>(orow + c * 32 + v * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+              wv[e] = Type16<T16>::pack2(__uint_as_float(raw[v * 8 + 2 * e]) * inv,
+                                         __uint_as_float(raw[v * 8 + 2 * e + 1]) * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + v * 8) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
           }
         }
       }
+      // O is read out before the next item's first P.V (which waits for
+      // this warp's first P of that item) overwrites it
+      tc_fence_before();
     }
+    if (!ok && lane == 0) record_error(err, kErrTimeout, kSiteAttnSoftmax);
   }
 
   tc_fence_before();
@@ -351,9 +396,16 @@ cudaError_t launch_t(const void* qkv, void* out, int B, int T, int n_head, cudaS
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  dim3 grid(B * n_head, (T + kTq - 1) / kTq);
-  return launch_pdl(attn_causal_tc<T16>, grid, kAttnThreads, kSmemBytes, stream, 0, map, static_cast<T16*>(out), T,
-                    n_head, device_error_word());
+  // persistent: two CTAs per SM (the launch bounds, 83 KB of shared memory
+  // and 256 tensor-memory columns each are sized for that), each walking its
+  // share of the (batch, head, query tile) items.  The block-occupancy query
+  // reports one per SM for this kernel on GB300 (measured: a 152-CTA grid
+  // runs at the speed of a one-per-SM launch), so the count is set directly.
+  const long long items = static_cast<long long>(B) * n_head * ((T + kTq - 1) / kTq);
+  const long long resident = 2ll * num_sms();
+  const int grid = static_cast<int>(items < resident ? items : resident);
+  return launch_pdl(attn_causal_tc<T16>, dim3(grid), kAttnThreads, kSmemBytes, stream, 0, map,
+                    static_cast<T16*>(out), B, T, n_head, device_error_word());
 }
 
 }  // namespace
