@@ -44,7 +44,7 @@ constexpr int kTq = 128;  // queries per CTA
 constexpr int kTk = 128;  // keys per tile
 constexpr int kAttnThreads = 192;
 constexpr int kTileBytes = kTq * kHd * 2;  // 16 KB, 128-byte rows, swizzled
-constexpr int kSmemBytes = 1024 + 5 * kTileBytes + 256;
+constexpr int kSmemBytes = 1024 + 6 * kTileBytes + 256;  // Q, K, V: two slots each
 constexpr uint32_t kTmemCols = 256;  // S: 128 columns, O: 64, P: 64
 constexpr uint32_t kOCol = 128;
 constexpr uint32_t kPCol = 192;
@@ -75,19 +75,21 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                    unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sQ = smem_u32(smem);
-  const uint32_t sK0 = sQ + kTileBytes;      // K stages 0, 1
-  const uint32_t sV0 = sQ + 3 * kTileBytes;  // V stages 0, 1
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 5 * kTileBytes);
-  const uint32_t q_full = smem_u32(bars + 0);
-  auto kv_full = [&](int s) { return smem_u32(bars + 1 + s); };
-  auto kv_empty = [&](int s) { return smem_u32(bars + 3 + s); };
-  const uint32_t s_full = smem_u32(bars + 5);
-  const uint32_t p_ready = smem_u32(bars + 6);
-  const uint32_t pv_done = smem_u32(bars + 7);
-  const uint32_t drain = smem_u32(bars + 8);
-  const uint32_t q_empty = smem_u32(bars + 9);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  const uint32_t sQ0 = smem_u32(smem);        // Q slots 0, 1 (items)
+  const uint32_t sK0 = sQ0 + 2 * kTileBytes;  // K slots 0, 1 (key tiles)
+  const uint32_t sV0 = sQ0 + 4 * kTileBytes;  // V slots 0, 1 (key tiles)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 6 * kTileBytes);
+  auto q_full = [&](int s) { return smem_u32(bars + 0 + s); };
+  auto q_empty = [&](int s) { return smem_u32(bars + 2 + s); };
+  auto k_full = [&](int s) { return smem_u32(bars + 4 + s); };
+  auto k_empty = [&](int s) { return smem_u32(bars + 6 + s); };
+  auto v_full = [&](int s) { return smem_u32(bars + 8 + s); };
+  auto v_empty = [&](int s) { return smem_u32(bars + 10 + s); };
+  const uint32_t s_full = smem_u32(bars + 12);
+  const uint32_t p_ready = smem_u32(bars + 13);
+  const uint32_t pv_done = smem_u32(bars + 14);
+  const uint32_t drain = smem_u32(bars + 15);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -99,11 +101,13 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_qkv);
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+      mbar_init(q_full(s), 1);
+      mbar_init(q_empty(s), 1);
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
     }
     mbar_init(s_full, 1);
     mbar_init(p_ready, 128);
@@ -123,89 +127,166 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   const uint32_t tmem = *tmem_slot;
 
   // Barrier phases run on across items: key tile g (counted over all items
-  // of this CTA) uses K/V stage g & 1 in its (g >> 1)-th round and the g-th
-  // phase of s_full / p_ready / pv_done; item i the i-th phase of q_full /
-  // q_empty.
+  // of this CTA) uses K and V slot g & 1 in its (g >> 1)-th round and the
+  // g-th phase of s_full / p_ready / pv_done; item i uses Q slot i & 1 in
+  // its (i >> 1)-th round.  A K slot is free again once its S = Q K^T has
+  // been computed, a V slot once its P.V has, so the producer issues each
+  // tile's K ahead of the V of the tile before: both then arrive about two
+  // key tiles ahead of their use, which covers the load latency.
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
-      long long g = 0;
+      struct Item {
+        int qt, row_base, h;
+      };
+      auto get_item = [&](int kk, Item& it) {
+        const int w = attn_item(kk, cta, G);
+        if (w >= n_items) return false;
+        const int bh = w % BH;
+        it.qt = n_qt - 1 - w / BH;
+        it.row_base = (bh / H) * T;
+        it.h = bh % H;
+        return true;
+      };
+      long long nq = 0, nk = 0, nv = 0;  // loads issued
+      auto load_q = [&](int kk, const Item& it) {
+        const int sl = kk & 1;
+        if (!mbar_wait(q_empty(sl), static_cast<uint32_t>((kk >> 1) & 1) ^ 1)) return false;
+        mbar_arrive_expect_tx(q_full(sl), kTileBytes);
+        tma_load_2d(sQ0 + sl * kTileBytes, &tm_qkv, q_full(sl), it.h * kHd, it.row_base + it.qt * kTq);
+        ++nq;
+        return true;
+      };
+      auto load_k = [&](long long gg, const Item& it, int jj) {
+        const int sl = static_cast<int>(gg & 1);
+        if (!mbar_wait(k_empty(sl), static_cast<uint32_t>((gg >> 1) & 1) ^ 1)) return false;
+        mbar_arrive_expect_tx(k_full(sl), kTileBytes);
+        tma_load_2d(sK0 + sl * kTileBytes, &tm_qkv, k_full(sl), D + it.h * kHd, it.row_base + jj * kTk);
+        ++nk;
+        return true;
+      };
+      auto load_v = [&](long long gg, const Item& it, int jj) {
+        const int sl = static_cast<int>(gg & 1);
+        if (!mbar_wait(v_empty(sl), static_cast<uint32_t>((gg >> 1) & 1) ^ 1)) return false;
+        mbar_arrive_expect_tx(v_full(sl), kTileBytes);
+        tma_load_2d(sV0 + sl * kTileBytes, &tm_qkv, v_full(sl), 2 * D + it.h * kHd, it.row_base + jj * kTk);
+        ++nv;
+        return true;
+      };
       bool ok = true;
-      int it = 0;
-      for (int k = 0; ok; ++k, ++it) {
-        const int w = attn_item(k, cta, G);
-        if (w >= n_items) break;
-        const int qt = n_qt - 1 - w / BH, bh = w % BH;
-        const int b = bh / H, h = bh % H;
-        const int row_base = b * T;
-        // the Q tile is free once the last S of the item before has been computed
-        if (it > 0 && !mbar_wait(q_empty, (it - 1) & 1)) {
-          record_error(err, kErrTimeout, kSiteAttnProducer);
-          break;
-        }
-        mbar_arrive_expect_tx(q_full, kTileBytes);
-        tma_load_2d(sQ, &tm_qkv, q_full, h * kHd, row_base + qt * kTq);
-        for (int j = 0; j <= qt; ++j, ++g) {
-          const int st = static_cast<int>(g & 1);
-          if (!mbar_wait(kv_empty(st), static_cast<uint32_t>((g >> 1) & 1) ^ 1)) {
-            record_error(err, kErrTimeout, kSiteAttnProducer);
+      Item cur;
+      if (get_item(0, cur)) {
+        int k = 0, j = 0;
+        long long g = 0;
+        ok = load_q(0, cur) && load_k(0, cur, 0);
+        while (ok) {
+          // the key tile after g: (k, j + 1), or the first of item k + 1
+          Item nx = cur;
+          int nk_i = k, nj = j + 1;
+          bool has_next = true;
+          if (nj > cur.qt) {
+            nk_i = k + 1;
+            nj = 0;
+            has_next = get_item(nk_i, nx);
+          }
+          if (has_next) {
+            if (nj == 0 && !load_q(nk_i, nx)) {
+              ok = false;
+              break;
+            }
+            if (!load_k(g + 1, nx, nj)) {
+              ok = false;
+              break;
+            }
+          }
+          if (!load_v(g, cur, j)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(kv_full(st), 2 * kTileBytes);
-          tma_load_2d(sK0 + st * kTileBytes, &tm_qkv, kv_full(st), D + h * kHd, row_base + j * kTk);
-          tma_load_2d(sV0 + st * kTileBytes, &tm_qkv, kv_full(st), 2 * D + h * kHd, row_base + j * kTk);
+          if (!has_next) break;
+          cur = nx;
+          k = nk_i;
+          j = nj;
+          ++g;
         }
       }
-      // copies still in flight: the last Q tile and the last (up to two) stages
-      if (it > 0 && !mbar_wait(q_full, (it - 1) & 1)) record_error(err, kErrTimeout, kSiteAttnProducer);
-      for (long long x = g > 2 ? g - 2 : 0; x < g; ++x)
-        if (!mbar_wait(kv_full(static_cast<int>(x & 1)), static_cast<uint32_t>((x >> 1) & 1))) {
-          record_error(err, kErrTimeout, kSiteAttnProducer);
-          break;
-        }
+      if (!ok) record_error(err, kErrTimeout, kSiteAttnProducer);
+      // copies still in flight: the last (up to two) of each kind
+      bool drained = true;
+      for (long long x = nq > 2 ? nq - 2 : 0; x < nq && drained; ++x)
+        drained = mbar_wait(q_full(static_cast<int>(x & 1)), static_cast<uint32_t>((x >> 1) & 1));
+      for (long long x = nk > 2 ? nk - 2 : 0; x < nk && drained; ++x)
+        drained = mbar_wait(k_full(static_cast<int>(x & 1)), static_cast<uint32_t>((x >> 1) & 1));
+      for (long long x = nv > 2 ? nv - 2 : 0; x < nv && drained; ++x)
+        drained = mbar_wait(v_full(static_cast<int>(x & 1)), static_cast<uint32_t>((x >> 1) & 1));
+      if (!drained) record_error(err, kErrTimeout, kSiteAttnProducer);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
       constexpr uint32_t idesc_s = idesc_f16kind_f32(kTq, kTk, false, false, Type16<T16>::kFormat);
       constexpr uint32_t idesc_pv = idesc_f16kind_f32(kTq, kHd, false, true, Type16<T16>::kFormat);
+      // Per key tile g: S(g) as soon as the softmax has released the S
+      // columns (p_ready of g - 1), then P.V of tile g - 1; so the softmax
+      // of tile g (its row maxima) runs while P.V(g - 1) does.
       bool ok = true;
       bool any = false;
       long long g = 0;
-      int it = 0;
-      for (int k = 0; ok; ++k, ++it) {
+      int prev_j = 0;     // tile index within its item of tile g - 1
+      int prev_st = 0;    // its K / V slot
+      uint32_t prev_ph = 0;
+      auto pv = [&](long long gp, int jj, int st, uint32_t ph) {
+        // P.V of tile gp: P (tensor memory) is published once p_ready
+        // reaches phase gp; V arrives on v_full
+        if (!mbar_wait(p_ready, static_cast<uint32_t>(gp & 1)) || !mbar_wait(v_full(st), ph)) return false;
+        tc_fence_after();
+        const uint32_t vb = sV0 + st * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTk / 16; ++kk)  // P: 8 tensor-memory columns (16 bf16) per K=16
+          umma_bf16_ts(tmem + kOCol, tmem + kPCol + kk * 8, sdesc_sw128(vb + kk * 2048, 8192, 1024), idesc_pv,
+                       (jj | kk) != 0 ? 1u : 0u);
+        umma_commit(pv_done);
+        umma_commit(v_empty(st));
+        return true;
+      };
+      for (int k = 0; ok; ++k) {
         const int w = attn_item(k, cta, G);
         if (w >= n_items) break;
         const int qt = n_qt - 1 - w / BH;
-        ok = mbar_wait(q_full, it & 1);
+        const int qs = k & 1;
+        ok = mbar_wait(q_full(qs), static_cast<uint32_t>((k >> 1) & 1));
+        const uint32_t qb = sQ0 + qs * kTileBytes;
         for (int j = 0; j <= qt && ok; ++j, ++g) {
           const int st = static_cast<int>(g & 1);
-          ok = mbar_wait(kv_full(st), static_cast<uint32_t>((g >> 1) & 1));
+          const uint32_t ph = static_cast<uint32_t>((g >> 1) & 1);
+          // the softmax of tile g - 1 has read S (and written P)
+          if (g > 0 && !mbar_wait(p_ready, static_cast<uint32_t>((g - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          ok = mbar_wait(k_full(st), ph);
           if (!ok) break;
           tc_fence_after();
           const uint32_t kb = sK0 + st * kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < kHd / 16; ++kk)
-            umma_bf16(tmem, sdesc_sw128(sQ + kk * 32, 16, 1024), sdesc_sw128(kb + kk * 32, 16, 1024), idesc_s,
+            umma_bf16(tmem, sdesc_sw128(qb + kk * 32, 16, 1024), sdesc_sw128(kb + kk * 32, 16, 1024), idesc_s,
                       kk > 0 ? 1u : 0u);
           umma_commit(s_full);
-          if (j == qt) umma_commit(q_empty);  // the item's last read of Q
+          umma_commit(k_empty(st));
+          if (j == qt) umma_commit(q_empty(qs));  // the item's last read of its Q
           any = true;
-          if (!mbar_wait(p_ready, static_cast<uint32_t>(g & 1))) {
+          if (g > 0 && !pv(g - 1, prev_j, prev_st, prev_ph)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint32_t vb = sV0 + st * kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < kTk / 16; ++kk)  // P: 8 tensor-memory columns (16 bf16) per K=16
-            umma_bf16_ts(tmem + kOCol, tmem + kPCol + kk * 8, sdesc_sw128(vb + kk * 2048, 8192, 1024), idesc_pv,
-                         (j | kk) != 0 ? 1u : 0u);
-          umma_commit(pv_done);
-          umma_commit(kv_empty(st));
+          prev_j = j;
+          prev_st = st;
+          prev_ph = ph;
         }
       }
+      // the last tile's P.V
+      if (ok && g > 0 && !pv(g - 1, prev_j, prev_st, prev_ph)) ok = false;
       if (!ok) record_error(err, kErrTimeout, kSiteAttnMma);
       if (any) {
         umma_commit(drain);
