@@ -20,8 +20,11 @@
 //                      tensor memory and V from shared memory (MN-major)
 // Tensor memory: S columns 0-127, O 128-191, P 192-255.  As soon as the
 // softmax of tile j has published P (and so finished reading S), the MMA
-// warp issues P.V for tile j and then S for tile j + 1, which overlap; the
-// softmax waits for that P.V before it rescales O or writes the next P.
+// warp issues S for tile j + 1 and then P.V for tile j, so that the next
+// softmax computes its row maxima while P.V runs; the softmax waits for
+// that P.V before it rescales O or writes the next P.  Q, K and V sit in
+// separate two-slot rings: a K slot is refilled as soon as its S has been
+// computed, a V slot once its P.V has.
 // The running maximum m is only raised (and O, l rescaled) when a row's new
 // maximum exceeds it by more than 8 in the log2 domain; otherwise P may reach
 // 2^8, harmless in fp32 sums and bf16.  Key tiles entirely above the
