@@ -5,7 +5,7 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 package imports nothing from it.
 """
 from .gpt2_ref import (  # noqa: F401
-    argmax_lowest, block_forward, causal_attention, causal_probs, conv1d, decode_step, embed,
-    forward_hidden, forward_logits, forward_loss, gelu_new, layer_norm, lm_head, merge_heads, mlp_forward,
+    argmax_lowest, attn_extra_scale, block_forward, causal_attention, causal_probs, conv1d, decode_step, embed,
+    forward_hidden, forward_logits, forward_loss, gelu_exact, gelu_new, layer_norm, lm_head, merge_heads, mlp_forward,
     logsumexp, prefill_cache, shifted_cross_entropy, split_qkv_heads,
 )

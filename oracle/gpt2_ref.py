@@ -68,6 +68,21 @@ def gelu_new(x):
     return 0.5 * x * (1.0 + np.tanh(math.sqrt(2.0 / math.pi) * (x + 0.044715 * x ** 3)))
 
 
+def gelu_exact(x):
+    """x * Phi(x) = 0.5 x (1 + erf(x / sqrt(2))), Phi the standard normal CDF.
+
+    llm.c notes 4.2 (GELU is x times the normal CDF; the tanh form above is
+    its usual approximation).  The MLP uses it when the model's
+    ``gelu_exact`` switch is on.
+    """
+    x = _f64(x)
+    return 0.5 * x * (1.0 + _erf(x / math.sqrt(2.0)))
+
+
+def _erf(x):
+    return np.vectorize(math.erf, otypes=[F64])(x)
+
+
 # ------------------------------------------------------------------- Conv1D
 def conv1d(x, w, b):
     """Hugging Face Conv1D: bias + x @ W with W stored [in, out].
@@ -103,7 +118,7 @@ def merge_heads(o):
     return o.transpose(0, 2, 1, 3).reshape(B, T, H * hd)
 
 
-def causal_probs(q, k):
+def causal_probs(q, k, extra_scale=1.0):
     """softmax over j <= i of q_i . k_j / sqrt(hd), per head.
 
     "逐行拆GPT-2源码", ``_attn``: scores = Q K^T / sqrt(value.size(-1)); the
@@ -115,7 +130,7 @@ def causal_probs(q, k):
     q, k = _f64(q), _f64(k)
     hd = q.shape[-1]
     Tq, Tk = q.shape[-2], k.shape[-2]
-    s = (q @ np.swapaxes(k, -1, -2)) / math.sqrt(hd)
+    s = (q @ np.swapaxes(k, -1, -2)) / math.sqrt(hd) * extra_scale
     qpos = np.arange(Tk - Tq, Tk)[:, None]
     kpos = np.arange(Tk)[None, :]
     s = np.where(kpos <= qpos, s, -np.inf)
@@ -124,35 +139,51 @@ def causal_probs(q, k):
     return e / e.sum(axis=-1, keepdims=True)
 
 
-def causal_attention(qkv, n_head):
-    """Multi-head causal self-attention on packed QKV [B, T, 3D] -> [B, T, D]."""
+def causal_attention(qkv, n_head, extra_scale=1.0):
+    """Multi-head causal self-attention on packed QKV [B, T, 3D] -> [B, T, D].
+
+    extra_scale multiplies the scores after the 1/sqrt(hd) scale ("逐行拆GPT-2
+    源码", GPT2Config section: with scale_attn_by_inverse_layer_idx each
+    layer's scores are further divided by layer_idx + 1).
+    """
     q, k, v = split_qkv_heads(qkv, n_head)
-    p = causal_probs(q, k)
+    p = causal_probs(q, k, extra_scale)
     return merge_heads(p @ v)
 
 
 # -------------------------------------------------------------------- block
-def block_forward(x, blk, n_head, eps):
+def attn_extra_scale(layer, scale_attn_by_inverse_layer_idx):
+    """1 / (layer + 1) with the switch on, else 1 (layer counted from 0)."""
+    return 1.0 / (layer + 1) if scale_attn_by_inverse_layer_idx else 1.0
+
+
+def block_forward(x, blk, n_head, eps, layer=0, scale_attn_by_inverse_layer_idx=False, gelu_exact_mlp=False):
     """One Pre-LN block, [B, T, D] -> [B, T, D].
 
     "Hidden State 如何流过 GPT-2 Block", section "GPT-2 Block":
     A = Attention(LN_attn(X)); H = X + A; M = MLP(LN_ffn(H)); X' = H + M.
     Attention = c_proj(merge(softmax-attention(split(c_attn(.))))) and
     MLP = c_proj(gelu_new(c_fc(.))) ("逐行拆GPT-2源码", GPT2Block / GPT2MLP).
+    The two GPT2Config switches change the attention scale of layer
+    ``layer`` and the MLP activation (gelu_exact).
     """
     x = _f64(x)
     a = layer_norm(x, blk["ln1_g"], blk["ln1_b"], eps)
     qkv = conv1d(a, blk["w_qkv"], blk["b_qkv"])
-    o = causal_attention(qkv, n_head)
+    o = causal_attention(qkv, n_head, attn_extra_scale(layer, scale_attn_by_inverse_layer_idx))
     h = x + conv1d(o, blk["w_o"], blk["b_o"])
-    m = conv1d(gelu_new(conv1d(layer_norm(h, blk["ln2_g"], blk["ln2_b"], eps), blk["w_fc"], blk["b_fc"])),
-               blk["w_proj"], blk["b_proj"])
-    return h + m
+    return h + mlp_forward(layer_norm(h, blk["ln2_g"], blk["ln2_b"], eps), blk, gelu_exact_mlp)
 
 
-def mlp_forward(a, blk):
-    """MLP on an already-normalised input: c_proj(gelu_new(c_fc(a)))."""
-    return conv1d(gelu_new(conv1d(a, blk["w_fc"], blk["b_fc"])), blk["w_proj"], blk["b_proj"])
+def mlp_forward(a, blk, gelu_exact_mlp=False):
+    """MLP on an already-normalised input: c_proj(act(c_fc(a))), act gelu_new
+    (or the exact GELU with the switch on)."""
+    act = gelu_exact if gelu_exact_mlp else gelu_new
+    return conv1d(act(conv1d(a, blk["w_fc"], blk["b_fc"])), blk["w_proj"], blk["b_proj"])
+
+
+def _switches(dims):
+    return (getattr(dims, "scale_attn_by_inverse_layer_idx", False), getattr(dims, "gelu_exact", False))
 
 
 # ------------------------------------------------------------ whole model
@@ -170,8 +201,9 @@ def embed(tokens, wte, wpe, pos0=0):
 def forward_hidden(tokens, params, dims):
     """Embedding, then the stack of blocks; returns the final residual stream."""
     x = embed(tokens, params["wte"], params["wpe"])
-    for blk in params["blocks"]:
-        x = block_forward(x, blk, dims.n_head, dims.eps)
+    inv, ge = _switches(dims)
+    for l, blk in enumerate(params["blocks"]):
+        x = block_forward(x, blk, dims.n_head, dims.eps, l, inv, ge)
     return x
 
 
@@ -257,6 +289,7 @@ def decode_step(params, dims, cache, past_len, tokens):
     D, H = dims.d_model, dims.n_head
     hd = D // H
     x = np.stack([_f64(params["wte"])[tokens[b]] + _f64(params["wpe"])[past_len[b]] for b in range(B)])
+    inv, ge = _switches(dims)
     for l, blk in enumerate(params["blocks"]):
         a = layer_norm(x, blk["ln1_g"], blk["ln1_b"], dims.eps)
         qkv = conv1d(a, blk["w_qkv"], blk["b_qkv"])
@@ -268,10 +301,10 @@ def decode_step(params, dims, cache, past_len, tokens):
             cache[l, 1, b, :, p, :] = qkv[b, 2 * D:].reshape(H, hd)
             k = cache[l, 0, b, :, :p + 1, :]
             v = cache[l, 1, b, :, :p + 1, :]
-            pr = causal_probs(q, k)            # the query is the last position
+            pr = causal_probs(q, k, attn_extra_scale(l, inv))  # the query is the last position
             o[b] = (pr @ v).reshape(D)
         h = x + conv1d(o, blk["w_o"], blk["b_o"])
-        x = h + mlp_forward(layer_norm(h, blk["ln2_g"], blk["ln2_b"], dims.eps), blk)
+        x = h + mlp_forward(layer_norm(h, blk["ln2_g"], blk["ln2_b"], dims.eps), blk, ge)
     logits = lm_head(x, params, dims)
     return argmax_lowest(logits), logits, cache, past_len + 1
 
@@ -284,11 +317,12 @@ def prefill_cache(tokens, params, dims, T_max):
     hd = D // H
     cache = np.zeros((dims.n_layer, 2, B, H, T_max, hd))
     x = embed(tokens, params["wte"], params["wpe"])
+    inv, ge = _switches(dims)
     for l, blk in enumerate(params["blocks"]):
         a = layer_norm(x, blk["ln1_g"], blk["ln1_b"], dims.eps)
         qkv = conv1d(a, blk["w_qkv"], blk["b_qkv"])
         _, k, v = split_qkv_heads(qkv, H)
         cache[l, 0, :, :, :T] = k
         cache[l, 1, :, :, :T] = v
-        x = block_forward(x, blk, H, dims.eps)
+        x = block_forward(x, blk, H, dims.eps, l, inv, ge)
     return cache

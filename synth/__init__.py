@@ -47,6 +47,11 @@ class Dims:
     vocab: int
     n_pos: int
     eps: float = 1e-5
+    # GPT2Config switches the pages name (both off for the GPT-2 workloads):
+    # attention scores of layer l also divided by l + 1, and the exact GELU
+    # x * Phi(x) in the MLP instead of its tanh approximation
+    scale_attn_by_inverse_layer_idx: bool = False
+    gelu_exact: bool = False
 
     @property
     def head_dim(self) -> int:

@@ -269,7 +269,9 @@ def _torch_model_logits(tokens, p, dims):
 
     Pre-LN blocks (x + attn(ln_1(x)); x + mlp(ln_2(x))), Conv1D-style
     ``addmm(bias, x, W)``, tanh GELU, causal SDPA, learned positions, final
-    LayerNorm and a head tied to wte.
+    LayerNorm and a head tied to wte.  The GPT2Config switches map onto
+    SDPA's ``scale`` (1 / (sqrt(hd) (l + 1)) for layer l) and torch's exact
+    GELU.
     """
     t = lambda a: torch.from_numpy(np.asarray(a, np.float64))  # noqa: E731
     D, H = dims.d_model, dims.n_head
@@ -277,16 +279,17 @@ def _torch_model_logits(tokens, p, dims):
     idx = torch.from_numpy(tokens)
     B, T = idx.shape
     x = t(p["wte"])[idx] + t(p["wpe"])[:T]
-    for b in p["blocks"]:
+    for l, b in enumerate(p["blocks"]):
         a = Fn.layer_norm(x, (D,), t(b["ln1_g"]), t(b["ln1_b"]), eps=dims.eps)
         qkv = torch.addmm(t(b["b_qkv"]), a.reshape(-1, D), t(b["w_qkv"])).view(B, T, 3 * D)
         q, k, v = qkv.split(D, dim=2)
         sh = lambda z: z.view(B, T, H, hd).permute(0, 2, 1, 3)  # noqa: E731
-        o = Fn.scaled_dot_product_attention(sh(q), sh(k), sh(v), is_causal=True)
+        sc = 1.0 / math.sqrt(hd) / ((l + 1) if dims.scale_attn_by_inverse_layer_idx else 1)
+        o = Fn.scaled_dot_product_attention(sh(q), sh(k), sh(v), is_causal=True, scale=sc)
         o = o.permute(0, 2, 1, 3).reshape(B * T, D)
         x = x + torch.addmm(t(b["b_o"]), o, t(b["w_o"])).view(B, T, D)
         a = Fn.layer_norm(x, (D,), t(b["ln2_g"]), t(b["ln2_b"]), eps=dims.eps).reshape(-1, D)
-        g = Fn.gelu(torch.addmm(t(b["b_fc"]), a, t(b["w_fc"])), approximate="tanh")
+        g = Fn.gelu(torch.addmm(t(b["b_fc"]), a, t(b["w_fc"])), approximate="none" if dims.gelu_exact else "tanh")
         x = x + torch.addmm(t(b["b_proj"]), g, t(b["w_proj"])).view(B, T, D)
     x = Fn.layer_norm(x, (D,), t(p["lnf_g"]), t(p["lnf_b"]), eps=dims.eps)
     return (x @ t(p["wte"]).T).numpy()
@@ -541,3 +544,86 @@ def test_prefill_cache_equals_token_by_token_decode():
         _, _, cache, past = O.decode_step(p, dims, cache, past, tokens[:, t])
     np.testing.assert_allclose(cache, ref, rtol=1e-11, atol=1e-12)
     assert np.all(ref[:, :, :, :, 9:] == 0)
+
+
+# ------------------------------------------------ GPT2Config variants
+def test_gelu_exact_matches_torch_and_identities():
+    """x Phi(x): torch's exact GELU in fp64; Phi(1) = 0.8413447460685429;
+    gelu(-x) = gelu(x) - x (Phi(-x) = 1 - Phi(x)); the tanh form of the
+    pages stays within 1e-3 of it.
+
+    Catches: a missing 1/sqrt(2), the tanh form in place of erf, a sign.
+    """
+    x = np.linspace(-8, 8, 4001)
+    ref = Fn.gelu(torch.from_numpy(x), approximate="none").numpy()
+    np.testing.assert_allclose(O.gelu_exact(x), ref, rtol=1e-13, atol=1e-15)
+    assert abs(O.gelu_exact(np.array([1.0]))[0] - 0.8413447460685429) < 1e-15
+    np.testing.assert_allclose(O.gelu_exact(-x), O.gelu_exact(x) - x, rtol=1e-12, atol=1e-13)
+    assert np.max(np.abs(O.gelu_exact(x) - O.gelu_new(x))) < 1e-3
+    assert np.max(np.abs(O.gelu_exact(x) - O.gelu_new(x))) > 1e-5  # the two differ
+
+
+def test_attention_extra_scale_matches_sdpa_and_scales_q():
+    """With scale_attn_by_inverse_layer_idx, layer l's scores are divided by
+    l + 1 as well: torch SDPA with scale 1/(8 (l + 1)) in fp64, and the same
+    as attention with every query divided by l + 1."""
+    B, T, H = 2, 33, 2
+    qkv = RNG.standard_normal((B, T, 3 * 64 * H)) * 2.0
+    for l in (0, 1, 5):
+        got = O.causal_attention(qkv, H, O.attn_extra_scale(l, True))
+        q, k, v = (torch.from_numpy(z) for z in O.split_qkv_heads(qkv, H))
+        ref = Fn.scaled_dot_product_attention(q, k, v, is_causal=True, scale=1.0 / (8.0 * (l + 1)))
+        np.testing.assert_allclose(got, O.merge_heads(ref.numpy()), rtol=1e-12, atol=1e-13)
+        qkv2 = qkv.copy()
+        qkv2[..., :64 * H] /= (l + 1)
+        np.testing.assert_allclose(got, O.causal_attention(qkv2, H), rtol=1e-12, atol=1e-13)
+    assert O.attn_extra_scale(3, False) == 1.0
+
+
+def test_variant_stack_matches_torch_modules():
+    """Both switches on and n_inner = 192 (not 4 D = 512): the oracle against
+    the torch module stack.  The weights are large enough that the switches
+    change the logits by far more than the tolerance (checked), so a switch
+    the oracle ignored would fail."""
+    base = Dims(n_layer=3, d_model=128, n_head=2, d_ff=192, vocab=61, n_pos=40)
+    var = Dims(n_layer=3, d_model=128, n_head=2, d_ff=192, vocab=61, n_pos=40,
+               scale_attn_by_inverse_layer_idx=True, gelu_exact=True)
+    p = _toy_params(base, seed=9)
+    for b in p["blocks"]:
+        for k in ("w_qkv", "w_o", "w_fc", "w_proj"):
+            b[k] = b[k] / 2.0
+    assert p["blocks"][0]["w_fc"].shape == (128, 192)
+    tokens = RNG.integers(0, base.vocab, size=(2, 29)).astype(np.int32)
+    got = O.forward_logits(tokens, p, var)
+    np.testing.assert_allclose(got, _torch_model_logits(tokens, p, var), rtol=1e-10, atol=1e-10)
+    assert np.max(np.abs(got - O.forward_logits(tokens, p, base))) > 1e-4
+    for one in (Dims(**{**base.__dict__, "gelu_exact": True}),
+                Dims(**{**base.__dict__, "scale_attn_by_inverse_layer_idx": True})):
+        np.testing.assert_allclose(O.forward_logits(tokens, p, one), _torch_model_logits(tokens, p, one),
+                                   rtol=1e-10, atol=1e-10)
+
+
+def test_inverse_layer_scale_leaves_layer_zero():
+    """Layer 0 is divided by 1: a one-layer model is the same with the
+    switch on or off."""
+    d0 = Dims(n_layer=1, d_model=128, n_head=2, d_ff=512, vocab=31, n_pos=20)
+    d1 = Dims(n_layer=1, d_model=128, n_head=2, d_ff=512, vocab=31, n_pos=20, scale_attn_by_inverse_layer_idx=True)
+    p = _toy_params(d0, seed=2)
+    tokens = RNG.integers(0, 31, size=(1, 17)).astype(np.int32)
+    assert np.array_equal(O.forward_logits(tokens, p, d0), O.forward_logits(tokens, p, d1))
+
+
+def test_variant_decode_and_prefill_follow_the_switches():
+    """Decode after prefill equals the full forward's rows with both
+    switches on (the decode path takes the layer-indexed scale and the exact
+    GELU too)."""
+    dims = Dims(n_layer=2, d_model=128, n_head=2, d_ff=192, vocab=41, n_pos=24,
+                scale_attn_by_inverse_layer_idx=True, gelu_exact=True)
+    p = _toy_params(dims, seed=12)
+    tokens = RNG.integers(0, dims.vocab, size=(2, 16)).astype(np.int32)
+    full = O.forward_logits(tokens, p, dims)
+    cache = O.prefill_cache(tokens[:, :10], p, dims, T_max=24)
+    past = np.full(2, 10, np.int32)
+    for step in range(10, 16):
+        _, logits, cache, past = O.decode_step(p, dims, cache, past, tokens[:, step])
+        np.testing.assert_allclose(logits, full[:, step], rtol=1e-10, atol=1e-10)
