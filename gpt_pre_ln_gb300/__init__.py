@@ -13,9 +13,10 @@ import ctypes
 import os
 
 __all__ = [
-    "GPT2Error", "F32", "BF16", "F16", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_GELU", "EPI_BIAS_RESIDUAL", "W_IN_OUT",
-    "W_OUT_IN", "Dims", "BlockWeights", "ModelWeights", "lib", "library_path", "gpt2_abi_version",
+    "GPT2Error", "F32", "BF16", "F16", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_GELU", "EPI_BIAS_RESIDUAL",
+    "EPI_BIAS_GELU_EXACT", "SCALE_ATTN_BY_INVERSE_LAYER_IDX", "GELU_EXACT", "W_IN_OUT", "W_OUT_IN", "Dims", "BlockWeights", "ModelWeights", "lib", "library_path", "gpt2_abi_version",
     "gpt2_status_string", "gpt2_last_error", "gpt2_layernorm", "gpt2_linear", "gpt2_attention_causal",
+    "gpt2_attention_causal_scaled", "gpt2_block_forward_layer",
     "gpt2_mlp_workspace_bytes", "gpt2_mlp", "gpt2_mlp_noalloc", "gpt2_mlp_noalloc_max_scratch_bytes",
     "gpt2_workspace_bytes", "gpt2_block_forward", "gpt2_forward_logits", "gpt2_loss_workspace_bytes",
     "gpt2_forward_loss", "gpt2_prefill_workspace_bytes", "gpt2_prefill",
@@ -28,7 +29,9 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 library_path = os.environ.get("GPT2GB_LIBRARY") or os.path.join(_PKG, "libgpt2gb.so")
 
 F32, BF16, F16 = 0, 1, 2
-EPI_NONE, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESIDUAL = 0, 1, 2, 3
+EPI_NONE, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESIDUAL, EPI_BIAS_GELU_EXACT = 0, 1, 2, 3, 4
+# GPT2Config switches (gpt2_dims.flags)
+SCALE_ATTN_BY_INVERSE_LAYER_IDX, GELU_EXACT = 1, 2
 W_IN_OUT, W_OUT_IN = 0, 1
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or type", 3: "workspace too small",
@@ -44,7 +47,7 @@ class GPT2Error(RuntimeError):
 class Dims(ctypes.Structure):
     _fields_ = [("n_layer", ctypes.c_int), ("d_model", ctypes.c_int), ("n_head", ctypes.c_int),
                 ("d_ff", ctypes.c_int), ("vocab", ctypes.c_int), ("n_pos", ctypes.c_int), ("eps", ctypes.c_float),
-                ("dtype", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("flags", ctypes.c_uint)]
 
 
 _BLOCK_FIELDS = ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_g", "ln2_b", "w_fc", "b_fc", "w_proj",
@@ -74,11 +77,14 @@ _SIGS = {
     "gpt2_layernorm": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _F, _I32, _I32, _VP]),
     "gpt2_linear": (_I32, [_VP, _VP, _VP, _VP, _VP, _I64, _I32, _I32, _I64, _I32, _I32, _I32, _I32, _VP]),
     "gpt2_attention_causal": (_I32, [_VP, _VP, _I32, _I32, _I32, _I32, _I32, _VP]),
+    "gpt2_attention_causal_scaled": (_I32, [_VP, _VP, _I32, _I32, _I32, _I32, _F, _I32, _VP]),
     "gpt2_mlp_workspace_bytes": (_SZ, [_I64, _I32, _I32]),
     "gpt2_mlp": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I32, _I32, _VP, _SZ, _I32, _VP]),
     "gpt2_workspace_bytes": (_SZ, [ctypes.POINTER(Dims), _I32, _I32]),
     "gpt2_block_forward": (_I32, [ctypes.POINTER(Dims), ctypes.POINTER(BlockWeights), _VP, _VP, _I32, _I32, _VP, _SZ,
                                   _VP]),
+    "gpt2_block_forward_layer": (_I32, [ctypes.POINTER(Dims), ctypes.POINTER(BlockWeights), _I32, _VP, _VP, _I32, _I32,
+                                        _VP, _SZ, _VP]),
     "gpt2_forward_logits": (_I32, [ctypes.POINTER(Dims), ctypes.POINTER(ModelWeights), _VP, _VP, _I64, _I32, _I32,
                                    _I32, _VP, _SZ, _VP]),
     "gpt2_loss_workspace_bytes": (_SZ, [ctypes.POINTER(Dims), _I32, _I32]),
@@ -167,6 +173,11 @@ def gpt2_attention_causal(qkv, out, B, T, n_head, head_dim, dtype, stream=None):
            "gpt2_attention_causal")
 
 
+def gpt2_attention_causal_scaled(qkv, out, B, T, n_head, head_dim, score_scale, dtype, stream=None):
+    _check(lib().gpt2_attention_causal_scaled(_ptr(qkv), _ptr(out), B, T, n_head, head_dim, score_scale, dtype,
+                                              _stream(stream)), "gpt2_attention_causal_scaled")
+
+
 def gpt2_mlp_workspace_bytes(M, F, dtype) -> int:
     return lib().gpt2_mlp_workspace_bytes(M, F, dtype)
 
@@ -193,6 +204,11 @@ def gpt2_workspace_bytes(dims: Dims, B: int, T: int) -> int:
 def gpt2_block_forward(dims: Dims, w: BlockWeights, x_in, x_out, B, T, ws, ws_bytes, stream=None):
     _check(lib().gpt2_block_forward(ctypes.byref(dims), ctypes.byref(w), _ptr(x_in), _ptr(x_out), B, T, _ptr(ws),
                                     ws_bytes, _stream(stream)), "gpt2_block_forward")
+
+
+def gpt2_block_forward_layer(dims: Dims, w: BlockWeights, layer, x_in, x_out, B, T, ws, ws_bytes, stream=None):
+    _check(lib().gpt2_block_forward_layer(ctypes.byref(dims), ctypes.byref(w), layer, _ptr(x_in), _ptr(x_out), B, T,
+                                          _ptr(ws), ws_bytes, _stream(stream)), "gpt2_block_forward_layer")
 
 
 def gpt2_forward_logits(dims: Dims, w: ModelWeights, tokens, logits, ld, logits_t, B, T, ws, ws_bytes, stream=None):
@@ -255,8 +271,8 @@ def gpt2_profile_read(max_entries: int = 64):
 
 
 # ------------------------------------------------------ weight marshalling
-def make_dims(n_layer, d_model, n_head, d_ff, vocab, n_pos, eps=1e-5, dtype=BF16) -> Dims:
-    return Dims(n_layer, d_model, n_head, d_ff, vocab, n_pos, eps, dtype)
+def make_dims(n_layer, d_model, n_head, d_ff, vocab, n_pos, eps=1e-5, dtype=BF16, flags=0) -> Dims:
+    return Dims(n_layer, d_model, n_head, d_ff, vocab, n_pos, eps, dtype, flags)
 
 
 def block_weights(tensors: dict) -> BlockWeights:

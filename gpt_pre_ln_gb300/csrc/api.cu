@@ -7,10 +7,12 @@
 //   a   = LN_1(x)                          layernorm (fused with the
 //                                          embedding for the first block)
 //   qkv = a W_qkv + b_qkv                  GEMM, epilogue + bias
-//   o   = causal attention(qkv)            attention kernel
+//   o   = causal attention(qkv)            attention kernel (scores / 8, and
+//                                          / (layer + 1) with that switch)
 //   h   = x + o W_o + b_o                  GEMM, epilogue + bias + residual
 //   a   = LN_2(h)                          layernorm
 //   g   = gelu_new(a W_fc + b_fc)          GEMM, epilogue gelu_new(+ bias)
+//                                          (the exact GELU with that switch)
 //   x'  = h + g W_proj + b_proj            GEMM, epilogue + bias + residual
 // then LN_f and the tied lm_head (GEMM against wte [V, D], no bias).
 #include <climits>
@@ -72,7 +74,7 @@ using namespace gpt2;
 
 namespace {
 
-constexpr int kAbiVersion = 2;
+constexpr int kAbiVersion = 3;
 
 // ------------------------------------------------------------- profiler
 struct ProfRec {
@@ -156,6 +158,7 @@ int check_dims(const gpt2_dims* d, bool need_model) {
   if (!(d->eps > 0.f) || !std::isfinite(d->eps)) return GPT2_ERR_ARG;
   if (d->d_model % d->n_head != 0 || d->d_model / d->n_head != 64) return GPT2_ERR_UNSUPPORTED;
   if (d->d_model > 4096 || d->d_ff % 64 != 0 || d->d_ff > 65536) return GPT2_ERR_UNSUPPORTED;
+  if (d->flags & ~static_cast<unsigned>(GPT2_SCALE_ATTN_BY_INVERSE_LAYER_IDX | GPT2_GELU_EXACT)) return GPT2_ERR_ARG;
   if (need_model) {
     if (d->n_layer <= 0 || d->vocab <= 0 || d->n_pos <= 0) return GPT2_ERR_ARG;
   }
@@ -197,14 +200,24 @@ cudaError_t linear(gpt2_dtype dt, const void* x, const void* w, const void* bias
                          res, static_cast<float*>(y), M, N, K, ldy, w_out_in, epi, s);
 }
 
-cudaError_t attention(gpt2_dtype dt, const void* qkv, void* out, int B, int T, int H, cudaStream_t s) {
+// Scores q.k / sqrt(64), and with GPT2_SCALE_ATTN_BY_INVERSE_LAYER_IDX also
+// / (layer + 1) ("逐行拆GPT-2源码", GPT2Config section).
+float score_scale(const gpt2_dims* d, int layer) {
+  const float base = 0.125f;  // 1 / sqrt(head_dim), head_dim = 64
+  return (d->flags & GPT2_SCALE_ATTN_BY_INVERSE_LAYER_IDX) ? base / static_cast<float>(layer + 1) : base;
+}
+
+// The c_fc epilogue: gelu_new, or the exact GELU with GPT2_GELU_EXACT.
+int mlp_epilogue(const gpt2_dims* d) { return (d->flags & GPT2_GELU_EXACT) ? GPT2_EPI_BIAS_GELU_EXACT : GPT2_EPI_BIAS_GELU; }
+
+cudaError_t attention(gpt2_dtype dt, const void* qkv, void* out, int B, int T, int H, float scale, cudaStream_t s) {
   // causal algorithmic work: q.k and p.v over the j <= i pairs only
   const double pairs = static_cast<double>(B) * H * T * (T + 1.0) / 2.0;
   const double D = 64.0 * H;
   ProfScope prof(dt == GPT2_BF16 ? "attn_causal_bf16_tc" : dt == GPT2_F16 ? "attn_causal_f16_tc" : "attn_causal_f32",
                  4.0 * 64.0 * pairs, static_cast<double>(B) * T * 4.0 * D * esize(dt), s);
-  if (is16(dt)) return launch_attention_tc(dt, qkv, out, B, T, H, s);
-  return launch_attention_f32(static_cast<const float*>(qkv), static_cast<float*>(out), B, T, H, s);
+  if (is16(dt)) return launch_attention_tc(dt, qkv, out, B, T, H, scale, s);
+  return launch_attention_f32(static_cast<const float*>(qkv), static_cast<float*>(out), B, T, H, scale, s);
 }
 
 cudaError_t layernorm(const void* x, const void* g, const void* b, void* y, int64_t rows, int D, float eps,
@@ -243,10 +256,11 @@ Acts carve_acts(void* ws, const gpt2_dims* d, int64_t M) {
   return a;
 }
 
-// The block body from `a = LN_1(x)` already computed; x -> x_out.  With
-// kv_layer (16-bit paths), the layer's K and V of all B T positions are
-// also written to cache slots 0..T-1 of a [2, B, n_head, T_max, 64] layer.
-int block_body(const gpt2_dims* d, const gpt2_block_weights* w, const float* x, float* x_out, int B, int T,
+// The body of block `layer` (counted from 0) from `a = LN_1(x)` already
+// computed; x -> x_out.  With kv_layer (16-bit paths), the layer's K and V of
+// all B T positions are also written to cache slots 0..T-1 of a
+// [2, B, n_head, T_max, 64] layer.
+int block_body(const gpt2_dims* d, const gpt2_block_weights* w, int layer, const float* x, float* x_out, int B, int T,
                const Acts& A, cudaStream_t s, void* kv_layer = nullptr, int T_max = 0) {
   const gpt2_dtype dt = d->dtype;
   const int64_t M = static_cast<int64_t>(B) * T;
@@ -256,10 +270,10 @@ int block_body(const gpt2_dims* d, const gpt2_block_weights* w, const float* x, 
     ProfScope prof("kv_from_qkv", 0.0, 2.0 * M * 2 * D * esize(dt), s);
     GPT2_CUDA(launch_kv_from_qkv(dt, A.qkv, kv_layer, B, T, H, T_max, s));
   }
-  GPT2_CUDA(attention(dt, A.qkv, A.o, B, T, H, s));
+  GPT2_CUDA(attention(dt, A.qkv, A.o, B, T, H, score_scale(d, layer), s));
   GPT2_CUDA(linear(dt, A.o, w->w_o, w->b_o, x, A.h, M, D, D, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32, s));
   GPT2_CUDA(layernorm(A.h, w->ln2_g, w->ln2_b, A.a, M, D, d->eps, GPT2_F32, dt, s));
-  GPT2_CUDA(linear(dt, A.a, w->w_fc, w->b_fc, nullptr, A.g, M, F, D, F, false, GPT2_EPI_BIAS_GELU, dt, s));
+  GPT2_CUDA(linear(dt, A.a, w->w_fc, w->b_fc, nullptr, A.g, M, F, D, F, false, mlp_epilogue(d), dt, s));
   GPT2_CUDA(linear(dt, A.g, w->w_proj, w->b_proj, A.h, x_out, M, D, F, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32, s));
   return GPT2_OK;
 }
@@ -347,7 +361,8 @@ struct DecodeGroup {
       // the cached lengths live on the device: the bytes of this kernel are
       // left to the caller, who knows them
       ProfScope prof("decode_attn", 0.0, 0.0, s);
-      if ((e = launch_decode_attention(dt, A.qkv, kv_layer, A.o, past_len, valid, nb, b0, B_cache, H, T_max, s)) !=
+      if ((e = launch_decode_attention(dt, A.qkv, kv_layer, A.o, past_len, valid, nb, b0, B_cache, H, T_max,
+                                       score_scale(d, l), s)) !=
           cudaSuccess)
         return e;
     }
@@ -355,7 +370,7 @@ struct DecodeGroup {
         cudaSuccess)
       return e;
     if ((e = layernorm(A.h, bw->ln2_g, bw->ln2_b, A.a, nb, D, d->eps, GPT2_F32, dt, s)) != cudaSuccess) return e;
-    if ((e = linear(dt, A.a, bw->w_fc, bw->b_fc, nullptr, A.g, nb, F, D, F, false, GPT2_EPI_BIAS_GELU, dt, s)) !=
+    if ((e = linear(dt, A.a, bw->w_fc, bw->b_fc, nullptr, A.g, nb, F, D, F, false, mlp_epilogue(d), dt, s)) !=
         cudaSuccess)
       return e;
     return linear(dt, A.g, bw->w_proj, bw->b_proj, A.h, A.x, nb, D, F, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32, s);
@@ -411,7 +426,7 @@ int forward_to_lnf(const gpt2_dims* dims, const gpt2_model_weights* w, const int
     if (kv_cache)
       kv_layer = static_cast<char*>(kv_cache) +
                  static_cast<size_t>(l) * 2 * B * dims->n_head * static_cast<size_t>(T_max) * 64 * esize(dt);
-    GPT2_TRY(block_body(dims, bw, A.x, A.x, B, T, A, s, kv_layer, T_max));
+    GPT2_TRY(block_body(dims, bw, l, A.x, A.x, B, T, A, s, kv_layer, T_max));
   }
   if (lnf) GPT2_CUDA(layernorm(A.x, w->lnf_g, w->lnf_b, A.a, M, D, dims->eps, GPT2_F32, dt, s));
   return GPT2_OK;
@@ -490,7 +505,7 @@ int gpt2_linear(const void* x, const void* w, const void* bias, const float* res
                 gpt2_dtype y_t, gpt2_stream_t stream) {
   if (!valid_dtype(dtype) || !valid_dtype(y_t)) return GPT2_ERR_ARG;
   if (w_layout != GPT2_W_IN_OUT && w_layout != GPT2_W_OUT_IN) return GPT2_ERR_ARG;
-  if (epilogue < GPT2_EPI_NONE || epilogue > GPT2_EPI_BIAS_RESIDUAL) return GPT2_ERR_ARG;
+  if (epilogue < GPT2_EPI_NONE || epilogue > GPT2_EPI_BIAS_GELU_EXACT) return GPT2_ERR_ARG;
   if (M < 0 || M > INT_MAX || N <= 0 || K <= 0 || ldy < N) return GPT2_ERR_ARG;
   if (K % 64 != 0) return GPT2_ERR_UNSUPPORTED;
   if (epilogue == GPT2_EPI_BIAS_RESIDUAL && y_t != GPT2_F32) return GPT2_ERR_UNSUPPORTED;
@@ -510,13 +525,19 @@ int gpt2_linear(const void* x, const void* w, const void* bias, const float* res
 
 int gpt2_attention_causal(const void* qkv, void* out, int B, int T, int n_head, int head_dim, gpt2_dtype dtype,
                           gpt2_stream_t stream) {
+  return gpt2_attention_causal_scaled(qkv, out, B, T, n_head, head_dim, 0.125f, dtype, stream);
+}
+
+int gpt2_attention_causal_scaled(const void* qkv, void* out, int B, int T, int n_head, int head_dim,
+                                 float score_scale, gpt2_dtype dtype, gpt2_stream_t stream) {
   if (!valid_dtype(dtype) || B < 0 || T < 0 || n_head <= 0 || head_dim <= 0) return GPT2_ERR_ARG;
+  if (!(score_scale > 0.f) || !std::isfinite(score_scale)) return GPT2_ERR_ARG;
   if (head_dim != 64) return GPT2_ERR_UNSUPPORTED;
   if (dtype == GPT2_F32 && T > 8192) return GPT2_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(B) * n_head > INT_MAX || T > 65535 * 64) return GPT2_ERR_UNSUPPORTED;
   if (B == 0 || T == 0) return GPT2_OK;
   if (!qkv || !out || !aligned16(qkv) || !aligned16(out)) return GPT2_ERR_ARG;
-  return cuda_status(attention(dtype, qkv, out, B, T, n_head, cs(stream)));
+  return cuda_status(attention(dtype, qkv, out, B, T, n_head, score_scale, cs(stream)));
 }
 
 size_t gpt2_mlp_workspace_bytes(int64_t M, int F, gpt2_dtype dtype) {
@@ -552,7 +573,13 @@ size_t gpt2_workspace_bytes(const gpt2_dims* dims, int B, int T) {
 
 int gpt2_block_forward(const gpt2_dims* dims, const gpt2_block_weights* w, const float* x_in, float* x_out, int B,
                        int T, void* ws, size_t ws_bytes, gpt2_stream_t stream) {
+  return gpt2_block_forward_layer(dims, w, 0, x_in, x_out, B, T, ws, ws_bytes, stream);
+}
+
+int gpt2_block_forward_layer(const gpt2_dims* dims, const gpt2_block_weights* w, int layer, const float* x_in,
+                             float* x_out, int B, int T, void* ws, size_t ws_bytes, gpt2_stream_t stream) {
   GPT2_TRY(check_dims(dims, false));
+  if (layer < 0) return GPT2_ERR_ARG;
   GPT2_TRY(check_block_ptrs(w));
   if (B < 0 || T < 0 || static_cast<int64_t>(B) * T > INT_MAX) return GPT2_ERR_ARG;
   if (B == 0 || T == 0) return GPT2_OK;
@@ -563,7 +590,7 @@ int gpt2_block_forward(const gpt2_dims* dims, const gpt2_block_weights* w, const
   Acts A = carve_acts(ws, dims, M);
   cudaStream_t s = cs(stream);
   GPT2_CUDA(layernorm(x_in, w->ln1_g, w->ln1_b, A.a, M, dims->d_model, dims->eps, GPT2_F32, dims->dtype, s));
-  return block_body(dims, w, x_in, x_out, B, T, A, s);
+  return block_body(dims, w, layer, x_in, x_out, B, T, A, s);
 }
 
 int gpt2_forward_logits(const gpt2_dims* dims, const gpt2_model_weights* w, const int32_t* tokens, void* logits,

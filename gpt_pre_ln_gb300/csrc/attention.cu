@@ -22,7 +22,8 @@ constexpr int kHd = 64;
 constexpr int kF32Warps = 4;
 
 __global__ void __launch_bounds__(kF32Warps * 32) attn_causal_f32(const float* __restrict__ qkv,
-                                                                  float* __restrict__ out, int T, int H) {
+                                                                  float* __restrict__ out, int T, int H,
+                                                                  float score_scale) {
   extern __shared__ float sc[];  // kF32Warps x T scores
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -45,7 +46,7 @@ __global__ void __launch_bounds__(kF32Warps * 32) attn_causal_f32(const float* _
     float acc = 0.f;
 #pragma unroll 16
     for (int d = 0; d < kHd; ++d) acc = fmaf(q[d], k[d], acc);
-    acc *= 0.125f;
+    acc *= score_scale;
     s[j] = acc;
     mx = fmaxf(mx, acc);
   }
@@ -74,7 +75,8 @@ __global__ void __launch_bounds__(kF32Warps * 32) attn_causal_f32(const float* _
 
 }  // namespace
 
-cudaError_t launch_attention_f32(const float* qkv, float* out, int B, int T, int n_head, cudaStream_t stream) {
+cudaError_t launch_attention_f32(const float* qkv, float* out, int B, int T, int n_head, float score_scale,
+                                 cudaStream_t stream) {
   if (B == 0 || T == 0) return cudaSuccess;
   const long long rows = static_cast<long long>(n_head) * T;
   dim3 grid(static_cast<unsigned>((rows + kF32Warps - 1) / kF32Warps), B);
@@ -84,7 +86,7 @@ cudaError_t launch_attention_f32(const float* qkv, float* out, int B, int T, int
         cudaFuncSetAttribute(attn_causal_f32, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  attn_causal_f32<<<grid, kF32Warps * 32, smem, stream>>>(qkv, out, T, n_head);
+  attn_causal_f32<<<grid, kF32Warps * 32, smem, stream>>>(qkv, out, T, n_head, score_scale);
   return cudaGetLastError();
 }
 

@@ -75,7 +75,7 @@ __device__ __forceinline__ int attn_item(int k, int c, int G) {
 template <typename T16>
 __global__ void __launch_bounds__(kAttnThreads, 2)
     attn_causal_tc(const __grid_constant__ CUtensorMap tm_qkv, T16* __restrict__ out, int B, int T, int H,
-                   unsigned* err) {
+                   float scale_log2, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ0 = smem_u32(smem);        // Q slots 0, 1 (items)
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     const uint32_t tS = tmem + lane_off;
     const uint32_t tO = tmem + lane_off + kOCol;
     const uint32_t tP = tmem + lane_off + kPCol;
-    const float scale = 1.4426950408889634f * 0.125f;  // log2(e) / sqrt(64)
+    const float scale = scale_log2;  // log2(e) times the score scale (1/sqrt(64) for GPT-2)
     bool ok = true;
     long long g = 0;
     for (int k = 0; ok; ++k) {
@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 }
 
 template <typename T16>
-cudaError_t launch_t(const void* qkv, void* out, int B, int T, int n_head, cudaStream_t stream) {
+cudaError_t launch_t(const void* qkv, void* out, int B, int T, int n_head, float score_scale, cudaStream_t stream) {
   if (B == 0 || T == 0) return cudaSuccess;
   const uint64_t D = static_cast<uint64_t>(n_head) * kHd;
   CUtensorMap map;
@@ -489,15 +489,15 @@ cudaError_t launch_t(const void* qkv, void* out, int B, int T, int n_head, cudaS
   const long long resident = 2ll * num_sms();
   const int grid = static_cast<int>(items < resident ? items : resident);
   return launch_pdl(attn_causal_tc<T16>, dim3(grid), kAttnThreads, kSmemBytes, stream, 0, map,
-                    static_cast<T16*>(out), B, T, n_head, device_error_word());
+                    static_cast<T16*>(out), B, T, n_head, 1.4426950408889634f * score_scale, device_error_word());
 }
 
 }  // namespace
 
-cudaError_t launch_attention_tc(gpt2_dtype dt, const void* qkv, void* out, int B, int T, int n_head,
+cudaError_t launch_attention_tc(gpt2_dtype dt, const void* qkv, void* out, int B, int T, int n_head, float score_scale,
                                 cudaStream_t stream) {
-  if (dt == GPT2_F16) return launch_t<__half>(qkv, out, B, T, n_head, stream);
-  return launch_t<__nv_bfloat16>(qkv, out, B, T, n_head, stream);
+  if (dt == GPT2_F16) return launch_t<__half>(qkv, out, B, T, n_head, score_scale, stream);
+  return launch_t<__nv_bfloat16>(qkv, out, B, T, n_head, score_scale, stream);
 }
 
 }  // namespace gpt2

@@ -112,6 +112,35 @@ __device__ __forceinline__ float gelu_new_fast(float x) {
   return fmaf(hx, tanh_hw(u), hx);
 }
 
+// GELU itself, x Phi(x) = 0.5 x (1 + erf(x / sqrt(2))) (llm.c notes 4.2: the
+// tanh form above approximates it); chosen per model by a GPT2Config switch.
+__device__ __forceinline__ float gelu_exact(float x) {
+  const float k1 = 0.7071067811865476f;  // 1 / sqrt(2)
+  return 0.5f * x * (1.0f + erff(k1 * x));
+}
+
+// The activation of the MLP's c_fc epilogue: the exact GELU when `exact`,
+// else gelu_new (hardware tanh where the result is rounded to 16 bits).
+template <bool OUT16>
+__device__ __forceinline__ float mlp_act(float x, bool exact) {
+  if (exact) return gelu_exact(x);
+  return OUT16 ? gelu_new_fast(x) : gelu_new_accurate(x);
+}
+
+// The same over a chunk of N values, with one branch for the whole chunk
+// (`exact` is uniform across the warp) so that the default path keeps its
+// straight-line code.
+template <bool OUT16, int N>
+__device__ __forceinline__ void mlp_act_chunk(float (&v)[N], bool exact) {
+  if (exact) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = gelu_exact(v[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = OUT16 ? gelu_new_fast(v[i]) : gelu_new_accurate(v[i]);
+  }
+}
+
 // Two fp32 FMAs in one instruction (sm_100 family): d = a * b + c for each
 // half of the pair, rounded to nearest: the same results as two fmaf calls.
 __device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {

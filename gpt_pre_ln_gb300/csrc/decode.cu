@@ -94,7 +94,7 @@ template <typename T16>
 __global__ void __launch_bounds__(kDaWarps * 32, 6)
     decode_attn_tma(const __grid_constant__ CUtensorMap kv_map, const T16* __restrict__ qkv, T16* kv_layer,
                     T16* __restrict__ out, const int32_t* __restrict__ past_len, const int* __restrict__ valid,
-                    int b_cache0, int B_cache, int H, int T_max, unsigned* err) {
+                    int b_cache0, int B_cache, int H, int T_max, float q_scale, unsigned* err) {
   extern __shared__ uint8_t da_smem_raw[];
   __shared__ __align__(8) uint64_t bars[kDaWarps][kDaStages];
   __shared__ float s_q[kHd];
@@ -141,8 +141,8 @@ __global__ void __launch_bounds__(kDaWarps * 32, 6)
     return;
   }
   const T16* row = qkv + static_cast<long long>(b) * 3 * D;
-  constexpr float kQScale = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) * log2(e)
-  if (tid < kHd) s_q[tid] = to_f32<T16>(row[h * kHd + tid]) * kQScale;
+  // q_scale = the score scale (1/sqrt(64) for GPT-2) times log2(e)
+  if (tid < kHd) s_q[tid] = to_f32<T16>(row[h * kHd + tid]) * q_scale;
   __syncthreads();
 
   const int key = lane >> 1;  // score phase: key of the chunk
@@ -425,7 +425,8 @@ cudaError_t launch_decode_embed_ln(gpt2_dtype dt, const int32_t* tokens, const i
 namespace {
 template <typename T16>
 cudaError_t launch_decode_attn_t(const void* qkv, void* kv_layer, void* out, const int32_t* past_len, const int* valid,
-                                 int B, int b_cache0, int B_cache, int n_head, int T_max, cudaStream_t stream) {
+                                 int B, int b_cache0, int B_cache, int n_head, int T_max, float score_scale,
+                                 cudaStream_t stream) {
   // the layer's K and V halves as one [2 * B_cache * n_head * T_max, 64] matrix
   const uint64_t rows = 2ull * B_cache * n_head * static_cast<uint64_t>(T_max);
   if (rows >= (1ull << 31)) return cudaErrorInvalidValue;
@@ -434,18 +435,18 @@ cudaError_t launch_decode_attn_t(const void* qkv, void* kv_layer, void* out, con
     return cudaErrorInvalidValue;
   return launch_pdl(decode_attn_tma<T16>, B * n_head, kDaWarps * 32, kDaSmem, stream, 0, map,
                     static_cast<const T16*>(qkv), static_cast<T16*>(kv_layer), static_cast<T16*>(out), past_len,
-                    valid, b_cache0, B_cache, n_head, T_max, device_error_word());
+                    valid, b_cache0, B_cache, n_head, T_max, score_scale * 1.4426950408889634f, device_error_word());
 }
 }  // namespace
 
 cudaError_t launch_decode_attention(gpt2_dtype dt, const void* qkv, void* kv_layer, void* out, const int32_t* past_len,
                                     const int* valid, int B, int b_cache0, int B_cache, int n_head, int T_max,
-                                    cudaStream_t stream) {
+                                    float score_scale, cudaStream_t stream) {
   if (dt == GPT2_F16)
     return launch_decode_attn_t<__half>(qkv, kv_layer, out, past_len, valid, B, b_cache0, B_cache, n_head, T_max,
-                                        stream);
+                                        score_scale, stream);
   return launch_decode_attn_t<__nv_bfloat16>(qkv, kv_layer, out, past_len, valid, B, b_cache0, B_cache, n_head,
-                                             T_max, stream);
+                                             T_max, score_scale, stream);
 }
 
 cudaError_t launch_argmax_candidates(const float2* cand, int n_cand, int B, const int* valid, int32_t* next_tokens,

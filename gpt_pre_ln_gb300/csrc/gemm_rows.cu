@@ -85,6 +85,8 @@ struct RowsArgs {
   // largest output value of the warp's 32 features and its lowest index, at
   // cand[m * 4 * n_tiles + q] (value, index bits)
   float2* cand;
+  // R_GELU: the exact GELU x Phi(x) in place of gelu_new
+  int gelu_exact;
 };
 
 // Argmax over the lanes of a warp for 32 rows at once: v[j], i[j] are this
@@ -122,7 +124,7 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 template <int EPI, typename OutT, typename T16>
 __device__ __forceinline__ void rows_store(const RowsArgs<OutT, T16>& a, int m, int n, float v, float b, float r) {
   if constexpr (EPI != R_NONE) v += b;
-  if constexpr (EPI == R_GELU) v = (sizeof(OutT) == 2) ? gelu_new_fast(v) : gelu_new_accurate(v);
+  if constexpr (EPI == R_GELU) v = mlp_act<sizeof(OutT) == 2>(v, a.gelu_exact != 0);
   if constexpr (EPI == R_RES) v += r;
   a.out[static_cast<long long>(m) * a.ldo + n] = from_f32<OutT>(v);
 }
@@ -532,6 +534,7 @@ cudaError_t rows_dispatch_epi(const T16* x, const T16* w, const T16* bias, const
   }
   if (y_t != GPT2_F32) {
     RowsArgs<T16, T16> ea{bias, residual, static_cast<T16*>(y), ldy, M, N, K, err, nullptr};
+    ea.gelu_exact = epi == GPT2_EPI_BIAS_GELU_EXACT;
     switch (epi) {
       case R_NONE: return run_rows<MP, W_MN, R_NONE, T16, T16>(x, w, ea, s);
       case R_BIAS: return run_rows<MP, W_MN, R_BIAS, T16, T16>(x, w, ea, s);
@@ -539,6 +542,7 @@ cudaError_t rows_dispatch_epi(const T16* x, const T16* w, const T16* bias, const
     }
   }
   RowsArgs<float, T16> ea{bias, residual, static_cast<float*>(y), ldy, M, N, K, err, nullptr};
+  ea.gelu_exact = epi == GPT2_EPI_BIAS_GELU_EXACT;
   switch (epi) {
     case R_NONE: return run_rows<MP, W_MN, R_NONE, float, T16>(x, w, ea, s);
     case R_BIAS: return run_rows<MP, W_MN, R_BIAS, float, T16>(x, w, ea, s);

@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(256) gemm_f32_simt(const float* __restrict__ x
       float v = acc[i][j];
       if (EPI != 0) v += bias[col];
       if (EPI == 2) v = gelu_new_accurate(v);
+      if (EPI == 4) v = gelu_exact(v);
       if (EPI == 3) v += residual[static_cast<long long>(row) * N + col];
       y[static_cast<long long>(row) * ldy + col] = v;
     }
@@ -94,6 +95,7 @@ cudaError_t dispatch(const float* x, const float* w, const float* bias, const fl
     case 0: gemm_f32_simt<W_OUT_IN, 0><<<grid, 256, 0, s>>>(x, w, bias, residual, y, M, N, K, ldy); break;
     case 1: gemm_f32_simt<W_OUT_IN, 1><<<grid, 256, 0, s>>>(x, w, bias, residual, y, M, N, K, ldy); break;
     case 2: gemm_f32_simt<W_OUT_IN, 2><<<grid, 256, 0, s>>>(x, w, bias, residual, y, M, N, K, ldy); break;
+    case 4: gemm_f32_simt<W_OUT_IN, 4><<<grid, 256, 0, s>>>(x, w, bias, residual, y, M, N, K, ldy); break;
     default: gemm_f32_simt<W_OUT_IN, 3><<<grid, 256, 0, s>>>(x, w, bias, residual, y, M, N, K, ldy); break;
   }
   return cudaGetLastError();

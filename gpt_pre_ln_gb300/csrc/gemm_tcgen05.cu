@@ -4,7 +4,8 @@
 //
 //   y[M, N] = epilogue( x[M, K] . W )      W = [K, N] ("in, out", Conv1D)
 //                                          or  [N, K] (wte as the lm_head)
-//   epilogues: none | + bias | gelu_new(+ bias) | + bias + residual (fp32)
+//   epilogues: none | + bias | gelu_new or exact GELU (+ bias) | + bias +
+//   residual (fp32)
 //              | log-sum-exp partials (the lm_head of the loss: no output)
 //
 // Two persistent kernels share one design (10 warps per CTA):
@@ -16,7 +17,7 @@
 //   warps 2-9   epilogue in two halves of four warps (one thread per
 //               accumulator row in each half); half h owns the column chunks
 //               h, h+2, ... (128 bytes of output per row each): tcgen05.ld,
-//               bias / gelu_new / residual in fp32, then each warp writes its
+//               bias / GELU / residual in fp32, then each warp writes its
 //               32 rows into a private swizzled staging area and reads them
 //               back transposed, so that every global store instruction
 //               covers four full 128-byte lines.  The fp32 residual is read
@@ -98,7 +99,7 @@ struct OutTraits {
 
 template <int EPI, typename OutT, typename T16>
 __device__ __forceinline__ void apply_bias_act(float (&v)[OutTraits<OutT>::CW], const T16* __restrict__ bias,
-                                               int col0, int N) {
+                                               int col0, int N, bool gelu_exact_on = false) {
   constexpr int CW = OutTraits<OutT>::CW;
   if constexpr (EPI != EPI_NONE) {
     // all 16-byte bias loads first (independent, so their latencies
@@ -133,17 +134,16 @@ __device__ __forceinline__ void apply_bias_act(float (&v)[OutTraits<OutT>::CW], 
     }
   }
   // 16-bit outputs: one hardware tanh per element (absolute error below
-  // 2^-11, under the rounding that follows); fp32 outputs: tanhf
-  if constexpr (EPI == EPI_GELU) {
-#pragma unroll
-    for (int i = 0; i < CW; ++i) v[i] = (sizeof(OutT) == 2) ? gelu_new_fast(v[i]) : gelu_new_accurate(v[i]);
-  }
+  // 2^-11, under the rounding that follows); fp32 outputs: tanhf; the exact
+  // GELU (a warp-uniform switch) with erff
+  if constexpr (EPI == EPI_GELU) mlp_act_chunk<sizeof(OutT) == 2>(v, gelu_exact_on);
 }
 
 // The same with the bias of the chunk read from shared memory (16-bit, zero
 // beyond column N), where the epilogue stages each tile's bias once.
 template <int EPI, typename OutT, typename T16>
-__device__ __forceinline__ void apply_bias_act_smem(float (&v)[OutTraits<OutT>::CW], uint32_t bias_addr) {
+__device__ __forceinline__ void apply_bias_act_smem(float (&v)[OutTraits<OutT>::CW], uint32_t bias_addr,
+                                                    bool gelu_exact_on) {
   constexpr int CW = OutTraits<OutT>::CW;
   uint4 raw[CW / 8];
 #pragma unroll
@@ -161,10 +161,7 @@ __device__ __forceinline__ void apply_bias_act_smem(float (&v)[OutTraits<OutT>::
       v[q * 8 + 2 * e + 1] += f.y;
     }
   }
-  if constexpr (EPI == EPI_GELU) {
-#pragma unroll
-    for (int i = 0; i < CW; ++i) v[i] = (sizeof(OutT) == 2) ? gelu_new_fast(v[i]) : gelu_new_accurate(v[i]);
-  }
+  if constexpr (EPI == EPI_GELU) mlp_act_chunk<sizeof(OutT) == 2>(v, gelu_exact_on);
 }
 
 template <typename OutT, typename T16>
@@ -182,6 +179,8 @@ struct EpiArgs {
   int T;
   float2* part;
   float* tgt;
+  // EPI_GELU: the exact GELU x Phi(x) in place of gelu_new
+  int gelu_exact;
 };
 
 // EPI_LSE: one 32-column chunk of a row's logits into the running (m, s) of
@@ -427,7 +426,7 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
         continue;
       }
       if constexpr (kBiasSmem)
-        apply_bias_act_smem<EPI, OutT, T16>(v, bias_b + static_cast<uint32_t>(c * CW * 2));
+        apply_bias_act_smem<EPI, OutT, T16>(v, bias_b + static_cast<uint32_t>(c * CW * 2), a.gelu_exact != 0);
       else if constexpr (EPI == EPI_NONE)
         apply_bias_act<EPI, OutT, T16>(v, a.bias, col0, N);
       // this lane's row (128 bytes) into the staging area (the 128-byte
@@ -1050,6 +1049,7 @@ cudaError_t dispatch(int v, const T16* x, const T16* w, const T16* bias, const f
   }
   if (y_t != GPT2_F32) {
     EpiArgs<T16, T16> ea{bias, residual, static_cast<T16*>(y), ldy, M, N, err};
+    ea.gelu_exact = epi == GPT2_EPI_BIAS_GELU_EXACT;
     switch (epi) {
       case EPI_NONE: return run_variant<B_MN, EPI_NONE, T16, T16>(v, x, w, ea, K, s);
       case EPI_BIAS: return run_variant<B_MN, EPI_BIAS, T16, T16>(v, x, w, ea, K, s);
@@ -1057,6 +1057,7 @@ cudaError_t dispatch(int v, const T16* x, const T16* w, const T16* bias, const f
     }
   }
   EpiArgs<float, T16> ea{bias, residual, static_cast<float*>(y), ldy, M, N, err};
+  ea.gelu_exact = epi == GPT2_EPI_BIAS_GELU_EXACT;
   switch (epi) {
     case EPI_NONE: return run_variant<B_MN, EPI_NONE, float, T16>(v, x, w, ea, K, s);
     case EPI_BIAS: return run_variant<B_MN, EPI_BIAS, float, T16>(v, x, w, ea, K, s);

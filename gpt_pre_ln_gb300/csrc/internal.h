@@ -92,9 +92,11 @@ cudaError_t launch_gemm_f32(const float* x, const float* w, const float* bias, c
 
 // tcgen05 version (S and O in tensor memory), head_dim 64; dt GPT2_BF16 or
 // GPT2_F16.
-cudaError_t launch_attention_tc(gpt2_dtype dt, const void* qkv, void* out, int B, int T, int n_head,
+// Scores are q.k times score_scale (1/sqrt(64) for GPT-2).
+cudaError_t launch_attention_tc(gpt2_dtype dt, const void* qkv, void* out, int B, int T, int n_head, float score_scale,
                                 cudaStream_t stream);
-cudaError_t launch_attention_f32(const float* qkv, float* out, int B, int T, int n_head, cudaStream_t stream);
+cudaError_t launch_attention_f32(const float* qkv, float* out, int B, int T, int n_head, float score_scale,
+                                 cudaStream_t stream);
 
 // Decode-step kernels (16-bit paths; dt GPT2_BF16 or GPT2_F16).
 cudaError_t launch_decode_embed_ln(gpt2_dtype dt, const int32_t* tokens, const int32_t* past_len, const void* wte,
@@ -104,7 +106,7 @@ cudaError_t launch_decode_embed_ln(gpt2_dtype dt, const int32_t* tokens, const i
 // b_cache0 + B - 1 of a cache laid out for B_cache sequences.
 cudaError_t launch_decode_attention(gpt2_dtype dt, const void* qkv, void* kv_layer, void* out, const int32_t* past_len,
                                     const int* valid, int B, int b_cache0, int B_cache, int n_head, int T_max,
-                                    cudaStream_t stream);
+                                    float score_scale, cudaStream_t stream);
 // Prefill: K and V of rows b T + t of qkv [B T, 3D] into cache slots t of
 // sequences b (layer layout [2, B, n_head, T_max, 64]).
 cudaError_t launch_kv_from_qkv(gpt2_dtype dt, const void* qkv, void* kv_layer, int B, int T, int n_head, int T_max,

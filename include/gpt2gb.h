@@ -69,9 +69,21 @@ typedef enum {
 
 typedef enum { GPT2_F32 = 0, GPT2_BF16 = 1, GPT2_F16 = 2 } gpt2_dtype;
 
+/* Switches of GPT2Config ("逐行拆GPT-2源码", GPT2Config section), OR-ed
+ * into gpt2_dims.flags; 0 is GPT-2 as released.
+ *   GPT2_SCALE_ATTN_BY_INVERSE_LAYER_IDX: the attention scores of layer l
+ *     (counted from 0) are divided by l + 1 on top of the 1/sqrt(64) scale
+ *     (scale_attn_by_inverse_layer_idx).
+ *   GPT2_GELU_EXACT: the MLP uses GELU itself, x Phi(x) =
+ *     0.5 x (1 + erf(x / sqrt(2))) (llm.c notes 4.2), in place of its tanh
+ *     approximation gelu_new. */
+enum { GPT2_SCALE_ATTN_BY_INVERSE_LAYER_IDX = 1, GPT2_GELU_EXACT = 2 };
+
 /* Model hyper-parameters (GPT2Config on "逐行拆GPT-2源码": n_layer, n_embd,
- * n_head, n_inner = 4 * n_embd by default, vocab_size, n_positions,
- * layer_norm_epsilon).  `dtype` selects the number path described above. */
+ * n_head, n_inner = d_ff (4 * n_embd by default; any multiple of 64 runs),
+ * vocab_size, n_positions, layer_norm_epsilon).  `dtype` selects the number
+ * path described above; `flags` holds the switches above (an unknown bit is
+ * GPT2_ERR_ARG).  Zero-initialise the struct so that flags start at 0. */
 typedef struct {
   int n_layer;
   int d_model;
@@ -81,6 +93,7 @@ typedef struct {
   int n_pos;
   float eps;
   gpt2_dtype dtype;
+  unsigned flags;
 } gpt2_dims;
 
 /* One block's 12 tensors (6 groups of weight + bias, the safetensors key
@@ -108,10 +121,11 @@ typedef struct {
 
 /* Epilogues of gpt2_linear. */
 typedef enum {
-  GPT2_EPI_NONE = 0,          /* y = x W                        */
-  GPT2_EPI_BIAS = 1,          /* y = x W + b                    */
-  GPT2_EPI_BIAS_GELU = 2,     /* y = gelu_new(x W + b)          */
-  GPT2_EPI_BIAS_RESIDUAL = 3  /* y = r + x W + b  (y, r fp32)   */
+  GPT2_EPI_NONE = 0,            /* y = x W                               */
+  GPT2_EPI_BIAS = 1,            /* y = x W + b                           */
+  GPT2_EPI_BIAS_GELU = 2,       /* y = gelu_new(x W + b)                 */
+  GPT2_EPI_BIAS_RESIDUAL = 3,   /* y = r + x W + b  (y, r fp32)          */
+  GPT2_EPI_BIAS_GELU_EXACT = 4  /* y = gelu(x W + b), gelu(u) = u Phi(u) */
 } gpt2_epilogue;
 
 /* Orientation of the weight of gpt2_linear. */
@@ -171,6 +185,13 @@ int gpt2_linear(const void *x, const void *w, const void *bias, const float *res
 int gpt2_attention_causal(const void *qkv, void *out, int B, int T, int n_head, int head_dim, gpt2_dtype dtype,
                           gpt2_stream_t stream);
 
+/* gpt2_attention_causal with the scores q_i . k_j multiplied by
+ * `score_scale` instead of 1/8 (with GPT2Config's
+ * scale_attn_by_inverse_layer_idx, layer l uses 1 / (8 (l + 1))).
+ * score_scale must be finite and > 0, else GPT2_ERR_ARG. */
+int gpt2_attention_causal_scaled(const void *qkv, void *out, int B, int T, int n_head, int head_dim,
+                                 float score_scale, gpt2_dtype dtype, gpt2_stream_t stream);
+
 /* Workspace needed by gpt2_mlp for M rows (the [M, F] hidden activation). */
 size_t gpt2_mlp_workspace_bytes(int64_t M, int F, gpt2_dtype dtype);
 
@@ -216,9 +237,17 @@ size_t gpt2_workspace_bytes(const gpt2_dims *dims, int B, int T);
  *   H = X + c_proj(attn(c_attn(LN_1(X)))); X' = H + mlp(LN_2(H)).
  *   x_in, x_out: fp32 [B, T, D] residual stream (x_out may equal x_in);
  *   weights of type dims->dtype; ws of gpt2_workspace_bytes(dims, B, T)
- *   bytes.  dims->n_layer, vocab and n_pos are not used. */
+ *   bytes.  dims->n_layer, vocab and n_pos are not used.  The block is
+ *   taken as layer 0 (this matters only with
+ *   GPT2_SCALE_ATTN_BY_INVERSE_LAYER_IDX). */
 int gpt2_block_forward(const gpt2_dims *dims, const gpt2_block_weights *w, const float *x_in, float *x_out, int B,
                        int T, void *ws, size_t ws_bytes, gpt2_stream_t stream);
+
+/* gpt2_block_forward for the block at index `layer` >= 0 of the stack
+ * (counted from 0): with GPT2_SCALE_ATTN_BY_INVERSE_LAYER_IDX its attention
+ * scores are divided by layer + 1. */
+int gpt2_block_forward_layer(const gpt2_dims *dims, const gpt2_block_weights *w, int layer, const float *x_in,
+                             float *x_out, int B, int T, void *ws, size_t ws_bytes, gpt2_stream_t stream);
 
 /* Whole forward to logits ("逐行拆GPT-2源码", GPT2Model + GPT2LMHeadModel;
  * "Transformer Stack" page, GPT.forward):

@@ -51,16 +51,19 @@ def test_header_constants_match_binding():
     assert consts["GPT2_EPI_BIAS_GELU"] == G.EPI_BIAS_GELU and consts["GPT2_EPI_BIAS_RESIDUAL"] == G.EPI_BIAS_RESIDUAL
     assert consts["GPT2_W_OUT_IN"] == G.W_OUT_IN
     assert consts["GPT2_ERR_TIMEOUT"] == 5 and consts["GPT2_ERR_RANGE"] == 6
+    assert consts["GPT2_EPI_BIAS_GELU_EXACT"] == G.EPI_BIAS_GELU_EXACT
+    assert consts["GPT2_SCALE_ATTN_BY_INVERSE_LAYER_IDX"] == G.SCALE_ATTN_BY_INVERSE_LAYER_IDX
+    assert consts["GPT2_GELU_EXACT"] == G.GELU_EXACT
 
 
 def test_struct_layout_matches_header(L):
-    assert ctypes.sizeof(G.Dims) == 8 * 4
+    assert ctypes.sizeof(G.Dims) == 9 * 4
     assert ctypes.sizeof(G.BlockWeights) == 12 * 8
     assert ctypes.sizeof(G.ModelWeights) == 5 * 8
 
 
 def test_status_strings(L):
-    assert G.gpt2_abi_version() == 2
+    assert G.gpt2_abi_version() == 3
     assert G.gpt2_status_string(0) == "ok"
     assert "workspace" in G.gpt2_status_string(3)
 
@@ -95,9 +98,21 @@ def test_argument_checks_before_any_launch(L):
     assert L.gpt2_linear(16, 16, 16, 16, 16, 10, 1002, 768, 1004, 1, 3, 1, 0, None) == 2  # residual needs N % 4
     assert L.gpt2_attention_causal(16, 16, 2, 64, 12, 32, 1, None) == 2                  # head_dim != 64
     assert L.gpt2_attention_causal(16, 16, 0, 64, 12, 64, 1, None) == 0                  # B = 0
+    assert L.gpt2_attention_causal_scaled(16, 16, 2, 64, 12, 64, 0.0, 1, None) == 1      # scale <= 0
+    assert L.gpt2_attention_causal_scaled(16, 16, 2, 64, 12, 64, float("inf"), 1, None) == 1
+    assert L.gpt2_attention_causal_scaled(16, 16, 0, 64, 12, 64, 0.0625, 1, None) == 0   # B = 0
+    assert L.gpt2_linear(16, 16, 16, None, 16, 10, 768, 768, 768, 0, 5, 1, 1, None) == 1  # unknown epilogue
     d = G.make_dims(2, 768, 12, 3072, 50257, 1024)
     blk = G.BlockWeights(*([256] * 12))
     assert L.gpt2_block_forward(ctypes.byref(d), ctypes.byref(blk), 256, 256, 2, 64, 256, 10, None) == 3  # ws small
+    assert L.gpt2_block_forward_layer(ctypes.byref(d), ctypes.byref(blk), -1, 256, 256, 2, 64, 256, 1 << 30,
+                                      None) == 1  # layer < 0
+    d_bad = G.make_dims(2, 768, 12, 3072, 50257, 1024, flags=4)
+    assert L.gpt2_block_forward(ctypes.byref(d_bad), ctypes.byref(blk), 256, 256, 2, 64, 256, 1 << 30,
+                                None) == 1  # unknown switch bit
+    d_sw = G.make_dims(2, 768, 12, 2048, 50257, 1024, flags=G.SCALE_ATTN_BY_INVERSE_LAYER_IDX | G.GELU_EXACT)
+    assert G.gpt2_workspace_bytes(d_sw, 8, 1024) == 2 * 8192 * 768 * 4 + 2 * 8192 * 768 * 2 + 8192 * 3 * 768 * 2 + \
+        8192 * 2048 * 2  # n_inner = 2048
     blk0 = G.BlockWeights(*([256] * 11 + [0]))
     assert L.gpt2_block_forward(ctypes.byref(d), ctypes.byref(blk0), 256, 256, 2, 64, 256, 1 << 30, None) == 1
     blocks = (G.BlockWeights * 2)(blk, blk)
