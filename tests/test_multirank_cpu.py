@@ -1,0 +1,69 @@
+"""The multi-process (torchrun) path of bench.py, on CPU with gloo ranks.
+
+The forward has no exchange step: each rank runs an independent replica,
+and the job's number is the tokens of all ranks over the slowest rank's
+time.  These tests run that host logic in two gloo processes (no GPU), and
+check that under the reference arm only rank 0 works and prints.
+"""
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        ms = bench._max_over_ranks(10.0 + 5.0 * rank, world, "cpu")  # rank 1 is the slow one
+        value = bench._job_tokens_per_s(8 * 1024, world, ms)
+        q.put((rank, ms, value))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_value_two_gloo_ranks():
+    torch = pytest.importorskip("torch")
+    mp = torch.multiprocessing.get_context("spawn")
+    q = mp.Queue()
+    port = _free_port()
+    procs = [mp.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    # both ranks see the slowest rank's time, and the job value counts the
+    # tokens of both replicas over it
+    assert [r[1] for r in res] == [15.0, 15.0]
+    assert all(abs(r[2] - 2 * 8 * 1024 / 0.015) < 1e-6 * r[2] for r in res)
+
+
+def test_single_process_needs_no_process_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench._max_over_ranks(3.5, 1, "cpu") == 3.5
+    assert bench._job_tokens_per_s(8192, 1, 2.0) == 8192 / 0.002
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    """Under torchrun the reference arm's other ranks exit 0 without work
+    or output."""
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1", MASTER_ADDR="127.0.0.1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
