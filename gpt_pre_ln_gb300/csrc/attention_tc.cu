@@ -6,32 +6,32 @@
 // ``_merge_heads``; llm.c notes 2.2-2.3: scale 1/sqrt(d_k), future positions
 // masked before the softmax, row maximum subtracted.)
 //
-// Persistent CTAs, two per SM so that one CTA's softmax overlaps the other's
-// tensor-core work; each walks a list of (batch, head, tile of 128 queries)
-// items, heaviest first, keeping its tensor memory and barriers, so that
-// one item's last softmax and output store overlap the next item's loads
-// and first S = Q K^T.  Per key tile of 128:
-//   S = Q K^T          tcgen05.mma M=128 N=128 K=64 -> tensor memory (fp32)
+// Persistent CTAs, four per SM, so that the softmax of some CTAs overlaps
+// the tensor-core work of the others; each walks a list of (batch, head,
+// tile of 128 queries) items, heaviest first, keeping its tensor memory and
+// barriers.  Per key tile of 64:
+//   S = Q K^T          tcgen05.mma M=128 N=64 K=64 -> tensor memory (fp32)
 //   softmax            4 warps, thread = query row = tensor-memory lane: the
 //                      row maximum and sum need no cross-thread exchange;
-//                      P = exp2(S * log2(e)/8 - m) written as bf16 into its
-//                      own 64 tensor-memory columns (tcgen05.st)
-//   O += P V           tcgen05.mma M=128 N=64 K=128 with A = P read from
+//                      P = exp2(S * log2(e)/8 - m) written as 16-bit values
+//                      over the S columns already read (tcgen05.st)
+//   O += P V           tcgen05.mma M=128 N=64 K=64 with A = P read from
 //                      tensor memory and V from shared memory (MN-major)
-// Tensor memory: S columns 0-127, O 128-191, P 192-255.  As soon as the
-// softmax of tile j has published P (and so finished reading S), the MMA
-// warp issues S for tile j + 1 and then P.V for tile j, so that the next
-// softmax computes its row maxima while P.V runs; the softmax waits for
-// that P.V before it rescales O or writes the next P.  Q, K and V sit in
-// separate two-slot rings: a K slot is refilled as soon as its S has been
-// computed, a V slot once its P.V has.
+// Tensor memory: S (and P over its first 32 columns) 0-63, O 64-127: 128
+// columns per CTA, so four CTAs share an SM's 512.  P.V of a tile is issued
+// once its softmax has published P, and the S of the next tile only after
+// that P.V has completed (S overwrites P; MMAs into different accumulators
+// are not ordered among themselves), so a CTA runs S -> softmax -> P.V in
+// turn and the four CTAs of an SM fill each other's gaps.  Q sits in one
+// slot, K and V in separate two-slot rings: a K slot is refilled as soon as
+// its S has been computed, a V slot once its P.V has.
 // The running maximum m is only raised (and O, l rescaled) when a row's new
 // maximum exceeds it by more than 8 in the log2 domain; otherwise P may reach
-// 2^8, harmless in fp32 sums and bf16.  Key tiles entirely above the
-// diagonal are never loaded; the diagonal tile is masked by index.  Q, K, V
-// tiles are read by TMA straight from the packed [B*T, 3D] c_attn output (the
-// Q|K|V split and head split are the TMA coordinates); the head merge is
-// the store into [B, T, D].
+// 2^8, harmless in fp32 sums and 16-bit P.  Key tiles entirely above the
+// diagonal or past T are never loaded; 32-key chunks of the diagonal tiles
+// are skipped or masked by index.  Q, K, V tiles are read by TMA straight
+// from the packed [B*T, 3D] c_attn output (the Q|K|V split and head split are
+// the TMA coordinates); the head merge is the store into [B, T, D].
 //
 // Waits are bounded (common.cuh): a timeout records GPT2_ERR_TIMEOUT and the
 // roles unwind; tensor memory is freed on every path.
@@ -43,15 +43,35 @@ namespace gpt2 {
 namespace {
 
 constexpr int kHd = 64;
-constexpr int kTq = 128;  // queries per CTA
-constexpr int kTk = 128;  // keys per tile
+constexpr int kTq = 128;  // queries per item
+constexpr int kTk = 64;   // keys per tile
 constexpr int kAttnThreads = 192;
-constexpr int kTileBytes = kTq * kHd * 2;  // 16 KB, 128-byte rows, swizzled
-constexpr int kSmemBytes = 1024 + 6 * kTileBytes + 256;  // Q, K, V: two slots each
-constexpr uint32_t kTmemCols = 256;  // S: 128 columns, O: 64, P: 64
-constexpr uint32_t kOCol = 128;
-constexpr uint32_t kPCol = 192;
+constexpr int kAttnCtasPerSm = 4;
+constexpr int kRowBytes = kHd * 2;              // one 128-byte swizzled row
+constexpr int kQBytes = kTq * kRowBytes;        // 16 KB
+constexpr int kKVBytes = kTk * kRowBytes;       // 8 KB (one TMA box)
+constexpr int kSmemBytes = 1024 + kQBytes + 4 * kKVBytes + 256;  // Q, K x2, V x2, barriers
+constexpr uint32_t kTmemCols = 128;  // S (P over its first 32 columns): 64, O: 64
+constexpr uint32_t kSCol = 0;
+constexpr uint32_t kPCol = 0;
+constexpr uint32_t kOCol = 64;
 constexpr float kRescaleLog2 = 8.f;
+
+// Key tiles of query tile qt: those below or on the diagonal, and holding
+// at least one key < T.
+__device__ __forceinline__ int attn_key_tiles(int qt, int T) {
+  const int diag = 2 * qt + 2;
+  const int valid = (T + kTk - 1) / kTk;
+  return diag < valid ? diag : valid;
+}
+
+// Position of the 32-key chunk c of key tile j against the 32 rows of warp
+// quadrant `quad` of query tile qt: d = first key - first row.  d <= -32:
+// every key is at or before every row (no mask); d == 0: key i of the chunk
+// is visible to lane L iff i <= L; d >= 32: no key is visible.
+__device__ __forceinline__ int attn_chunk_offset(int j, int c, int qt, int quad) {
+  return kTk * j + 32 * c - kTq * qt - 32 * quad;
+}
 
 // D[tmem] (+)= A[tmem] * B[smem], kind::f16.
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
@@ -73,26 +93,26 @@ __device__ __forceinline__ int attn_item(int k, int c, int G) {
 }
 
 template <typename T16>
-__global__ void __launch_bounds__(kAttnThreads, 2)
+__global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     attn_causal_tc(const __grid_constant__ CUtensorMap tm_qkv, T16* __restrict__ out, int B, int T, int H,
                    float scale_log2, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sQ0 = smem_u32(smem);        // Q slots 0, 1 (items)
-  const uint32_t sK0 = sQ0 + 2 * kTileBytes;  // K slots 0, 1 (key tiles)
-  const uint32_t sV0 = sQ0 + 4 * kTileBytes;  // V slots 0, 1 (key tiles)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 6 * kTileBytes);
-  auto q_full = [&](int s) { return smem_u32(bars + 0 + s); };
-  auto q_empty = [&](int s) { return smem_u32(bars + 2 + s); };
-  auto k_full = [&](int s) { return smem_u32(bars + 4 + s); };
-  auto k_empty = [&](int s) { return smem_u32(bars + 6 + s); };
-  auto v_full = [&](int s) { return smem_u32(bars + 8 + s); };
-  auto v_empty = [&](int s) { return smem_u32(bars + 10 + s); };
-  const uint32_t s_full = smem_u32(bars + 12);
-  const uint32_t p_ready = smem_u32(bars + 13);
-  const uint32_t pv_done = smem_u32(bars + 14);
-  const uint32_t drain = smem_u32(bars + 15);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  const uint32_t sQ = smem_u32(smem);          // Q (one item)
+  const uint32_t sK0 = sQ + kQBytes;           // K slots 0, 1 (key tiles)
+  const uint32_t sV0 = sK0 + 2 * kKVBytes;     // V slots 0, 1 (key tiles)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQBytes + 4 * kKVBytes);
+  const uint32_t q_full = smem_u32(bars + 0);
+  const uint32_t q_empty = smem_u32(bars + 1);
+  auto k_full = [&](int s) { return smem_u32(bars + 2 + s); };
+  auto k_empty = [&](int s) { return smem_u32(bars + 4 + s); };
+  auto v_full = [&](int s) { return smem_u32(bars + 6 + s); };
+  auto v_empty = [&](int s) { return smem_u32(bars + 8 + s); };
+  const uint32_t s_full = smem_u32(bars + 10);
+  const uint32_t p_ready = smem_u32(bars + 11);
+  const uint32_t pv_done = smem_u32(bars + 12);
+  const uint32_t drain = smem_u32(bars + 13);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -104,9 +124,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_qkv);
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(q_full(s), 1);
-      mbar_init(q_empty(s), 1);
       mbar_init(k_full(s), 1);
       mbar_init(k_empty(s), 1);
       mbar_init(v_full(s), 1);
@@ -131,48 +151,48 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 
   // Barrier phases run on across items: key tile g (counted over all items
   // of this CTA) uses K and V slot g & 1 in its (g >> 1)-th round and the
-  // g-th phase of s_full / p_ready / pv_done; item i uses Q slot i & 1 in
-  // its (i >> 1)-th round.  A K slot is free again once its S = Q K^T has
-  // been computed, a V slot once its P.V has, so the producer issues each
-  // tile's K ahead of the V of the tile before: both then arrive about two
-  // key tiles ahead of their use, which covers the load latency.
+  // g-th phase of s_full / p_ready / pv_done; item i uses the Q slot in its
+  // i-th round.  The producer issues each tile's K ahead of the V of the
+  // tile before.
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
       struct Item {
-        int qt, row_base, h;
+        int qt, nkt, row_base, h;
       };
       auto get_item = [&](int kk, Item& it) {
         const int w = attn_item(kk, cta, G);
         if (w >= n_items) return false;
         const int bh = w % BH;
         it.qt = n_qt - 1 - w / BH;
+        it.nkt = attn_key_tiles(it.qt, T);
         it.row_base = (bh / H) * T;
         it.h = bh % H;
         return true;
       };
       long long nq = 0, nk = 0, nv = 0;  // loads issued
       auto load_q = [&](int kk, const Item& it) {
-        const int sl = kk & 1;
-        if (!mbar_wait(q_empty(sl), static_cast<uint32_t>((kk >> 1) & 1) ^ 1)) return false;
-        mbar_arrive_expect_tx(q_full(sl), kTileBytes);
-        tma_load_2d(sQ0 + sl * kTileBytes, &tm_qkv, q_full(sl), it.h * kHd, it.row_base + it.qt * kTq);
+        if (!mbar_wait(q_empty, static_cast<uint32_t>(kk & 1) ^ 1)) return false;
+        mbar_arrive_expect_tx(q_full, kQBytes);
+        const int r0 = it.row_base + it.qt * kTq;
+        tma_load_2d(sQ, &tm_qkv, q_full, it.h * kHd, r0);
+        tma_load_2d(sQ + kKVBytes, &tm_qkv, q_full, it.h * kHd, r0 + kTk);
         ++nq;
         return true;
       };
       auto load_k = [&](long long gg, const Item& it, int jj) {
         const int sl = static_cast<int>(gg & 1);
         if (!mbar_wait(k_empty(sl), static_cast<uint32_t>((gg >> 1) & 1) ^ 1)) return false;
-        mbar_arrive_expect_tx(k_full(sl), kTileBytes);
-        tma_load_2d(sK0 + sl * kTileBytes, &tm_qkv, k_full(sl), D + it.h * kHd, it.row_base + jj * kTk);
+        mbar_arrive_expect_tx(k_full(sl), kKVBytes);
+        tma_load_2d(sK0 + sl * kKVBytes, &tm_qkv, k_full(sl), D + it.h * kHd, it.row_base + jj * kTk);
         ++nk;
         return true;
       };
       auto load_v = [&](long long gg, const Item& it, int jj) {
         const int sl = static_cast<int>(gg & 1);
         if (!mbar_wait(v_empty(sl), static_cast<uint32_t>((gg >> 1) & 1) ^ 1)) return false;
-        mbar_arrive_expect_tx(v_full(sl), kTileBytes);
-        tma_load_2d(sV0 + sl * kTileBytes, &tm_qkv, v_full(sl), 2 * D + it.h * kHd, it.row_base + jj * kTk);
+        mbar_arrive_expect_tx(v_full(sl), kKVBytes);
+        tma_load_2d(sV0 + sl * kKVBytes, &tm_qkv, v_full(sl), 2 * D + it.h * kHd, it.row_base + jj * kTk);
         ++nv;
         return true;
       };
@@ -187,7 +207,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
           Item nx = cur;
           int nk_i = k, nj = j + 1;
           bool has_next = true;
-          if (nj > cur.qt) {
+          if (nj >= cur.nkt) {
             nk_i = k + 1;
             nj = 0;
             has_next = get_item(nk_i, nx);
@@ -214,10 +234,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         }
       }
       if (!ok) record_error(err, kErrTimeout, kSiteAttnProducer);
-      // copies still in flight: the last (up to two) of each kind
+      // copies still in flight: the last Q and the last (up to two) K and V
       bool drained = true;
-      for (long long x = nq > 2 ? nq - 2 : 0; x < nq && drained; ++x)
-        drained = mbar_wait(q_full(static_cast<int>(x & 1)), static_cast<uint32_t>((x >> 1) & 1));
+      if (nq > 0) drained = mbar_wait(q_full, static_cast<uint32_t>((nq - 1) & 1));
       for (long long x = nk > 2 ? nk - 2 : 0; x < nk && drained; ++x)
         drained = mbar_wait(k_full(static_cast<int>(x & 1)), static_cast<uint32_t>((x >> 1) & 1));
       for (long long x = nv > 2 ? nv - 2 : 0; x < nv && drained; ++x)
@@ -229,23 +248,20 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       // ------------------------------------------------ MMA issuer
       constexpr uint32_t idesc_s = idesc_f16kind_f32(kTq, kTk, false, false, Type16<T16>::kFormat);
       constexpr uint32_t idesc_pv = idesc_f16kind_f32(kTq, kHd, false, true, Type16<T16>::kFormat);
-      // Per key tile g: S(g) as soon as the softmax has released the S
-      // columns (p_ready of g - 1), then P.V of tile g - 1; so the softmax
-      // of tile g (its row maxima) runs while P.V(g - 1) does.
+      // Per key tile g: P.V of tile g - 1 once its softmax has published P,
+      // then (after that P.V has read P) S of tile g into the same columns.
       bool ok = true;
       bool any = false;
       long long g = 0;
-      int prev_j = 0;     // tile index within its item of tile g - 1
-      int prev_st = 0;    // its K / V slot
-      uint32_t prev_ph = 0;
-      auto pv = [&](long long gp, int jj, int st, uint32_t ph) {
-        // P.V of tile gp: P (tensor memory) is published once p_ready
-        // reaches phase gp; V arrives on v_full
+      int prev_j = 0;   // tile index within its item of tile g - 1
+      auto pv = [&](long long gp, int jj) {
+        const int st = static_cast<int>(gp & 1);
+        const uint32_t ph = static_cast<uint32_t>((gp >> 1) & 1);
         if (!mbar_wait(p_ready, static_cast<uint32_t>(gp & 1)) || !mbar_wait(v_full(st), ph)) return false;
         tc_fence_after();
-        const uint32_t vb = sV0 + st * kTileBytes;
+        const uint32_t vb = sV0 + st * kKVBytes;
 #pragma unroll
-        for (int kk = 0; kk < kTk / 16; ++kk)  // P: 8 tensor-memory columns (16 bf16) per K=16
+        for (int kk = 0; kk < kTk / 16; ++kk)  // P: 8 tensor-memory columns (16 keys) per K=16
           umma_bf16_ts(tmem + kOCol, tmem + kPCol + kk * 8, sdesc_sw128(vb + kk * 2048, 8192, 1024), idesc_pv,
                        (jj | kk) != 0 ? 1u : 0u);
         umma_commit(pv_done);
@@ -256,40 +272,38 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         const int w = attn_item(k, cta, G);
         if (w >= n_items) break;
         const int qt = n_qt - 1 - w / BH;
-        const int qs = k & 1;
-        ok = mbar_wait(q_full(qs), static_cast<uint32_t>((k >> 1) & 1));
-        const uint32_t qb = sQ0 + qs * kTileBytes;
-        for (int j = 0; j <= qt && ok; ++j, ++g) {
+        const int nkt = attn_key_tiles(qt, T);
+        for (int j = 0; j < nkt && ok; ++j, ++g) {
+          if (g > 0) {
+            if (!pv(g - 1, prev_j) || !mbar_wait(pv_done, static_cast<uint32_t>((g - 1) & 1))) {
+              ok = false;
+              break;
+            }
+          }
           const int st = static_cast<int>(g & 1);
-          const uint32_t ph = static_cast<uint32_t>((g >> 1) & 1);
-          // the softmax of tile g - 1 has read S (and written P)
-          if (g > 0 && !mbar_wait(p_ready, static_cast<uint32_t>((g - 1) & 1))) {
+          if (j == 0 && !mbar_wait(q_full, static_cast<uint32_t>(k & 1))) {
             ok = false;
             break;
           }
-          ok = mbar_wait(k_full(st), ph);
-          if (!ok) break;
+          if (!mbar_wait(k_full(st), static_cast<uint32_t>((g >> 1) & 1))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint32_t kb = sK0 + st * kTileBytes;
+          const uint32_t kb = sK0 + st * kKVBytes;
 #pragma unroll
           for (int kk = 0; kk < kHd / 16; ++kk)
-            umma_bf16(tmem, sdesc_sw128(qb + kk * 32, 16, 1024), sdesc_sw128(kb + kk * 32, 16, 1024), idesc_s,
-                      kk > 0 ? 1u : 0u);
+            umma_bf16(tmem + kSCol, sdesc_sw128(sQ + kk * 32, 16, 1024), sdesc_sw128(kb + kk * 32, 16, 1024),
+                      idesc_s, kk > 0 ? 1u : 0u);
           umma_commit(s_full);
           umma_commit(k_empty(st));
-          if (j == qt) umma_commit(q_empty(qs));  // the item's last read of its Q
+          if (j == nkt - 1) umma_commit(q_empty);  // the item's last read of its Q
           any = true;
-          if (g > 0 && !pv(g - 1, prev_j, prev_st, prev_ph)) {
-            ok = false;
-            break;
-          }
           prev_j = j;
-          prev_st = st;
-          prev_ph = ph;
         }
       }
       // the last tile's P.V
-      if (ok && g > 0 && !pv(g - 1, prev_j, prev_st, prev_ph)) ok = false;
+      if (ok && g > 0 && !pv(g - 1, prev_j)) ok = false;
       if (!ok) record_error(err, kErrTimeout, kSiteAttnMma);
       if (any) {
         umma_commit(drain);
@@ -301,7 +315,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_off;
+    const uint32_t tS = tmem + lane_off + kSCol;
     const uint32_t tO = tmem + lane_off + kOCol;
     const uint32_t tP = tmem + lane_off + kPCol;
     const float scale = scale_log2;  // log2(e) times the score scale (1/sqrt(64) for GPT-2)
@@ -313,60 +327,44 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       const int qt = n_qt - 1 - w / BH, bh = w % BH;
       const int b = bh / H, h = bh % H;
       const int q = qt * kTq + r;
+      const int nkt = attn_key_tiles(qt, T);
       float m_run = -INFINITY;
       float l = 0.f;
-      for (int j = 0; j <= qt; ++j, ++g) {
+      for (int j = 0; j < nkt; ++j, ++g) {
+        // S of tile g; the P.V of tile g - 1 completed before it was issued,
+        // and this commit covers it, so O is settled too
         const bool got = mbar_wait(s_full, static_cast<uint32_t>(g & 1));
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const bool diag = (j == qt);
         // pass 1: row maximum of the raw scores (8 independent partial
         // maxima, three-input max; the scale is positive, so it is applied
-        // once to the maximum).  In the diagonal tile, key chunk c holds
-        // keys c*32 .. c*32+31 of the tile against rows quad*32 + lane:
-        // chunks c > quad are above the diagonal for the whole warp and are
-        // skipped, chunk c == quad is masked per lane.
+        // once to the maximum); chunks wholly above the diagonal skipped
         float pm[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) pm[e] = -INFINITY;
 #pragma unroll
-        for (int c2 = 0; c2 < kTk / 64; ++c2) {
-          if (diag && 2 * c2 > quad) break;
-          uint32_t raw[2][32];
-          tmem_ld_32x32b_x32(tS + c2 * 64, raw[0]);
-          tmem_ld_32x32b_x32(tS + c2 * 64 + 32, raw[1]);
+        for (int c = 0; c < kTk / 32; ++c) {
+          const int d = attn_chunk_offset(j, c, qt, quad);
+          if (d > 0) continue;
+          uint32_t raw[32];
+          tmem_ld_32x32b_x32(tS + c * 32, raw);
           tmem_ld_wait();
+          if (d == 0) {
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int c = 2 * c2 + h2;
-            if (diag && c >= quad) {
-              if (c == quad) {
+            for (int i = 0; i < 32; ++i)
+              if (i <= lane) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(raw[i]));
+          } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (i <= lane) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(raw[h2][i]));
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 16; ++i)
-                pm[i & 7] = max3f(pm[i & 7], __uint_as_float(raw[h2][2 * i]), __uint_as_float(raw[h2][2 * i + 1]));
-            }
+            for (int i = 0; i < 16; ++i)
+              pm[i & 7] = max3f(pm[i & 7], __uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]));
           }
         }
         const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                                fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * scale;
         const bool raise = mx > m_run + kRescaleLog2;
-        // the previous P.V of this item has read P and updated O
-        if (j > 0) {
-          const bool pv_ok = __all_sync(0xffffffffu, mbar_wait(pv_done, static_cast<uint32_t>((g - 1) & 1)));
-          if (!pv_ok) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
         // tcgen05.ld / tcgen05.st are warp-collective: the whole warp takes
         // the rescale branch if any of its rows needs it (alpha = 1 for the
         // others)
@@ -385,9 +383,11 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
           }
         }
         if (raise) m_run = mx;
-        // pass 2: P = exp2(s * scale - m_run) as 16-bit values into the P
-        // columns, paired fp32 arithmetic; 4 independent pair sums.  Chunks
-        // of the diagonal tile above the diagonal are written as zeros.
+        // pass 2: P = exp2(s * scale - m_run) as 16-bit values, 16 columns
+        // per 32-key chunk, written over S columns this thread has already
+        // read (chunk c's P lands in columns 16c .. 16c + 15 < 32c + 32);
+        // paired fp32 arithmetic, 4 independent pair sums; masked chunks
+        // are written as zeros
         float2 ps[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) ps[e] = make_float2(0.f, 0.f);
@@ -395,8 +395,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         const float2 neg_m2 = make_float2(-m_run, -m_run);
 #pragma unroll
         for (int c = 0; c < kTk / 32; ++c) {
+          const int d = attn_chunk_offset(j, c, qt, quad);
           uint32_t pk[16];
-          if (diag && c > quad) {
+          if (d > 0) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) pk[i] = 0u;
           } else {
@@ -408,7 +409,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
               const float2 x = fma_f32x2(make_float2(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])),
                                          scale2, neg_m2);
               float2 p2 = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-              if (diag && c == quad) {
+              if (d == 0) {
                 if (2 * i > lane) p2.x = 0.f;
                 if (2 * i + 1 > lane) p2.y = 0.f;
               }
@@ -469,7 +470,7 @@ cudaError_t launch_t(const void* qkv, void* out, int B, int T, int n_head, float
   if (B == 0 || T == 0) return cudaSuccess;
   const uint64_t D = static_cast<uint64_t>(n_head) * kHd;
   CUtensorMap map;
-  if (!encode_tma_2d(&map, Type16<T16>::kTma, qkv, 3 * D, static_cast<uint64_t>(B) * T, 3 * D * 2, kHd, kTq))
+  if (!encode_tma_2d(&map, Type16<T16>::kTma, qkv, 3 * D, static_cast<uint64_t>(B) * T, 3 * D * 2, kHd, kTk))
     return cudaErrorInvalidValue;
   static int configured[64] = {0};
   int dev = 0;
@@ -480,13 +481,11 @@ cudaError_t launch_t(const void* qkv, void* out, int B, int T, int n_head, float
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  // persistent: two CTAs per SM (the launch bounds, 83 KB of shared memory
-  // and 256 tensor-memory columns each are sized for that), each walking its
-  // share of the (batch, head, query tile) items.  The block-occupancy query
-  // reports one per SM for this kernel on GB300 (measured: a 152-CTA grid
-  // runs at the speed of a one-per-SM launch), so the count is set directly.
+  // persistent: four CTAs per SM (the launch bounds, ~50 KB of shared
+  // memory and 128 tensor-memory columns each are sized for that), each
+  // walking its share of the (batch, head, query tile) items
   const long long items = static_cast<long long>(B) * n_head * ((T + kTq - 1) / kTq);
-  const long long resident = 2ll * num_sms();
+  const long long resident = static_cast<long long>(kAttnCtasPerSm) * num_sms();
   const int grid = static_cast<int>(items < resident ? items : resident);
   return launch_pdl(attn_causal_tc<T16>, dim3(grid), kAttnThreads, kSmemBytes, stream, 0, map,
                     static_cast<T16*>(out), B, T, n_head, 1.4426950408889634f * score_scale, device_error_word());
