@@ -16,7 +16,8 @@ __all__ = [
     "GPT2Error", "F32", "BF16", "F16", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_GELU", "EPI_BIAS_RESIDUAL",
     "EPI_BIAS_GELU_EXACT", "SCALE_ATTN_BY_INVERSE_LAYER_IDX", "GELU_EXACT", "W_IN_OUT", "W_OUT_IN", "Dims", "BlockWeights", "ModelWeights", "lib", "library_path", "gpt2_abi_version",
     "gpt2_status_string", "gpt2_last_error", "gpt2_layernorm", "gpt2_linear", "gpt2_attention_causal",
-    "gpt2_attention_causal_scaled", "gpt2_block_forward_layer",
+    "gpt2_attention_causal_scaled", "gpt2_block_forward_layer", "BlockGrads", "block_grads",
+    "gpt2_block_backward_workspace_bytes", "gpt2_block_backward",
     "gpt2_mlp_workspace_bytes", "gpt2_mlp", "gpt2_mlp_noalloc", "gpt2_mlp_noalloc_max_scratch_bytes",
     "gpt2_workspace_bytes", "gpt2_block_forward", "gpt2_forward_logits", "gpt2_loss_workspace_bytes",
     "gpt2_forward_loss", "gpt2_prefill_workspace_bytes", "gpt2_prefill",
@@ -58,6 +59,10 @@ class BlockWeights(ctypes.Structure):
     _fields_ = [(k, ctypes.c_void_p) for k in _BLOCK_FIELDS]
 
 
+class BlockGrads(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_void_p) for k in _BLOCK_FIELDS]
+
+
 class ModelWeights(ctypes.Structure):
     _fields_ = [("wte", ctypes.c_void_p), ("wpe", ctypes.c_void_p), ("lnf_g", ctypes.c_void_p),
                 ("lnf_b", ctypes.c_void_p), ("blocks", ctypes.POINTER(BlockWeights))]
@@ -85,6 +90,9 @@ _SIGS = {
                                   _VP]),
     "gpt2_block_forward_layer": (_I32, [ctypes.POINTER(Dims), ctypes.POINTER(BlockWeights), _I32, _VP, _VP, _I32, _I32,
                                         _VP, _SZ, _VP]),
+    "gpt2_block_backward_workspace_bytes": (_SZ, [ctypes.POINTER(Dims), _I32, _I32]),
+    "gpt2_block_backward": (_I32, [ctypes.POINTER(Dims), ctypes.POINTER(BlockWeights), _I32, _VP, _VP, _VP,
+                                   ctypes.POINTER(BlockGrads), _I32, _I32, _VP, _SZ, _VP]),
     "gpt2_forward_logits": (_I32, [ctypes.POINTER(Dims), ctypes.POINTER(ModelWeights), _VP, _VP, _I64, _I32, _I32,
                                    _I32, _VP, _SZ, _VP]),
     "gpt2_loss_workspace_bytes": (_SZ, [ctypes.POINTER(Dims), _I32, _I32]),
@@ -211,6 +219,17 @@ def gpt2_block_forward_layer(dims: Dims, w: BlockWeights, layer, x_in, x_out, B,
                                           _ptr(ws), ws_bytes, _stream(stream)), "gpt2_block_forward_layer")
 
 
+def gpt2_block_backward_workspace_bytes(dims: Dims, B: int, T: int) -> int:
+    return lib().gpt2_block_backward_workspace_bytes(ctypes.byref(dims), B, T)
+
+
+def gpt2_block_backward(dims: Dims, w: BlockWeights, layer, x_in, dx_out, dx_in, grads: BlockGrads, B, T, ws,
+                        ws_bytes, stream=None):
+    _check(lib().gpt2_block_backward(ctypes.byref(dims), ctypes.byref(w), layer, _ptr(x_in), _ptr(dx_out),
+                                     _ptr(dx_in), ctypes.byref(grads), B, T, _ptr(ws), ws_bytes, _stream(stream)),
+           "gpt2_block_backward")
+
+
 def gpt2_forward_logits(dims: Dims, w: ModelWeights, tokens, logits, ld, logits_t, B, T, ws, ws_bytes, stream=None):
     _check(lib().gpt2_forward_logits(ctypes.byref(dims), ctypes.byref(w), _ptr(tokens), _ptr(logits), ld, logits_t,
                                      B, T, _ptr(ws), ws_bytes, _stream(stream)), "gpt2_forward_logits")
@@ -278,6 +297,11 @@ def make_dims(n_layer, d_model, n_head, d_ff, vocab, n_pos, eps=1e-5, dtype=BF16
 def block_weights(tensors: dict) -> BlockWeights:
     """BlockWeights from a dict of device tensors keyed like the C struct."""
     return BlockWeights(*[_ptr(tensors[k]) for k in _BLOCK_FIELDS])
+
+
+def block_grads(tensors: dict) -> BlockGrads:
+    """BlockGrads from a dict of fp32 device tensors keyed like the C struct."""
+    return BlockGrads(*[_ptr(tensors[k]) for k in _BLOCK_FIELDS])
 
 
 def model_weights(tensors: dict):

@@ -457,6 +457,101 @@ size_t loss_extra_bytes(const gpt2_dims* d, int64_t M) {
   return b;
 }
 
+// ------------------------------------------------------- block backward
+// Workspace of gpt2_block_backward (fp32): the recomputed forward
+// intermediates, the gradients between the steps, the LayerNorm products
+// and the attention row statistics.
+struct BwdActs {
+  float *a, *qkv, *o, *h, *a2, *u, *g;        // forward: LN_1(x), c_attn, attention, h, LN_2(h), c_fc, act
+  float *dg, *du, *da2, *dh, *dout, *dqkv, *da;  // backward
+  float *prod, *lse, *delta;
+};
+
+size_t bwd_ws_bytes(const gpt2_dims* d, int B, int T) {
+  const size_t M = static_cast<size_t>(B) * T, D = d->d_model, F = d->d_ff, H = d->n_head;
+  const size_t rows_d = align256(M * D * 4), rows_3d = align256(M * 3 * D * 4), rows_f = align256(M * F * 4);
+  const size_t stats = align256(static_cast<size_t>(B) * H * T * 4);
+  return rows_d * 9 + rows_3d * 2 + rows_f * 4 + stats * 2;
+}
+
+BwdActs carve_bwd(void* ws, const gpt2_dims* d, int B, int T) {
+  Carve c(ws);
+  const size_t M = static_cast<size_t>(B) * T, D = d->d_model, F = d->d_ff, H = d->n_head;
+  BwdActs A;
+  A.a = c.take<float>(M * D, 4);
+  A.qkv = c.take<float>(M * 3 * D, 4);
+  A.o = c.take<float>(M * D, 4);
+  A.h = c.take<float>(M * D, 4);
+  A.a2 = c.take<float>(M * D, 4);
+  A.u = c.take<float>(M * F, 4);
+  A.g = c.take<float>(M * F, 4);
+  A.dg = c.take<float>(M * F, 4);
+  A.du = c.take<float>(M * F, 4);
+  A.da2 = c.take<float>(M * D, 4);
+  A.dh = c.take<float>(M * D, 4);
+  A.dout = c.take<float>(M * D, 4);
+  A.dqkv = c.take<float>(M * 3 * D, 4);
+  A.da = c.take<float>(M * D, 4);
+  A.prod = c.take<float>(M * D, 4);
+  A.lse = c.take<float>(static_cast<size_t>(B) * H * T, 4);
+  A.delta = c.take<float>(static_cast<size_t>(B) * H * T, 4);
+  return A;
+}
+
+// Recomputes the block's forward, then runs its steps backwards:
+//   x' = h + c_proj2(g):  dg = dx' W_proj^T, dW_proj = g^T dx', db_proj
+//   g = act(u):           du = dg act'(u)
+//   u = c_fc(LN_2(h)):    da2 = du W_fc^T, dW_fc = a2^T du, db_fc
+//   LN_2, residual:       dh = dx' + LN_2'(h)^T da2, dln2_g, dln2_b
+//   h = x + c_proj(o):    do = dh W_o^T, dW_o = o^T dh, db_o
+//   o = attention(qkv):   dqkv
+//   qkv = c_attn(LN_1(x)): da = dqkv W_qkv^T, dW_qkv = a^T dqkv, db_qkv
+//   LN_1, residual:       dx = dh + LN_1'(x)^T da, dln1_g, dln1_b
+int block_backward_f32(const gpt2_dims* d, const gpt2_block_weights* w, int layer, const float* x, const float* dy,
+                       float* dx, const gpt2_block_grads* gr, int B, int T, void* ws, cudaStream_t s) {
+  const int64_t M = static_cast<int64_t>(B) * T;
+  const int D = d->d_model, F = d->d_ff, H = d->n_head;
+  const float eps = d->eps, sc = score_scale(d, layer);
+  const bool exact = (d->flags & GPT2_GELU_EXACT) != 0;
+  BwdActs A = carve_bwd(ws, d, B, T);
+  auto f = [](const void* p) { return static_cast<const float*>(p); };
+  // forward
+  GPT2_CUDA(layernorm(x, w->ln1_g, w->ln1_b, A.a, M, D, eps, GPT2_F32, GPT2_F32, s));
+  GPT2_CUDA(linear(GPT2_F32, A.a, w->w_qkv, w->b_qkv, nullptr, A.qkv, M, 3 * D, D, 3 * D, false, GPT2_EPI_BIAS,
+                   GPT2_F32, s));
+  GPT2_CUDA(attention(GPT2_F32, A.qkv, A.o, B, T, H, sc, s));
+  GPT2_CUDA(linear(GPT2_F32, A.o, w->w_o, w->b_o, x, A.h, M, D, D, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32, s));
+  GPT2_CUDA(layernorm(A.h, w->ln2_g, w->ln2_b, A.a2, M, D, eps, GPT2_F32, GPT2_F32, s));
+  GPT2_CUDA(linear(GPT2_F32, A.a2, w->w_fc, w->b_fc, nullptr, A.u, M, F, D, F, false, GPT2_EPI_BIAS, GPT2_F32, s));
+  GPT2_CUDA(launch_gelu_f32(A.u, A.g, M * F, exact, s));
+  // MLP
+  GPT2_CUDA(linear(GPT2_F32, dy, w->w_proj, nullptr, nullptr, A.dg, M, F, D, F, true, GPT2_EPI_NONE, GPT2_F32, s));
+  GPT2_CUDA(launch_gemm_at_f32(A.g, dy, gr->w_proj, M, F, D, s));
+  GPT2_CUDA(launch_colsum_f32(dy, gr->b_proj, M, D, s));
+  GPT2_CUDA(launch_gelu_backward_f32(A.dg, A.u, A.du, M * F, exact, s));
+  GPT2_CUDA(linear(GPT2_F32, A.du, w->w_fc, nullptr, nullptr, A.da2, M, D, F, D, true, GPT2_EPI_NONE, GPT2_F32, s));
+  GPT2_CUDA(launch_gemm_at_f32(A.a2, A.du, gr->w_fc, M, D, F, s));
+  GPT2_CUDA(launch_colsum_f32(A.du, gr->b_fc, M, F, s));
+  // LN_2 and the residual path
+  GPT2_CUDA(launch_ln_backward_f32(A.da2, A.h, f(w->ln2_g), dy, A.dh, A.prod, M, D, eps, s));
+  GPT2_CUDA(launch_colsum_f32(A.prod, gr->ln2_g, M, D, s));
+  GPT2_CUDA(launch_colsum_f32(A.da2, gr->ln2_b, M, D, s));
+  // attention sublayer
+  GPT2_CUDA(linear(GPT2_F32, A.dh, w->w_o, nullptr, nullptr, A.dout, M, D, D, D, true, GPT2_EPI_NONE, GPT2_F32, s));
+  GPT2_CUDA(launch_gemm_at_f32(A.o, A.dh, gr->w_o, M, D, D, s));
+  GPT2_CUDA(launch_colsum_f32(A.dh, gr->b_o, M, D, s));
+  GPT2_CUDA(launch_attention_backward_f32(A.qkv, A.dout, A.dqkv, A.lse, A.delta, B, T, H, sc, s));
+  GPT2_CUDA(linear(GPT2_F32, A.dqkv, w->w_qkv, nullptr, nullptr, A.da, M, D, 3 * D, D, true, GPT2_EPI_NONE,
+                   GPT2_F32, s));
+  GPT2_CUDA(launch_gemm_at_f32(A.a, A.dqkv, gr->w_qkv, M, D, 3 * D, s));
+  GPT2_CUDA(launch_colsum_f32(A.dqkv, gr->b_qkv, M, 3 * D, s));
+  // LN_1 and the residual path
+  GPT2_CUDA(launch_ln_backward_f32(A.da, x, f(w->ln1_g), A.dh, dx, A.prod, M, D, eps, s));
+  GPT2_CUDA(launch_colsum_f32(A.prod, gr->ln1_g, M, D, s));
+  GPT2_CUDA(launch_colsum_f32(A.da, gr->ln1_b, M, D, s));
+  return GPT2_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -591,6 +686,40 @@ int gpt2_block_forward_layer(const gpt2_dims* dims, const gpt2_block_weights* w,
   cudaStream_t s = cs(stream);
   GPT2_CUDA(layernorm(x_in, w->ln1_g, w->ln1_b, A.a, M, dims->d_model, dims->eps, GPT2_F32, dims->dtype, s));
   return block_body(dims, w, layer, x_in, x_out, B, T, A, s);
+}
+
+size_t gpt2_block_backward_workspace_bytes(const gpt2_dims* dims, int B, int T) {
+  if (check_dims(dims, false) != GPT2_OK || dims->dtype != GPT2_F32 || B < 0 || T < 0) return 0;
+  return bwd_ws_bytes(dims, B, T);
+}
+
+int gpt2_block_backward(const gpt2_dims* dims, const gpt2_block_weights* w, int layer, const float* x_in,
+                        const float* dx_out, float* dx_in, const gpt2_block_grads* grads, int B, int T, void* ws,
+                        size_t ws_bytes, gpt2_stream_t stream) {
+  GPT2_TRY(check_dims(dims, false));
+  GPT2_TRY(check_block_ptrs(w));
+  if (dims->dtype != GPT2_F32) return GPT2_ERR_UNSUPPORTED;
+  if (layer < 0 || B < 0 || T < 0 || static_cast<int64_t>(B) * T > INT_MAX) return GPT2_ERR_ARG;
+  if (T > 4096) return GPT2_ERR_UNSUPPORTED;
+  if (B == 0 || T == 0) return GPT2_OK;
+  if (!grads || !x_in || !dx_out || !dx_in) return GPT2_ERR_ARG;
+  const void* gs[12] = {grads->ln1_g, grads->ln1_b, grads->w_qkv, grads->b_qkv, grads->w_o,    grads->b_o,
+                        grads->ln2_g, grads->ln2_b, grads->w_fc,  grads->b_fc,  grads->w_proj, grads->b_proj};
+  for (const void* p : gs)
+    if (!p || !aligned16(p)) return GPT2_ERR_ARG;
+  if (!aligned16(x_in) || !aligned16(dx_out) || !aligned16(dx_in)) return GPT2_ERR_ARG;
+  const int64_t M = static_cast<int64_t>(B) * T;
+  const int D = dims->d_model;
+  const size_t bytes = static_cast<size_t>(M) * D * 4;
+  auto overlap = [&](const void* a, const void* b) {
+    const char* x = static_cast<const char*>(a);
+    const char* y = static_cast<const char*>(b);
+    return x < y + bytes && y < x + bytes;
+  };
+  if (overlap(dx_in, x_in) || overlap(dx_in, dx_out)) return GPT2_ERR_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return GPT2_ERR_ARG;
+  if (ws_bytes < bwd_ws_bytes(dims, B, T)) return GPT2_ERR_WORKSPACE;
+  return block_backward_f32(dims, w, layer, x_in, dx_out, dx_in, grads, B, T, ws, cs(stream));
 }
 
 int gpt2_forward_logits(const gpt2_dims* dims, const gpt2_model_weights* w, const int32_t* tokens, void* logits,

@@ -132,4 +132,22 @@ cudaError_t launch_lse_from_logits(const float* logits, int64_t ld, int64_t M, i
 cudaError_t launch_argmax_candidates(const float2* cand, int n_cand, int B, const int* valid, int32_t* next_tokens,
                                      int32_t* past_len, cudaStream_t stream);
 
+// Backward of one block on the fp32 path (backward_f32.cu).
+// dw[K, N] = x[M, K]^T dy[M, N].
+cudaError_t launch_gemm_at_f32(const float* x, const float* dy, float* dw, int64_t M, int K, int N,
+                               cudaStream_t stream);
+// out[N] = column sums of in[M, N], rows in order.
+cudaError_t launch_colsum_f32(const float* in, float* out, int64_t M, int N, cudaStream_t stream);
+// LayerNorm backward: dx = LN'(x)^T dy (+ dres when not null), prod = dy * xhat.
+cudaError_t launch_ln_backward_f32(const float* dy, const float* x, const float* gamma, const float* dres, float* dx,
+                                   float* prod, int64_t rows, int D, float eps, cudaStream_t stream);
+// g = gelu(u) and du = dg * gelu'(u), the exact GELU or gelu_new.
+cudaError_t launch_gelu_f32(const float* u, float* g, int64_t n, bool exact, cudaStream_t stream);
+cudaError_t launch_gelu_backward_f32(const float* dg, const float* u, float* du, int64_t n, bool exact,
+                                     cudaStream_t stream);
+// Causal attention backward: dqkv [B, T, 3D] from qkv and dout [B, T, D];
+// lse, delta: [B, n_head, T] scratch.  T <= 4096.
+cudaError_t launch_attention_backward_f32(const float* qkv, const float* dout, float* dqkv, float* lse, float* delta,
+                                          int B, int T, int n_head, float score_scale, cudaStream_t stream);
+
 }  // namespace gpt2

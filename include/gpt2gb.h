@@ -260,6 +260,39 @@ int gpt2_forward_logits(const gpt2_dims *dims, const gpt2_model_weights *w, cons
                         int64_t ld, gpt2_dtype logits_t, int B, int T, void *ws, size_t ws_bytes,
                         gpt2_stream_t stream);
 
+/* Gradients of one block's 12 tensors, fp32 device buffers shaped like the
+ * tensors of gpt2_block_weights (written, not accumulated). */
+typedef struct {
+  float *ln1_g, *ln1_b;
+  float *w_qkv, *b_qkv;
+  float *w_o, *b_o;
+  float *ln2_g, *ln2_b;
+  float *w_fc, *b_fc;
+  float *w_proj, *b_proj;
+} gpt2_block_grads;
+
+/* Workspace needed by gpt2_block_backward for a [B, T] batch (0 if the dims
+ * are invalid or not the F32 path). */
+size_t gpt2_block_backward_workspace_bytes(const gpt2_dims *dims, int B, int T);
+
+/* Backward pass of one Pre-LN block on the F32 path (llm.c notes section
+ * 5.3: LayerNorm gradients through the mean, the variance and the
+ * normalised value, with gamma's and beta's own; the softmax gradient;
+ * zero gradient at causally masked positions).  Given the block's input
+ * x_in [B, T, D] and the gradient dx_out [B, T, D] of a scalar loss with
+ * respect to its output, writes dx_in [B, T, D] (the gradient with respect
+ * to the input) and every weight gradient into `grads`.  The forward
+ * intermediates are recomputed into the workspace.  `layer` as in
+ * gpt2_block_forward_layer (the index of the block in its stack).
+ *   dims->dtype must be GPT2_F32 (else GPT2_ERR_UNSUPPORTED); T <= 4096;
+ *   dx_in must not overlap x_in or dx_out; ws of
+ *   gpt2_block_backward_workspace_bytes(dims, B, T) bytes, 256-byte
+ *   aligned.  fp32 CUDA cores throughout; the sums over rows run in a
+ *   fixed order, so results are deterministic. */
+int gpt2_block_backward(const gpt2_dims *dims, const gpt2_block_weights *w, int layer, const float *x_in,
+                        const float *dx_out, float *dx_in, const gpt2_block_grads *grads, int B, int T, void *ws,
+                        size_t ws_bytes, gpt2_stream_t stream);
+
 /* Workspace needed by gpt2_forward_loss for a [B, T] batch (0 if the dims
  * are invalid). */
 size_t gpt2_loss_workspace_bytes(const gpt2_dims *dims, int B, int T);

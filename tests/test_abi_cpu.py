@@ -113,6 +113,19 @@ def test_argument_checks_before_any_launch(L):
     d_sw = G.make_dims(2, 768, 12, 2048, 50257, 1024, flags=G.SCALE_ATTN_BY_INVERSE_LAYER_IDX | G.GELU_EXACT)
     assert G.gpt2_workspace_bytes(d_sw, 8, 1024) == 2 * 8192 * 768 * 4 + 2 * 8192 * 768 * 2 + 8192 * 3 * 768 * 2 + \
         8192 * 2048 * 2  # n_inner = 2048
+    grads = G.BlockGrads(*([256] * 12))
+    assert L.gpt2_block_backward(ctypes.byref(d), ctypes.byref(blk), 0, 256, 512, 768, ctypes.byref(grads), 2, 64,
+                                 256, 1 << 30, None) == 2  # 16-bit dims: the backward is F32 only
+    d32b = G.make_dims(2, 768, 12, 3072, 50257, 1024, dtype=G.F32)
+    assert G.gpt2_block_backward_workspace_bytes(d, 2, 64) == 0
+    wsb = G.gpt2_block_backward_workspace_bytes(d32b, 2, 64)
+    assert wsb > 0
+    assert L.gpt2_block_backward(ctypes.byref(d32b), ctypes.byref(blk), 0, 256, 1 << 20, 1 << 24,
+                                 ctypes.byref(grads), 2, 64, 256, wsb - 1, None) == 3  # workspace too small
+    assert L.gpt2_block_backward(ctypes.byref(d32b), ctypes.byref(blk), 0, 256, 1 << 20, 256 + 4096,
+                                 ctypes.byref(grads), 2, 64, 256, wsb, None) == 1  # dx_in overlaps x_in
+    assert L.gpt2_block_backward(ctypes.byref(d32b), ctypes.byref(blk), 0, 256, 1 << 20, 1 << 24,
+                                 ctypes.byref(grads), 1, 4097, 256, 1 << 40, None) == 2  # T > 4096
     blk0 = G.BlockWeights(*([256] * 11 + [0]))
     assert L.gpt2_block_forward(ctypes.byref(d), ctypes.byref(blk0), 256, 256, 2, 64, 256, 1 << 30, None) == 1
     blocks = (G.BlockWeights * 2)(blk, blk)
