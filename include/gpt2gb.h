@@ -60,7 +60,7 @@ typedef struct CUstream_st *gpt2_stream_t;
 typedef enum {
   GPT2_OK = 0,
   GPT2_ERR_ARG = 1,          /* null pointer, negative size, inconsistent dims */
-  GPT2_ERR_UNSUPPORTED = 2,  /* a shape or type combination this build does not run */
+  GPT2_ERR_UNSUPPORTED = 2,  /* a shape or type combination the library does not run */
   GPT2_ERR_WORKSPACE = 3,    /* workspace smaller than gpt2_*_workspace_bytes() */
   GPT2_ERR_CUDA = 4,         /* a CUDA runtime call or a kernel launch failed */
   GPT2_ERR_TIMEOUT = 5,      /* device side: a bounded wait ran out */

@@ -1,6 +1,6 @@
 """Block, whole-forward and decode-step parity on the GPU against the oracle.
 
-Gates (stated by the task's acceptance criteria, restated here):
+Gates (the accuracy targets of this path, restated here):
 * F32 path, one block: max relative error <= 1e-4 on the hidden state, with
   the error measured as max_i |g - r| / max(|r_i|, rms(r)).
 * BF16 path, logits: relative L2 <= 1e-2, and every argmax that differs
