@@ -27,6 +27,12 @@ with random-init weights of the GPT-2 small architecture.
   (whole sequences of the same batch, until about 10 s of work).
 * decode: the KV-cache decode step of the same model at B=64 with 1023
   cached positions, 64 greedy steps, as achieved HBM GB/s.
+* layernorm_micro: LayerNorm alone (8192 rows, fp32 in, bf16 out, D = 768,
+  1024, 1600) against the measured HBM bandwidth, inputs rotated over more
+  than the L2.
+* larger_forwards: the GPT-2 medium (B=16) and XL (B=4) forwards at T=1024,
+  tokens/s and the end-to-end fraction of the sustained bf16 peak (weights
+  drawn on the device).  Both are left out with --no-decode.
 * --impl reference: the oracle alone, timed as the reference arm.
 Multi-GPU (torchrun): each rank runs an independent replica on its own GPU
 (the forward has no exchange step); value sums the tokens of all ranks over
@@ -36,6 +42,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -337,6 +344,120 @@ def _decode_measure(G, torch, steps=64):
     }
 
 
+def _device_model(G, torch, dims, seed):
+    """Random-init weights of `dims` drawn on the device (seeded, the recipe's
+    distributions: W ~ N(0, 0.02), c_proj weights N(0, 0.02 / sqrt(2 L)),
+    biases N(0, 0.01), LN gamma 1 + N(0, 0.02), beta N(0, 0.02)), in bf16.
+    For timing only: drawing a 1.5 B-parameter model on the host would take
+    longer than the measurement."""
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    D, F, L = dims.d_model, dims.d_ff, dims.n_layer
+
+    def n(shape, std, mean=0.0):
+        return (torch.randn(*shape, device="cuda", generator=g) * std + mean).to(torch.bfloat16)
+
+    proj = 0.02 / math.sqrt(2 * L)
+    p = {"wte": n((dims.vocab, D), 0.02), "wpe": n((dims.n_pos, D), 0.02), "blocks": []}
+    for _ in range(L):
+        p["blocks"].append({"ln1_g": n((D,), 0.02, 1.0), "ln1_b": n((D,), 0.02), "w_qkv": n((D, 3 * D), 0.02),
+                            "b_qkv": n((3 * D,), 0.01), "w_o": n((D, D), proj), "b_o": n((D,), 0.01),
+                            "ln2_g": n((D,), 0.02, 1.0), "ln2_b": n((D,), 0.02), "w_fc": n((D, F), 0.02),
+                            "b_fc": n((F,), 0.01), "w_proj": n((F, D), proj), "b_proj": n((D,), 0.01)})
+    p["lnf_g"] = n((D,), 0.02, 1.0)
+    p["lnf_b"] = n((D,), 0.02)
+    return p
+
+
+def _forward_flops(dims, B, T):
+    """Algorithmic flops of one forward: the GEMMs (2 M N K) and causal
+    attention over the j <= i pairs only (q.k and p.v: 4 hd per pair)."""
+    M, D, F, H = B * T, dims.d_model, dims.d_ff, dims.n_head
+    gemm = dims.n_layer * 2.0 * M * (D * 3 * D + D * D + D * F + F * D) + 2.0 * M * dims.vocab * D
+    attn = dims.n_layer * 4.0 * 64 * B * H * T * (T + 1) / 2
+    return gemm + attn
+
+
+def _larger_forwards(G, torch, peaks, steps=5):
+    """GPT-2 medium (B=16) and XL (B=4) forwards at T=1024, bf16, fp32 logits:
+    tokens/s and the end-to-end fraction of the sustained bf16 peak, device
+    weights (see _device_model), inputs resident, event-timed."""
+    import synth
+    out = {}
+    for name, dims, B, seed in (("gpt2_medium_fwd_b16_t1024", synth.GPT2_MEDIUM, 16, 1236),
+                                ("gpt2_xl_fwd_b4_t1024", synth.GPT2_XL, 4, 1237)):
+        try:
+            T = 1024
+            dev = _device_model(G, torch, dims, seed)
+            mw, keep = G.model_weights(dev)
+            cd = G.make_dims(dims.n_layer, dims.d_model, dims.n_head, dims.d_ff, dims.vocab, dims.n_pos, dims.eps,
+                             G.BF16)
+            gen = torch.Generator(device="cuda").manual_seed(seed)
+            tokens = torch.randint(0, dims.vocab, (B, T), device="cuda", dtype=torch.int32, generator=gen)
+            ld = (dims.vocab + 7) // 8 * 8
+            logits = torch.empty(B, T, ld, device="cuda", dtype=torch.float32)
+            wsb = G.gpt2_workspace_bytes(cd, B, T)
+            ws = torch.empty(wsb, device="cuda", dtype=torch.uint8)
+            stream = torch.cuda.current_stream()
+            for _ in range(3):
+                G.gpt2_forward_logits(cd, mw, tokens, logits, ld, G.F32, B, T, ws, wsb, stream)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                G.gpt2_forward_logits(cd, mw, tokens, logits, ld, G.F32, B, T, ws, wsb, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            st, site = G.gpt2_last_error()
+            ms = e0.elapsed_time(e1) / steps
+            tf = _forward_flops(dims, B, T) / (ms / 1e3) / 1e12
+            out[name] = {"tokens_per_s": B * T / (ms / 1e3), "ms_per_step": ms, "steps": steps,
+                         "end_to_end_tflops": tf, "end_to_end_frac": tf / peaks["bf16_tflops_sustained"],
+                         "finite": bool(torch.isfinite(logits[0, -1, :dims.vocab]).all().item()),
+                         "device_status": st}
+            del keep, dev, logits, ws
+            torch.cuda.empty_cache()
+        except Exception as exc:  # reported, not fatal: the headline run is already done
+            out[name] = {"error": f"{type(exc).__name__}: {exc}"}
+    return out
+
+
+def _layernorm_micro(G, torch, peaks, reps=20):
+    """LayerNorm alone at M=8192 rows, fp32 in, bf16 out, D = 768/1024/1600:
+    algorithmic bytes (6 per element) / time, against the measured HBM
+    bandwidth.  The launches rotate over enough input/output buffers that
+    their total exceeds the L2, so every launch reads from HBM."""
+    out = {}
+    rows = 8192
+    for D in (768, 1024, 1600):
+        try:
+            per = rows * D * 6
+            nbuf = max(2, -(-256 * 2 ** 20 // per))
+            gen = torch.Generator(device="cuda").manual_seed(D)
+            xs = [torch.randn(rows, D, device="cuda", generator=gen) for _ in range(nbuf)]
+            ys = [torch.empty(rows, D, device="cuda", dtype=torch.bfloat16) for _ in range(nbuf)]
+            g = (1 + 0.02 * torch.randn(D, device="cuda", generator=gen)).to(torch.bfloat16)
+            b = (0.02 * torch.randn(D, device="cuda", generator=gen)).to(torch.bfloat16)
+            stream = torch.cuda.current_stream()
+            for i in range(nbuf):
+                G.gpt2_layernorm(xs[i], g, b, ys[i], rows, D, 1e-5, G.F32, G.BF16, stream)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for r in range(reps):
+                i = r % nbuf
+                G.gpt2_layernorm(xs[i], g, b, ys[i], rows, D, 1e-5, G.F32, G.BF16, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / reps
+            gbs = per / (us * 1e-6) / 1e9
+            out[f"d{D}"] = {"us_per_launch": us, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"], "buffers": nbuf}
+            del xs, ys
+            torch.cuda.empty_cache()
+        except Exception as exc:
+            out[f"d{D}"] = {"error": f"{type(exc).__name__}: {exc}"}
+    return out
+
+
 def _gemm_replay(G, torch, dims, dev, logits, ld, M, stream, reps=5):
     """Time the forward's GEMM launches back to back (one event pair per
     replay of all of them), on operands of the forward's shapes: per layer
@@ -572,6 +693,9 @@ def run_ours(args):
         dec = _decode_measure(G, torch)
         dec["frac_of_hbm"] = dec["achieved_gbs"] / peaks["hbm_gbs"]
         out["decode"] = dec
+    if rank == 0 and not args.no_decode:
+        out["layernorm_micro"] = _layernorm_micro(G, torch, peaks)
+        out["larger_forwards"] = _larger_forwards(G, torch, peaks)
     if rank == 0 and world == 1 and not args.no_cpu:
         toks, secs, seqs = _cpu_oracle_time(inp, budget_s=10.0)
         out["cpu_baseline"] = {"value": toks / secs, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
