@@ -32,7 +32,10 @@ with random-init weights of the GPT-2 small architecture.
   than the L2.
 * larger_forwards: the GPT-2 medium (B=16) and XL (B=4) forwards at T=1024,
   tokens/s and the end-to-end fraction of the sustained bf16 peak (weights
-  drawn on the device).  Both are left out with --no-decode.
+  drawn on the device).
+* block_backward_f32: one GPT-2 small block's backward on the fp32 path at
+  B=8, T=1024 (time, TFLOP/s against the fp32 CUDA-core peak).  These three
+  are left out with --no-decode.
 * --impl reference: the oracle alone, timed as the reference arm.
 Multi-GPU (torchrun): each rank runs an independent replica on its own GPU
 (the forward has no exchange step); value sums the tokens of all ranks over
@@ -421,6 +424,65 @@ def _larger_forwards(G, torch, peaks, steps=5):
     return out
 
 
+def _block_backward_measure(G, torch, reps=3):
+    """One GPT-2 small block's backward on the fp32 path (gpt2_block_backward:
+    forward recomputed, all gradients) at B=8, T=1024: time per call and
+    algorithmic TFLOP/s against the fp32 CUDA-core peak (152 SMs x 128 fp32
+    lanes x 2 flop x 2.07 GHz = 80.5 TFLOP/s; the path runs on CUDA cores).
+    Algorithmic flops: the forward recomputed once (GEMMs 2 M N K,
+    attention 4 hd per visible pair) and the backward (two GEMMs per forward
+    GEMM, attention 8 hd per visible pair)."""
+    import synth
+    try:
+        dims = synth.GPT2_SMALL
+        B, T = 8, 1024
+        D, F, H = dims.d_model, dims.d_ff, dims.n_head
+        M = B * T
+        g = torch.Generator(device="cuda").manual_seed(77)
+
+        def n(shape, std, mean=0.0):
+            return torch.randn(*shape, device="cuda", generator=g) * std + mean
+
+        proj = 0.02 / math.sqrt(2 * dims.n_layer)
+        w = {"ln1_g": n((D,), 0.02, 1.0), "ln1_b": n((D,), 0.02), "w_qkv": n((D, 3 * D), 0.02),
+             "b_qkv": n((3 * D,), 0.01), "w_o": n((D, D), proj), "b_o": n((D,), 0.01), "ln2_g": n((D,), 0.02, 1.0),
+             "ln2_b": n((D,), 0.02), "w_fc": n((D, F), 0.02), "b_fc": n((F,), 0.01), "w_proj": n((F, D), proj),
+             "b_proj": n((D,), 0.01)}
+        grads = {k: torch.empty_like(v) for k, v in w.items()}
+        x = n((B, T, D), 1.0)
+        dy = n((B, T, D), 1.0)
+        dx = torch.empty_like(x)
+        cd = G.make_dims(1, D, H, F, dims.vocab, dims.n_pos, dims.eps, G.F32)
+        wsb = G.gpt2_block_backward_workspace_bytes(cd, B, T)
+        ws = torch.empty(wsb, device="cuda", dtype=torch.uint8)
+        stream = torch.cuda.current_stream()
+        bw, bg = G.block_weights(w), G.block_grads(grads)
+        G.gpt2_block_backward(cd, bw, 0, x, dy, dx, bg, B, T, ws, wsb, stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            G.gpt2_block_backward(cd, bw, 0, x, dy, dx, bg, B, T, ws, wsb, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        st, site = G.gpt2_last_error()
+        ms = e0.elapsed_time(e1) / reps
+        gemm = 2.0 * M * (D * 3 * D + D * D + 2 * D * F)
+        pairs = B * H * T * (T + 1) / 2
+        flops = 3 * gemm + (4 + 8) * 64 * pairs
+        peak = 152 * 128 * 2 * 2.07e9 / 1e12
+        tf = flops / (ms / 1e3) / 1e12
+        out = {"workload": "gpt2_small_block_bwd_f32_b8_t1024", "ms_per_call": ms, "tflops": tf,
+               "roofline": {"bound": "alu", "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                            "peak_source": "fp32 lanes x 2 x max SM clock (unit counts)"},
+               "finite": bool(torch.isfinite(dx).all().item()), "device_status": st}
+        del ws, grads, w
+        torch.cuda.empty_cache()
+        return out
+    except Exception as exc:  # reported, not fatal
+        return {"error": f"{type(exc).__name__}: {exc}"}
+
+
 def _layernorm_micro(G, torch, peaks, reps=20):
     """LayerNorm alone at M=8192 rows, fp32 in, bf16 out, D = 768/1024/1600:
     algorithmic bytes (6 per element) / time, against the measured HBM
@@ -696,6 +758,7 @@ def run_ours(args):
     if rank == 0 and not args.no_decode:
         out["layernorm_micro"] = _layernorm_micro(G, torch, peaks)
         out["larger_forwards"] = _larger_forwards(G, torch, peaks)
+        out["block_backward_f32"] = _block_backward_measure(G, torch)
     if rank == 0 and world == 1 and not args.no_cpu:
         toks, secs, seqs = _cpu_oracle_time(inp, budget_s=10.0)
         out["cpu_baseline"] = {"value": toks / secs, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
