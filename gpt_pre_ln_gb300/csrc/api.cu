@@ -700,7 +700,7 @@ int gpt2_block_backward(const gpt2_dims* dims, const gpt2_block_weights* w, int 
   GPT2_TRY(check_block_ptrs(w));
   if (dims->dtype != GPT2_F32) return GPT2_ERR_UNSUPPORTED;
   if (layer < 0 || B < 0 || T < 0 || static_cast<int64_t>(B) * T > INT_MAX) return GPT2_ERR_ARG;
-  if (T > 4096) return GPT2_ERR_UNSUPPORTED;
+  if (T > 4096 || B > 65535) return GPT2_ERR_UNSUPPORTED;  // the attention kernels' grid holds B in y
   if (B == 0 || T == 0) return GPT2_OK;
   if (!grads || !x_in || !dx_out || !dx_in) return GPT2_ERR_ARG;
   const void* gs[12] = {grads->ln1_g, grads->ln1_b, grads->w_qkv, grads->b_qkv, grads->w_o,    grads->b_o,

@@ -284,7 +284,8 @@ size_t gpt2_block_backward_workspace_bytes(const gpt2_dims *dims, int B, int T);
  * to the input) and every weight gradient into `grads`.  The forward
  * intermediates are recomputed into the workspace.  `layer` as in
  * gpt2_block_forward_layer (the index of the block in its stack).
- *   dims->dtype must be GPT2_F32 (else GPT2_ERR_UNSUPPORTED); T <= 4096;
+ *   dims->dtype must be GPT2_F32 (else GPT2_ERR_UNSUPPORTED); T <= 4096 and
+ *   B <= 65535;
  *   dx_in must not overlap x_in or dx_out; ws of
  *   gpt2_block_backward_workspace_bytes(dims, B, T) bytes, 256-byte
  *   aligned.  fp32 CUDA cores throughout; the sums over rows run in a

@@ -126,6 +126,8 @@ def test_argument_checks_before_any_launch(L):
                                  ctypes.byref(grads), 2, 64, 256, wsb, None) == 1  # dx_in overlaps x_in
     assert L.gpt2_block_backward(ctypes.byref(d32b), ctypes.byref(blk), 0, 256, 1 << 20, 1 << 24,
                                  ctypes.byref(grads), 1, 4097, 256, 1 << 40, None) == 2  # T > 4096
+    assert L.gpt2_block_backward(ctypes.byref(d32b), ctypes.byref(blk), 0, 256, 1 << 20, 1 << 24,
+                                 ctypes.byref(grads), 65536, 1, 256, 1 << 40, None) == 2  # B > 65535
     blk0 = G.BlockWeights(*([256] * 11 + [0]))
     assert L.gpt2_block_forward(ctypes.byref(d), ctypes.byref(blk0), 256, 256, 2, 64, 256, 1 << 30, None) == 1
     blocks = (G.BlockWeights * 2)(blk, blk)
