@@ -55,14 +55,6 @@ constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kWarpStageBytes = 4096;   // 32 rows x 128 bytes per epilogue warp
 constexpr int kSmemLimit = 232448;      // 227 KB opt-in maximum per block
-#ifndef GPT2_GEMM_1SM_CLUSTER
-#define GPT2_GEMM_1SM_CLUSTER 1
-#endif
-// 1 or 2.  Clusters of two cut each SM's operand bytes per k-block by a
-// third on the D-wide GEMMs, but measured slightly slower on the GPT-2 small
-// forward (the pairs' lock step and fewer resident CTAs), so one is the
-// default; 2 builds and passes the same tests.
-constexpr int kOneSmCluster = GPT2_GEMM_1SM_CLUSTER;
 
 enum Epi : int { EPI_NONE = 0, EPI_BIAS = 1, EPI_GELU = 2, EPI_RES = 3, EPI_LSE = 4 };
 
@@ -492,13 +484,8 @@ __device__ __forceinline__ void drain_loads(long long issued, FullBar full_bar, 
 }
 
 // ------------------------------------------------------------------ 1 SM
-// Launched alone (a cluster of one) or as clusters of C = 2 CTAs that work
-// on vertically adjacent tiles of the same column block: each CTA loads half
-// of the k-rows (or columns) of the shared W tile and multicasts it into both
-// CTAs' shared memory, which cuts the operand bytes each SM takes in per
-// k-block from A + W to A + W/2.  A stage is refilled only when the MMAs of
-// both CTAs have read it (each MMA commit arrives on the empty barriers of
-// both), and neither CTA leaves before the other is done.
+// One CTA per 128 x BN tile, persistent over the tiles; every CTA loads its
+// own A and W tiles (no operand is shared between CTAs).
 template <int BN, bool B_MN, int EPI, typename OutT, typename T16>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_1sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -525,14 +512,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int M = ea.M, N = ea.N;
-  const int C = static_cast<int>(cluster_nctarank());  // 1 or 2
-  const int rank = static_cast<int>(cluster_ctarank());
-  const uint16_t cmask = static_cast<uint16_t>((1u << C) - 1u);
   const int m_tiles = (M + kBM - 1) / kBM;
   const int n_tiles = (N + BN - 1) / BN;
-  const int m_groups = (m_tiles + C - 1) / C;  // C vertically adjacent tiles per cluster tile
-  const int num_tiles = m_groups * n_tiles;     // cluster tiles
-  const int tile0 = blockIdx.x / C, tile_step = gridDim.x / C;
+  const int num_tiles = m_tiles * n_tiles;
+  const int tile0 = blockIdx.x, tile_step = gridDim.x;
   const int k_blocks = K / kBK;
 
   if (threadIdx.x == 0) {
@@ -541,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmY);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), C);  // the MMA commits of every CTA of the cluster
+      mbar_init(empty_bar(s), 1);  // the MMA commit that has read the stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -571,8 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       long long issued = 0;
       bool ok = true;
       for (int tile = tile0; tile < num_tiles && ok; tile += tile_step) {
-        const int m0 = ((tile % m_groups) * C + rank) * kBM;
-        const int n0 = (tile / m_groups) * BN;
+        const int m0 = (tile % m_tiles) * kBM;
+        const int n0 = (tile / m_tiles) * BN;
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1)) {
             record_error(err, kErrTimeout, kSiteGemmProducer);
@@ -582,27 +565,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
           tma_load_2d(smem_u32(sA + stage * Cfg::A_BYTES), &tmA, full_bar(stage), kb * kBK, m0);
           const uint32_t b_dst = smem_u32(sB + stage * Cfg::B_BYTES);
-          if (C == 1) {
-            if constexpr (B_MN) {
-              // W [K, N]: one box of 64 N-columns x 64 K-rows per 64-wide atom
+          if constexpr (B_MN) {
+            // W [K, N]: one box of 64 N-columns x 64 K-rows per 64-wide atom
 #pragma unroll
-              for (int j = 0; j < BN / 64; ++j)
-                tma_load_2d(b_dst + j * (kBK * 128), &tmB, full_bar(stage), n0 + j * 64, kb * kBK);
-            } else {
-              tma_load_2d(b_dst, &tmB, full_bar(stage), kb * kBK, n0);
-            }
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(b_dst + j * (kBK * 128), &tmB, full_bar(stage), n0 + j * 64, kb * kBK);
           } else {
-            // this CTA's half of W, into both CTAs: k-rows rank*32.. of each
-            // [64 x 64] atom (W [K, N]), or rows rank*BN/2.. (W [N, K])
-            if constexpr (B_MN) {
-#pragma unroll
-              for (int j = 0; j < BN / 64; ++j)
-                tma_load_2d_multicast(b_dst + j * (kBK * 128) + rank * (kBK / 2) * 128, &tmB, full_bar(stage),
-                                      n0 + j * 64, kb * kBK + rank * (kBK / 2), cmask);
-            } else {
-              tma_load_2d_multicast(b_dst + rank * (BN / 2) * 128, &tmB, full_bar(stage), kb * kBK,
-                                    n0 + rank * (BN / 2), cmask);
-            }
+            tma_load_2d(b_dst, &tmB, full_bar(stage), kb * kBK, n0);
           }
           ++issued;
           if (++stage == STAGES) {
@@ -657,10 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_bf16(d_tmem, adesc, bdesc, idesc, (EPI == EPI_RES || (kb | k) != 0) ? 1u : 0u);
             any = true;
           }
-          if (C == 1)
-            umma_commit(empty_bar(stage));
-          else
-            umma_commit_multicast(empty_bar(stage), cmask);
+          umma_commit(empty_bar(stage));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -679,15 +645,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     epilogue_role<BN, EPI, OutT, T16, false>(ea, &tmY, warp, lane, smem_u32(sOut), smem_u32(sBias), bias_full_bar(0),
                                          bias_full_bar(1), bias_empty_bar(0), bias_empty_bar(1), tmem_base,
                                          tfull_bar(0), tfull_bar(1),
-                                         tempty_bar(0), tempty_bar(1), tile0, tile_step, num_tiles, m_groups, C * kBM,
-                                         rank * kBM);
+                                         tempty_bar(0), tempty_bar(1), tile0, tile_step, num_tiles, m_tiles, kBM, 0);
   }
 
   tc_fence_before();
   __syncthreads();
-  // no CTA leaves while the other may still multicast into its shared memory
-  // or arrive on its barriers
-  if (C > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
@@ -918,43 +880,14 @@ cudaError_t run_1sm(const T16* x, const T16* w, const EpiArgs<OutT, T16>& ea, in
   if (e != cudaSuccess) return e;
   const int M = ea.M, N = ea.N;
   const int m_tiles = (M + kBM - 1) / kBM;
-  // clusters of kOneSmCluster (W shared by multicast) when there are two row tiles
-  const int C = m_tiles >= 2 ? kOneSmCluster : 1;
   CUtensorMap ta, tb;
   if (!make_map(&ta, dt, x, K, M, kBM)) return cudaErrorInvalidValue;
-  if (!(B_MN ? make_map(&tb, dt, w, N, K, kBK / C) : make_map(&tb, dt, w, K, N, BN / C)))
-    return cudaErrorInvalidValue;
-  const int cluster_tiles = ((m_tiles + C - 1) / C) * ((N + BN - 1) / BN);
-  int max_clusters = num_sms() / C;
-  if (C > 1) {
-    // clusters resident at once (the two CTAs need two SMs of one GPC)
-    static int known[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64) {
-      if (known[dev] == 0) {
-        cudaLaunchConfig_t qc = {};
-        qc.gridDim = dim3(C * (num_sms() / C), 1, 1);
-        qc.blockDim = dim3(kThreads, 1, 1);
-        qc.dynamicSmemBytes = Cfg::SMEM_BYTES;
-        cudaLaunchAttribute qa;
-        qa.id = cudaLaunchAttributeClusterDimension;
-        qa.val.clusterDim.x = C;
-        qa.val.clusterDim.y = 1;
-        qa.val.clusterDim.z = 1;
-        qc.attrs = &qa;
-        qc.numAttrs = 1;
-        int n = 0;
-        known[dev] = (cudaOccupancyMaxActiveClusters(&n, kern, &qc) == cudaSuccess && n > 0) ? n : num_sms() / C;
-      }
-      max_clusters = std::min(known[dev], num_sms() / C);
-    }
-  }
-  const int clusters = cluster_tiles < max_clusters ? cluster_tiles : max_clusters;
+  if (!(B_MN ? make_map(&tb, dt, w, N, K, kBK) : make_map(&tb, dt, w, K, N, BN))) return cudaErrorInvalidValue;
+  const int tiles = m_tiles * ((N + BN - 1) / BN);
+  const int ctas = tiles < num_sms() ? tiles : num_sms();
   CUtensorMap ty = ta;  // EPI_LSE stores no tile (a valid map, never used)
   if (EPI != EPI_LSE && !make_out_map(&ty, ea)) return cudaErrorInvalidValue;
-  return launch_pdl(kern, C * clusters, kThreads, Cfg::SMEM_BYTES, stream, static_cast<unsigned>(C), ta, tb, ty, ea,
-                    K);
+  return launch_pdl(kern, ctas, kThreads, Cfg::SMEM_BYTES, stream, 0, ta, tb, ty, ea, K);
 }
 
 template <bool B_MN, int EPI, typename OutT, typename T16>
