@@ -554,6 +554,31 @@ int block_backward_f32(const gpt2_dims* d, const gpt2_block_weights* w, int laye
 
 }  // namespace
 
+namespace gpt2 {
+
+cudaError_t launch_mlp(gpt2_dtype dt, const void* x, const void* w_fc, const void* b_fc, const void* w_proj,
+                       const void* b_proj, const float* residual, float* out, int64_t M, int D, int F, void* hidden,
+                       cudaStream_t s) {
+  cudaError_t e = linear(dt, x, w_fc, b_fc, nullptr, hidden, M, F, D, F, false, GPT2_EPI_BIAS_GELU, dt, s);
+  if (e != cudaSuccess) return e;
+  return linear(dt, hidden, w_proj, b_proj, residual, out, M, D, F, D, false,
+                residual ? GPT2_EPI_BIAS_RESIDUAL : GPT2_EPI_BIAS, GPT2_F32, s);
+}
+
+// Failure-detection self-test: one thread waits, through the bounded wait
+// every kernel of the library uses, on an mbarrier that nothing arrives on.
+// When `limit_ns` has passed it records GPT2_ERR_TIMEOUT at its own site and
+// returns, as a kernel whose producer never delivered would.
+__global__ void selftest_wait_kernel(unsigned long long limit_ns, unsigned* err) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_barrier_init();
+  if (!mbar_wait_for(b, 0, limit_ns)) record_error(err, kErrTimeout, kSiteSelfTestWait);
+}
+
+}  // namespace gpt2
+
 extern "C" {
 
 int gpt2_abi_version(void) { return kAbiVersion; }
@@ -582,6 +607,12 @@ int gpt2_last_error(int* site) {
   }
   if (site) *site = static_cast<int>(v >> 8);
   return static_cast<int>(v & 0xFFu);
+}
+
+int gpt2_selftest_wait_timeout(uint64_t limit_ns, gpt2_stream_t stream) {
+  if (limit_ns == 0 || limit_ns > kWaitLimitNs) return GPT2_ERR_ARG;
+  selftest_wait_kernel<<<1, 1, 0, cs(stream)>>>(static_cast<unsigned long long>(limit_ns), device_error_word());
+  return cuda_status(cudaGetLastError());
 }
 
 int gpt2_layernorm(const void* x, const void* gamma, const void* beta, void* y, int64_t rows, int D, float eps,
@@ -652,13 +683,7 @@ int gpt2_mlp(const void* x, const void* w_fc, const void* b_fc, const void* w_pr
   if (residual && !aligned16(residual)) return GPT2_ERR_ARG;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return GPT2_ERR_ARG;
   if (ws_bytes < gpt2_mlp_workspace_bytes(M, F, dtype)) return GPT2_ERR_WORKSPACE;
-  cudaStream_t s = cs(stream);
-  GPT2_CUDA(linear(dtype, x, w_fc, b_fc, nullptr, ws, M, F, D, F, false, GPT2_EPI_BIAS_GELU, dtype, s));
-  if (residual)
-    GPT2_CUDA(linear(dtype, ws, w_proj, b_proj, residual, out, M, D, F, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32, s));
-  else
-    GPT2_CUDA(linear(dtype, ws, w_proj, b_proj, nullptr, out, M, D, F, D, false, GPT2_EPI_BIAS, GPT2_F32, s));
-  return GPT2_OK;
+  return cuda_status(launch_mlp(dtype, x, w_fc, b_fc, w_proj, b_proj, residual, out, M, D, F, ws, cs(stream)));
 }
 
 size_t gpt2_workspace_bytes(const gpt2_dims* dims, int B, int T) {

@@ -86,6 +86,14 @@ cudaError_t launch_gemm_rows_16(gpt2_dtype dt, const void* x, const void* w, con
                                 void* y, int64_t M, int N, int K, int64_t ldy, bool w_out_in, int epilogue,
                                 gpt2_dtype y_t, cudaStream_t stream, float2* argmax_cand = nullptr);
 
+// The MLP sublayer of gpt2_mlp: hidden = gelu_new(x W_fc + b_fc) (type dt,
+// [M, F], caller memory), then out = residual + hidden W_proj + b_proj (fp32;
+// no residual when it is null).  Both GEMMs go through the library's linear
+// layer (per-kernel profiling included).
+cudaError_t launch_mlp(gpt2_dtype dt, const void* x, const void* w_fc, const void* b_fc, const void* w_proj,
+                       const void* b_proj, const float* residual, float* out, int64_t M, int D, int F, void* hidden,
+                       cudaStream_t s);
+
 // fp32 CUDA-core GEMM with the same epilogues.
 cudaError_t launch_gemm_f32(const float* x, const float* w, const float* bias, const float* residual, float* y,
                             int64_t M, int N, int K, int64_t ldy, bool w_out_in, int epilogue, cudaStream_t stream);

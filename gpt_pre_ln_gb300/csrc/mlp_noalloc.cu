@@ -20,6 +20,13 @@
 // Every call on a device shares the one array: calls whose GPU work can
 // overlap (different streams without ordering between them) race on it and
 // produce wrong results; calls ordered on one stream are safe.
+//
+// The cached address belongs to the CUDA context it was looked up in.  A
+// caller that resets a device (cudaDeviceReset) and keeps using the library
+// in the same process gets a new context whose copy of the array may sit
+// elsewhere; the cache is not refreshed, so such a caller must not use this
+// entry point after the reset.
+#include <climits>
 #include <mutex>
 
 #include "common.cuh"
@@ -65,7 +72,7 @@ int gpt2_mlp_noalloc(const void* x, const void* w_fc, const void* b_fc, const vo
                      const float* residual, float* out, int64_t M, int D, int F, gpt2_dtype dtype,
                      gpt2_stream_t stream) {
   if (dtype != GPT2_F32 && dtype != GPT2_BF16 && dtype != GPT2_F16) return GPT2_ERR_ARG;
-  if (M < 0 || D <= 0 || F <= 0) return GPT2_ERR_ARG;
+  if (M < 0 || M > INT_MAX || D <= 0 || F <= 0) return GPT2_ERR_ARG;
   if (D % 64 != 0 || F % 64 != 0) return GPT2_ERR_UNSUPPORTED;
   const size_t esz = dtype == GPT2_F32 ? 4 : 2;
   if (static_cast<size_t>(M) * static_cast<size_t>(F) * esz > kMlpScratchBytes) return GPT2_ERR_WORKSPACE;
@@ -76,22 +83,9 @@ int gpt2_mlp_noalloc(const void* x, const void* w_fc, const void* b_fc, const vo
   if (residual && !aligned16(residual)) return GPT2_ERR_ARG;
   void* g = scratch_address();
   if (!g) return GPT2_ERR_CUDA;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (dtype != GPT2_F32) {
-    e = launch_gemm_16(dtype, x, w_fc, b_fc, nullptr, g, M, F, D, F, false, GPT2_EPI_BIAS_GELU, dtype, s);
-    if (e != cudaSuccess) return GPT2_ERR_CUDA;
-    e = launch_gemm_16(dtype, g, w_proj, b_proj, residual, out, M, D, F, D, false,
-                       residual ? GPT2_EPI_BIAS_RESIDUAL : GPT2_EPI_BIAS, GPT2_F32, s);
-  } else {
-    e = launch_gemm_f32(static_cast<const float*>(x), static_cast<const float*>(w_fc),
-                        static_cast<const float*>(b_fc), nullptr, static_cast<float*>(g), M, F, D, F, false,
-                        GPT2_EPI_BIAS_GELU, s);
-    if (e != cudaSuccess) return GPT2_ERR_CUDA;
-    e = launch_gemm_f32(static_cast<const float*>(g), static_cast<const float*>(w_proj),
-                        static_cast<const float*>(b_proj), residual, out, M, D, F, D, false,
-                        residual ? GPT2_EPI_BIAS_RESIDUAL : GPT2_EPI_BIAS, s);
-  }
+  // the same launches as gpt2_mlp, with the scratch array as the hidden buffer
+  const cudaError_t e = launch_mlp(dtype, x, w_fc, b_fc, w_proj, b_proj, residual, out, M, D, F, g,
+                                   reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
