@@ -17,6 +17,7 @@ import pytest
 
 import oracle as O
 import synth
+from bf16_emulation import EMULATION_AGREE, EMULATION_POSITIONS, SAMPLED_SEQUENCES
 from gpu_util import max_rel_err, rel_l2, rng, to_np, to_t, top1_check
 
 torch = pytest.importorskip("torch")
@@ -117,12 +118,13 @@ def _forward(dims, dtype, params, tokens, logits_t=G.BF16):
 
 # Top-1 agreement reachable by a path that rounds the GEMM inputs (LayerNorm
 # outputs, QKV, probabilities, attention output, MLP hidden) to bf16: an
-# exact float64 computation with only those roundings agrees with the oracle
-# on 98.98% of the 2 x 1024 positions of the GPT-2 small workload (rel L2
+# exact float64 computation with only those roundings (bf16_emulation,
+# recomputed by test_bf16_emulation.py) agrees with the oracle on 2027 of the
+# 2048 positions of the two sampled GPT-2 small sequences (98.975%, rel L2
 # 3.85e-3), because random-init logits have top-1/top-2 gaps down to 1e-4.
 # The bf16 path is held to that flip rate with a 3-sigma binomial allowance
 # for the number of positions checked; every flip must be a near tie.
-BF16_PATH_FLIP_RATE = 1.0 - 0.9898
+BF16_PATH_FLIP_RATE = 1.0 - EMULATION_AGREE / EMULATION_POSITIONS
 
 
 def _min_top1(n):
@@ -192,10 +194,10 @@ def test_forward_logits_gpt2_small_full_size():
     inp = synth.workload_inputs("gpt2_small_fwd_b8_t1024")
     dims, params, tokens = inp["dims"], inp["params"], inp["tokens"]
     logits = _forward(dims, "bf16", params, tokens, G.F32)
-    for b in (0, 7):
-        got = to_np(logits[b:b + 1])
-        ref = O.forward_logits(tokens[b:b + 1], params, dims)
-        _check_logits(got, ref)
+    got = np.concatenate([to_np(logits[b:b + 1]) for b in SAMPLED_SEQUENCES])
+    ref = np.concatenate([O.forward_logits(tokens[b:b + 1], params, dims) for b in SAMPLED_SEQUENCES])
+    # the positions the emulation's agreement was counted on, pooled
+    _check_logits(got, ref)
 
 
 @pytest.mark.parametrize("name,seqs", [("gpt2_medium_fwd_b16_t1024", (15,)), ("gpt2_xl_fwd_b4_t1024", (3,))],
