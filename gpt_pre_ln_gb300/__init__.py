@@ -15,7 +15,7 @@ import os
 __all__ = [
     "GPT2Error", "F32", "BF16", "F16", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_GELU", "EPI_BIAS_RESIDUAL",
     "EPI_BIAS_GELU_EXACT", "SCALE_ATTN_BY_INVERSE_LAYER_IDX", "GELU_EXACT", "W_IN_OUT", "W_OUT_IN", "Dims", "BlockWeights", "ModelWeights", "lib", "library_path", "gpt2_abi_version",
-    "gpt2_status_string", "gpt2_last_error", "gpt2_layernorm", "gpt2_linear", "gpt2_attention_causal",
+    "gpt2_status_string", "gpt2_last_error", "gpt2_selftest_wait_timeout", "gpt2_layernorm", "gpt2_linear", "gpt2_attention_causal",
     "gpt2_attention_causal_scaled", "gpt2_block_forward_layer", "BlockGrads", "block_grads",
     "gpt2_block_backward_workspace_bytes", "gpt2_block_backward",
     "gpt2_mlp_workspace_bytes", "gpt2_mlp", "gpt2_mlp_noalloc", "gpt2_mlp_noalloc_max_scratch_bytes",
@@ -79,6 +79,7 @@ _SIGS = {
     "gpt2_abi_version": (_I32, []),
     "gpt2_status_string": (ctypes.c_char_p, [_I32]),
     "gpt2_last_error": (_I32, [ctypes.POINTER(ctypes.c_int)]),
+    "gpt2_selftest_wait_timeout": (_I32, [ctypes.c_uint64, _VP]),
     "gpt2_layernorm": (_I32, [_VP, _VP, _VP, _VP, _I64, _I32, _F, _I32, _I32, _VP]),
     "gpt2_linear": (_I32, [_VP, _VP, _VP, _VP, _VP, _I64, _I32, _I32, _I64, _I32, _I32, _I32, _I32, _VP]),
     "gpt2_attention_causal": (_I32, [_VP, _VP, _I32, _I32, _I32, _I32, _I32, _VP]),
@@ -164,6 +165,10 @@ def gpt2_last_error():
     site = ctypes.c_int(0)
     st = lib().gpt2_last_error(ctypes.byref(site))
     return st, site.value
+
+
+def gpt2_selftest_wait_timeout(limit_ns, stream=None):
+    _check(lib().gpt2_selftest_wait_timeout(int(limit_ns), _stream(stream)), "gpt2_selftest_wait_timeout")
 
 
 def gpt2_layernorm(x, gamma, beta, y, rows, D, eps, x_t, y_t, stream=None):

@@ -147,6 +147,19 @@ const char *gpt2_status_string(int status);
  * the kernel and the wait that failed (0 when there is none). */
 int gpt2_last_error(int *site);
 
+/* Self-test of the failure detection above; the pages have no counterpart
+ * (they describe no GPU code).  Enqueues one GPU thread that waits, through
+ * the same bounded mbarrier wait every kernel of the library uses, on a
+ * barrier that nothing ever arrives on, with a wait limit of `limit_ns`
+ * nanoseconds of GPU wall time (1 .. 2e9; the library's own kernels use
+ * 2e9) in place of the library's.  When the limit runs out the thread
+ * records GPT2_ERR_TIMEOUT with site 18 in the device error word and the
+ * kernel returns; nothing faults, traps or hangs, and the context stays
+ * usable.  A following gpt2_last_error() returns GPT2_ERR_TIMEOUT and site
+ * 18 (and clears the word).  Returns GPT2_ERR_ARG for a limit outside the
+ * range (nothing enqueued), GPT2_ERR_CUDA if the launch failed. */
+int gpt2_selftest_wait_timeout(uint64_t limit_ns, gpt2_stream_t stream);
+
 /* LayerNorm over the last axis: y = gamma * (x - mean) / sqrt(var + eps) + beta,
  * var the population variance ("Hidden State 如何流过 GPT-2 Block", section
  * "Pre-Norm"; llm.c notes section 3.2: eps added to the variance).
@@ -222,7 +235,10 @@ int gpt2_mlp(const void *x, const void *w_fc, const void *b_fc, const void *w_pr
  *   address (cudaGetSymbolAddress); make that first call outside stream
  *   capture.  All calls on a device share the one array: calls whose GPU
  *   work may overlap (unordered streams) race on it; calls ordered on one
- *   stream are safe.  No part of the array needs clearing between calls. */
+ *   stream are safe.  No part of the array needs clearing between calls.
+ *   The looked-up address is kept for the life of the process: after a
+ *   cudaDeviceReset of a device, do not call this entry point on it again
+ *   in the same process (the new context's array may lie elsewhere). */
 size_t gpt2_mlp_noalloc_max_scratch_bytes(void);
 int gpt2_mlp_noalloc(const void *x, const void *w_fc, const void *b_fc, const void *w_proj, const void *b_proj,
                      const float *residual, float *out, int64_t M, int D, int F, gpt2_dtype dtype,

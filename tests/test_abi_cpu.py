@@ -139,6 +139,8 @@ def test_argument_checks_before_any_launch(L):
     d32 = G.make_dims(2, 768, 12, 3072, 50257, 1024, dtype=G.F32)
     assert L.gpt2_decode_step(ctypes.byref(d32), ctypes.byref(mw), 256, 4, 64, 256, 256, 256, None, 0, 256,
                               1 << 34, None) == 2  # decode is bf16 only
+    assert L.gpt2_selftest_wait_timeout(0, None) == 1  # wait limit outside 1 .. 2e9 ns
+    assert L.gpt2_selftest_wait_timeout(2_000_000_001, None) == 1
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
