@@ -174,13 +174,23 @@ def draw_activations(d: _Draw, B: int, T: int, D: int) -> np.ndarray:
     return round_to(d.rng.standard_normal((B, T, D)), "f32")
 
 
+def kv_cache_slabs(d: _Draw, dims: Dims, B: int, T_fill: int):
+    """The filled slots of the KV cache one (layer, K|V) slab at a time, in
+    draw order: yields (l, kv, slab [B, H, T_fill, head_dim] ~ N(0,1), bf16
+    values).  Lets a caller move a large cache to the device without holding
+    it all on the host."""
+    H, hd = dims.n_head, dims.head_dim
+    for l in range(dims.n_layer):
+        for kv in range(2):
+            yield l, kv, round_to(d.rng.standard_normal((B, H, T_fill, hd)), "bf16")
+
+
 def draw_kv_cache(d: _Draw, dims: Dims, B: int, T_max: int, T_fill: int) -> np.ndarray:
     """KV cache [L, 2, B, H, T_max, head_dim]; slots < T_fill ~ N(0,1) (bf16), rest 0."""
     L, H, hd = dims.n_layer, dims.n_head, dims.head_dim
     cache = np.zeros((L, 2, B, H, T_max, hd), dtype=np.float32)
-    for l in range(L):
-        for kv in range(2):
-            cache[l, kv, :, :, :T_fill, :] = round_to(d.rng.standard_normal((B, H, T_fill, hd)), "bf16")
+    for l, kv, slab in kv_cache_slabs(d, dims, B, T_fill):
+        cache[l, kv, :, :, :T_fill, :] = slab
     return cache
 
 
@@ -209,13 +219,16 @@ def param_shapes(dims: Dims) -> dict:
     return {"wte": (dims.vocab, D), "wpe": (dims.n_pos, D), "block": blk, "lnf_g": (D,), "lnf_b": (D,)}
 
 
-def workload_inputs(name: str, T_override: int | None = None, B_override: int | None = None):
+def workload_inputs(name: str, T_override: int | None = None, B_override: int | None = None,
+                    cache_as_slabs: bool = False):
     """Draw every input of a named workload, in recipe order.
 
     Returns a dict with ``dims``, ``dtype``, ``params`` and either ``x``
     (block workloads) or ``tokens`` (forward / decode workloads); decode
     workloads also get ``cache`` (filled slots ``cache_len``) and
-    ``past_len``.
+    ``past_len``; with ``cache_as_slabs`` the cache comes as the generator
+    of ``kv_cache_slabs`` (``cache_slabs``) instead, to be consumed after
+    everything else has been drawn.
     """
     w = WORKLOADS[name]
     B = B_override or w.B
@@ -235,7 +248,10 @@ def workload_inputs(name: str, T_override: int | None = None, B_override: int | 
         out["tokens"] = draw_tokens(d, B, 1, w.dims.vocab)[:, 0]
         T_max = w.cache_len + w.decode_steps
         out["T_max"] = T_max
-        out["cache"] = draw_kv_cache(d, w.dims, B, T_max, w.cache_len)
+        if cache_as_slabs:
+            out["cache_slabs"] = kv_cache_slabs(d, w.dims, B, w.cache_len)
+        else:
+            out["cache"] = draw_kv_cache(d, w.dims, B, T_max, w.cache_len)
         out["past_len"] = np.full((B,), w.cache_len, dtype=np.int32)
     return out
 
