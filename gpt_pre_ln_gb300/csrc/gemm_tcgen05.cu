@@ -217,15 +217,14 @@ __device__ __forceinline__ void lse_chunk(float (&v)[32], int col0, int N, int l
 // once per tile on the accumulator-empty barrier of the tile's accumulator:
 // locally, or at a cluster address when CLUSTER_ARRIVE (the barrier of the
 // pair's even CTA).
-//   Other epilogues: the arrival comes after the thread's last read of the
-//   tile's accumulator, and means "free for the tile after next".
-//   EPI_RES: the accumulator of a tile starts from residual + bias (fp32),
-//   written into tensor memory by these warps before the tile's MMAs, which
-//   then accumulate on top of it.  Each warp preloads its 32 rows of the
-//   first two tiles up front and, after reading out tile t, those of tile
-//   t + 2 into the same accumulator; the arrival follows each preload.  The
-//   residual loads thus run while the MMAs of the other accumulator do, and
-//   the read-out has no global loads left.
+//   The arrival comes after the thread's last read of the tile's
+//   accumulator, and means "free for the tile after next".
+//   EPI_RES: residual + bias are added at read-out.  A warp loads the
+//   residual of its 32 rows for a chunk with coalesced loads one chunk ahead
+//   of the read-out (the first chunk of a tile before the wait for its
+//   MMAs), and transposes it through its staging area just before the
+//   chunk's output goes there: the loads overlap the MMAs, which never wait
+//   for them.
 template <int BN, int EPI, typename OutT, typename T16, bool CLUSTER_ARRIVE>
 __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const CUtensorMap* tmY, int warp, int lane,
                                               uint32_t stage_base, uint32_t bias_s, uint32_t bias_full0,
@@ -254,72 +253,19 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
       mbar_arrive(tempty);
   };
 
-  // ---- EPI_RES: residual + bias into the accumulator of `tile`
-  // residual chunk (fp32, 32 columns) of rows row0..row0+31: coalesced
-  // loads, 4 rows of 128 B per instruction
-  auto load_res = [&](float4 (&r)[8], int row0, int col0) {
+  // EPI_RES: the residual of a chunk (32 fp32 columns from col0) of this
+  // warp's 32 rows, coalesced: load i of lane L covers row i * 4 + L / 8,
+  // columns 4 (L % 8) .. + 3 (four full 128-byte lines per instruction);
+  // zero outside [M, N) (N is a multiple of 4)
+  auto load_res = [&](float4 (&r)[8], int row0_, int col0) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int rr = i * 4 + (lane >> 3);
+      const int rr = row0_ + i * 4 + (lane >> 3);
       const int cc = col0 + (lane & 7) * 4;
-      r[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (row0 + rr < M && cc < N)
-        r[i] = *reinterpret_cast<const float4*>(a.residual + static_cast<long long>(row0 + rr) * N + cc);
+      r[i] = (rr < M && cc < N) ? __ldg(reinterpret_cast<const float4*>(a.residual + static_cast<long long>(rr) * N + cc))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   };
-  // transpose a chunk through the staging area (row = lane), add the bias
-  // of its columns and store it into tensor memory
-  auto put_res = [&](const float4 (&r)[8], uint32_t t_col, int col0) {
-    staging_free();
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(stage_w + swz(i * 4 + (lane >> 3), lane & 7)),
-                   "f"(r[i].x), "f"(r[i].y), "f"(r[i].z), "f"(r[i].w)
-                   : "memory");
-    __syncwarp();
-    float v[32];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float4 q;
-      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                   : "=f"(q.x), "=f"(q.y), "=f"(q.z), "=f"(q.w)
-                   : "r"(stage_w + swz(lane, j)));
-      v[4 * j] = q.x;
-      v[4 * j + 1] = q.y;
-      v[4 * j + 2] = q.z;
-      v[4 * j + 3] = q.w;
-    }
-    __syncwarp();
-    apply_bias_act<EPI_BIAS, float, T16>(v, a.bias, col0, N);
-    tmem_st_32x32b_x32(t_col, v);
-  };
-  auto preload = [&](int tile, int acc) {
-    const int m0 = (tile % m_units) * unit_rows + row_off;
-    const int n0 = (tile / m_units) * BN;
-    const int row0 = m0 + quad * 32;
-    const int valid_cols = N - n0 < BN ? N - n0 : BN;
-    const int nch = (valid_cols + CW - 1) / CW;
-    const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
-    // two chunks in flight (chunks c and c + 2 of this half), no copies
-    float4 ra[8], rb[8];
-    int c = half;
-    if (c < nch) load_res(ra, row0, n0 + c * CW);
-    while (c < nch) {
-      if (c + 2 < nch) load_res(rb, row0, n0 + (c + 2) * CW);
-      put_res(ra, t_addr + c * CW, n0 + c * CW);
-      c += 2;
-      if (c >= nch) break;
-      if (c + 2 < nch) load_res(ra, row0, n0 + (c + 2) * CW);
-      put_res(rb, t_addr + c * CW, n0 + c * CW);
-      c += 2;
-    }
-    tmem_st_wait();
-    arrive_empty(acc);
-  };
-  if constexpr (EPI == EPI_RES) {
-    if (tile_begin < num_tiles) preload(tile_begin, 0);
-    if (tile_begin + tile_stride < num_tiles) preload(tile_begin + tile_stride, 1);
-  }
 
   int t_local = 0;
   for (int tile = tile_begin; tile < num_tiles; tile += tile_stride, ++t_local) {
@@ -333,7 +279,7 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
     // EPI_BIAS / EPI_GELU: the tile's bias into the shared buffer of this
     // accumulator (loaded by warp 2 while the MMAs run; the buffer is free
     // once all eight warps have released it after its previous tile)
-    constexpr bool kBiasSmem = EPI == EPI_BIAS || EPI == EPI_GELU;
+    constexpr bool kBiasSmem = EPI == EPI_BIAS || EPI == EPI_GELU || EPI == EPI_RES;
     const uint32_t bias_b = bias_s + acc * (BN * 2);
     if constexpr (kBiasSmem) {
       if (warp == 2) {
@@ -367,6 +313,10 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
         if (lane == 0) mbar_arrive(acc ? bias_full1 : bias_full0);
       }
     }
+    float4 res_next[EPI == EPI_RES ? 8 : 1];
+    if constexpr (EPI == EPI_RES) {
+      if (half < nch) load_res(res_next, row0, n0 + half * CW);
+    }
     const bool got = mbar_wait(acc ? tfull1 : tfull0, acc_par);
     if (!__all_sync(0xffffffffu, got)) {
       if (lane == 0) {
@@ -389,7 +339,7 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
     // columns are no longer read (-1: none)
     const int last_c = (nch - 1 - half) >= 0 ? nch - 1 - ((nch - 1 - half) & 1) : -1;
     const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
-    if (EPI != EPI_RES && last_c < 0) arrive_empty(acc);
+    if (last_c < 0) arrive_empty(acc);
     // EPI_LSE: this lane's row, its target column (-1: none) and running
     // log-sum-exp over this half's chunks
     const int row = row0 + lane;
@@ -412,10 +362,34 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[l * 32 + i] = __uint_as_float(raw[l][i]);
       }
-      if (EPI != EPI_RES && c == last_c) arrive_empty(acc);  // this half has read its last columns
+      if (c == last_c) arrive_empty(acc);  // this half has read its last columns
       if constexpr (EPI == EPI_LSE) {
         lse_chunk(v, col0, N, lbl, lse_m, lse_s, a.tgt + row);
         continue;
+      }
+      if constexpr (EPI == EPI_RES) {
+        // this chunk's residual transposed through the staging area (row =
+        // lane), then the next chunk's loads put in flight
+        staging_free();
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(stage_w + swz(i * 4 + (lane >> 3), lane & 7)),
+                       "f"(res_next[i].x), "f"(res_next[i].y), "f"(res_next[i].z), "f"(res_next[i].w)
+                       : "memory");
+        __syncwarp();
+        if (c + 2 < nch) load_res(res_next, row0, n0 + (c + 2) * CW);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float4 q;
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(q.x), "=f"(q.y), "=f"(q.z), "=f"(q.w)
+                       : "r"(stage_w + swz(lane, j)));
+          v[4 * j] += q.x;
+          v[4 * j + 1] += q.y;
+          v[4 * j + 2] += q.z;
+          v[4 * j + 3] += q.w;
+        }
+        __syncwarp();  // every lane has read the staging area before it is rewritten below
       }
       if constexpr (kBiasSmem)
         apply_bias_act_smem<EPI, OutT, T16>(v, bias_b + static_cast<uint32_t>(c * CW * 2), a.gelu_exact != 0);
@@ -459,10 +433,6 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
     if constexpr (EPI == EPI_LSE) {
       // slice (n0 / BN) * 2 + half; lanes write consecutive rows
       if (row < M) a.part[static_cast<long long>((n0 / BN) * 2 + half) * M + row] = make_float2(lse_m, lse_s);
-    }
-    if constexpr (EPI == EPI_RES) {
-      const int next = tile + 2 * tile_stride;  // the next tile on this accumulator
-      if (next < num_tiles) preload(next, acc);
     }
   }
   if (lane == 0) bulk_wait_group<0>();  // this warp's stores are complete
@@ -594,9 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = tile0; tile < num_tiles && ok; tile += tile_step, ++t_local) {
         const int acc = t_local & 1;
         const uint32_t acc_par = (t_local >> 1) & 1;
-        // EPI_RES: wait for this tile's residual preload (every use);
-        // otherwise for the read-out of the tile before last (none at first)
-        if (!mbar_wait(tempty_bar(acc), EPI == EPI_RES ? acc_par : acc_par ^ 1)) {
+        // wait for the read-out of the tile before last (none at first)
+        if (!mbar_wait(tempty_bar(acc), acc_par ^ 1)) {
           record_error(err, kErrTimeout, kSiteGemmMma);
           break;
         }
@@ -623,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               bdesc = sdesc_sw128(b_base + k * 32, 16, 1024);
             }
-            umma_bf16(d_tmem, adesc, bdesc, idesc, (EPI == EPI_RES || (kb | k) != 0) ? 1u : 0u);
+            umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
             any = true;
           }
           umma_commit(empty_bar(stage));
@@ -771,9 +740,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int tile = pair; tile < num_tiles && ok; tile += num_pairs, ++t_local) {
         const int acc = t_local & 1;
         const uint32_t acc_par = (t_local >> 1) & 1;
-        // EPI_RES: wait for this tile's residual preload (every use);
-        // otherwise for the read-out of the tile before last (none at first)
-        if (!mbar_wait(tempty_bar(acc), EPI == EPI_RES ? acc_par : acc_par ^ 1)) {
+        // wait for the read-out of the tile before last (none at first)
+        if (!mbar_wait(tempty_bar(acc), acc_par ^ 1)) {
           record_error(err, kErrTimeout, kSiteGemmMma);
           break;
         }
@@ -797,7 +765,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             } else {
               bdesc = sdesc_sw128(b_base + k * 32, 16, 1024);
             }
-            umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (EPI == EPI_RES || (kb | k) != 0) ? 1u : 0u);
+            umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
             any = true;
           }
           umma_commit_pair_multicast(empty_bar(stage), kBoth);
