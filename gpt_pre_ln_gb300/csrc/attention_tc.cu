@@ -94,8 +94,8 @@ __device__ __forceinline__ int attn_item(int k, int c, int G) {
 
 template <typename T16>
 __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
-    attn_causal_tc(const __grid_constant__ CUtensorMap tm_qkv, T16* __restrict__ out, int B, int T, int H,
-                   float scale_log2, unsigned* err) {
+    attn_causal_tc(const __grid_constant__ CUtensorMap tm_qkv, T16* __restrict__ out, float* __restrict__ lse_out,
+                   int B, int T, int H, float scale_log2, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(smem);          // Q (one item)
@@ -432,6 +432,9 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
       }
       tc_fence_after();
       const float inv = 1.f / l;
+      // the row's log-sum-exp of the scaled scores, in log2 units (for the
+      // backward): log2 sum_j 2^(s_j * scale) = m_run + log2 l
+      if (lse_out && q < T) lse_out[(static_cast<long long>(b) * H + h) * T + q] = m_run + log2f(l);
       T16* orow = out + (static_cast<long long>(b) * T + q) * D + h * kHd;
 #pragma unroll
       for (int c = 0; c < kHd / 32; ++c) {
@@ -466,7 +469,8 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
 }
 
 template <typename T16>
-cudaError_t launch_t(const void* qkv, void* out, int B, int T, int n_head, float score_scale, cudaStream_t stream) {
+cudaError_t launch_t(const void* qkv, void* out, float* lse, int B, int T, int n_head, float score_scale,
+                     cudaStream_t stream) {
   if (B == 0 || T == 0) return cudaSuccess;
   const uint64_t D = static_cast<uint64_t>(n_head) * kHd;
   CUtensorMap map;
@@ -488,15 +492,15 @@ cudaError_t launch_t(const void* qkv, void* out, int B, int T, int n_head, float
   const long long resident = static_cast<long long>(kAttnCtasPerSm) * num_sms();
   const int grid = static_cast<int>(items < resident ? items : resident);
   return launch_pdl(attn_causal_tc<T16>, dim3(grid), kAttnThreads, kSmemBytes, stream, 0, map,
-                    static_cast<T16*>(out), B, T, n_head, 1.4426950408889634f * score_scale, device_error_word());
+                    static_cast<T16*>(out), lse, B, T, n_head, 1.4426950408889634f * score_scale, device_error_word());
 }
 
 }  // namespace
 
 cudaError_t launch_attention_tc(gpt2_dtype dt, const void* qkv, void* out, int B, int T, int n_head, float score_scale,
-                                cudaStream_t stream) {
-  if (dt == GPT2_F16) return launch_t<__half>(qkv, out, B, T, n_head, score_scale, stream);
-  return launch_t<__nv_bfloat16>(qkv, out, B, T, n_head, score_scale, stream);
+                                cudaStream_t stream, float* lse) {
+  if (dt == GPT2_F16) return launch_t<__half>(qkv, out, lse, B, T, n_head, score_scale, stream);
+  return launch_t<__nv_bfloat16>(qkv, out, lse, B, T, n_head, score_scale, stream);
 }
 
 }  // namespace gpt2

@@ -37,6 +37,7 @@ enum ErrSite : unsigned {
   kSiteRowsEpilogue = 16,
   kSiteLossLabel = 17,
   kSiteSelfTestWait = 18,
+  kSiteAttnBwd = 19,
 };
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
