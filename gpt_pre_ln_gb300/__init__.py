@@ -16,8 +16,10 @@ __all__ = [
     "GPT2Error", "F32", "BF16", "F16", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_GELU", "EPI_BIAS_RESIDUAL",
     "EPI_BIAS_GELU_EXACT", "SCALE_ATTN_BY_INVERSE_LAYER_IDX", "GELU_EXACT", "W_IN_OUT", "W_OUT_IN", "Dims", "BlockWeights", "ModelWeights", "lib", "library_path", "gpt2_abi_version",
     "gpt2_status_string", "gpt2_last_error", "gpt2_selftest_wait_timeout", "gpt2_layernorm", "gpt2_linear", "gpt2_attention_causal",
-    "gpt2_attention_causal_scaled", "gpt2_block_forward_layer", "BlockGrads", "block_grads",
-    "gpt2_block_backward_workspace_bytes", "gpt2_block_backward",
+    "gpt2_attention_causal_scaled", "gpt2_attention_causal_lse", "gpt2_attention_backward_workspace_bytes",
+    "gpt2_attention_causal_backward", "gpt2_block_forward_layer", "BlockGrads", "block_grads",
+    "gpt2_block_backward_workspace_bytes", "gpt2_block_backward", "ModelGrads", "model_grads",
+    "gpt2_train_workspace_bytes", "gpt2_forward_backward",
     "gpt2_mlp_workspace_bytes", "gpt2_mlp", "gpt2_mlp_noalloc", "gpt2_mlp_noalloc_max_scratch_bytes",
     "gpt2_workspace_bytes", "gpt2_block_forward", "gpt2_forward_logits", "gpt2_loss_workspace_bytes",
     "gpt2_forward_loss", "gpt2_prefill_workspace_bytes", "gpt2_prefill",
@@ -63,6 +65,11 @@ class BlockGrads(ctypes.Structure):
     _fields_ = [(k, ctypes.c_void_p) for k in _BLOCK_FIELDS]
 
 
+class ModelGrads(ctypes.Structure):
+    _fields_ = [("wte", ctypes.c_void_p), ("wpe", ctypes.c_void_p), ("lnf_g", ctypes.c_void_p),
+                ("lnf_b", ctypes.c_void_p), ("blocks", ctypes.POINTER(BlockGrads))]
+
+
 class ModelWeights(ctypes.Structure):
     _fields_ = [("wte", ctypes.c_void_p), ("wpe", ctypes.c_void_p), ("lnf_g", ctypes.c_void_p),
                 ("lnf_b", ctypes.c_void_p), ("blocks", ctypes.POINTER(BlockWeights))]
@@ -84,6 +91,10 @@ _SIGS = {
     "gpt2_linear": (_I32, [_VP, _VP, _VP, _VP, _VP, _I64, _I32, _I32, _I64, _I32, _I32, _I32, _I32, _VP]),
     "gpt2_attention_causal": (_I32, [_VP, _VP, _I32, _I32, _I32, _I32, _I32, _VP]),
     "gpt2_attention_causal_scaled": (_I32, [_VP, _VP, _I32, _I32, _I32, _I32, _F, _I32, _VP]),
+    "gpt2_attention_causal_lse": (_I32, [_VP, _VP, _VP, _I32, _I32, _I32, _I32, _F, _I32, _VP]),
+    "gpt2_attention_backward_workspace_bytes": (_SZ, [_I32, _I32, _I32]),
+    "gpt2_attention_causal_backward": (_I32, [_VP, _VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32, _F, _VP, _SZ, _I32,
+                                              _VP]),
     "gpt2_mlp_workspace_bytes": (_SZ, [_I64, _I32, _I32]),
     "gpt2_mlp": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I32, _I32, _VP, _SZ, _I32, _VP]),
     "gpt2_workspace_bytes": (_SZ, [ctypes.POINTER(Dims), _I32, _I32]),
@@ -99,6 +110,9 @@ _SIGS = {
     "gpt2_loss_workspace_bytes": (_SZ, [ctypes.POINTER(Dims), _I32, _I32]),
     "gpt2_forward_loss": (_I32, [ctypes.POINTER(Dims), ctypes.POINTER(ModelWeights), _VP, _VP, _VP, _VP, _VP, _I32,
                                  _I32, _VP, _SZ, _VP]),
+    "gpt2_train_workspace_bytes": (_SZ, [ctypes.POINTER(Dims), _I32, _I32]),
+    "gpt2_forward_backward": (_I32, [ctypes.POINTER(Dims), ctypes.POINTER(ModelWeights), _VP, _VP,
+                                     ctypes.POINTER(ModelGrads), _VP, _I32, _I32, _VP, _SZ, _VP]),
     "gpt2_kv_cache_bytes": (_SZ, [ctypes.POINTER(Dims), _I32, _I32]),
     "gpt2_decode_workspace_bytes": (_SZ, [ctypes.POINTER(Dims), _I32]),
     "gpt2_prefill_workspace_bytes": (_SZ, [ctypes.POINTER(Dims), _I32, _I32]),
@@ -191,6 +205,22 @@ def gpt2_attention_causal_scaled(qkv, out, B, T, n_head, head_dim, score_scale, 
                                               _stream(stream)), "gpt2_attention_causal_scaled")
 
 
+def gpt2_attention_causal_lse(qkv, out, lse, B, T, n_head, head_dim, score_scale, dtype, stream=None):
+    _check(lib().gpt2_attention_causal_lse(_ptr(qkv), _ptr(out), _ptr(lse), B, T, n_head, head_dim, score_scale,
+                                           dtype, _stream(stream)), "gpt2_attention_causal_lse")
+
+
+def gpt2_attention_backward_workspace_bytes(B, T, n_head) -> int:
+    return lib().gpt2_attention_backward_workspace_bytes(B, T, n_head)
+
+
+def gpt2_attention_causal_backward(qkv, out, lse, dout, dqkv, B, T, n_head, head_dim, score_scale, ws, ws_bytes,
+                                   dtype, stream=None):
+    _check(lib().gpt2_attention_causal_backward(_ptr(qkv), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dqkv), B, T,
+                                                n_head, head_dim, score_scale, _ptr(ws), ws_bytes, dtype,
+                                                _stream(stream)), "gpt2_attention_causal_backward")
+
+
 def gpt2_mlp_workspace_bytes(M, F, dtype) -> int:
     return lib().gpt2_mlp_workspace_bytes(M, F, dtype)
 
@@ -249,6 +279,17 @@ def gpt2_forward_loss(dims: Dims, w: ModelWeights, tokens, labels, token_loss, l
     _check(lib().gpt2_forward_loss(ctypes.byref(dims), ctypes.byref(w), _ptr(tokens), _ptr(labels), _ptr(token_loss),
                                    _ptr(lse), _ptr(mean_loss), B, T, _ptr(ws), ws_bytes, _stream(stream)),
            "gpt2_forward_loss")
+
+
+def gpt2_train_workspace_bytes(dims: Dims, B: int, T: int) -> int:
+    return lib().gpt2_train_workspace_bytes(ctypes.byref(dims), B, T)
+
+
+def gpt2_forward_backward(dims: Dims, w: ModelWeights, tokens, labels, grads: ModelGrads, mean_loss, B, T, ws,
+                          ws_bytes, stream=None):
+    _check(lib().gpt2_forward_backward(ctypes.byref(dims), ctypes.byref(w), _ptr(tokens), _ptr(labels),
+                                       ctypes.byref(grads), _ptr(mean_loss), B, T, _ptr(ws), ws_bytes,
+                                       _stream(stream)), "gpt2_forward_backward")
 
 
 def gpt2_kv_cache_bytes(dims: Dims, B: int, T_max: int) -> int:
@@ -315,6 +356,14 @@ def model_weights(tensors: dict):
     mw = ModelWeights(_ptr(tensors["wte"]), _ptr(tensors["wpe"]), _ptr(tensors["lnf_g"]), _ptr(tensors["lnf_b"]),
                       ctypes.cast(blocks, ctypes.POINTER(BlockWeights)))
     return mw, blocks
+
+
+def model_grads(tensors: dict):
+    """(ModelGrads, keep-alive) from {wte, wpe, lnf_g, lnf_b, blocks: [dict]} of fp32 device tensors."""
+    blocks = (BlockGrads * len(tensors["blocks"]))(*[block_grads(b) for b in tensors["blocks"]])
+    mg = ModelGrads(_ptr(tensors["wte"]), _ptr(tensors["wpe"]), _ptr(tensors["lnf_g"]), _ptr(tensors["lnf_b"]),
+                    ctypes.cast(blocks, ctypes.POINTER(BlockGrads)))
+    return mg, blocks
 
 
 def to_device(params: dict, dtype: int, device="cuda"):

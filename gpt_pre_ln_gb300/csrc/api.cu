@@ -15,6 +15,7 @@
 //                                          (the exact GELU with that switch)
 //   x'  = h + g W_proj + b_proj            GEMM, epilogue + bias + residual
 // then LN_f and the tied lm_head (GEMM against wte [V, D], no bias).
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstring>
@@ -552,6 +553,230 @@ int block_backward_f32(const gpt2_dims* d, const gpt2_block_weights* w, int laye
   return GPT2_OK;
 }
 
+// ------------------------------------------------------- training step
+// Buffers of gpt2_forward_backward (bf16 path).  Per layer the forward keeps
+// what the backward reads (llm.c notes 5.2: the intermediates are kept):
+// the block input x (fp32), LN_1 output a, qkv, the attention output o and
+// its row log-sum-exp, h (fp32), LN_2 output a2, the c_fc output u and its
+// GELU g.  Then x_L, LN_f(x_L), the loss buffers, and the backward scratch.
+struct TrainLayer {
+  float *x, *h, *lse;
+  void *a, *qkv, *o, *a2, *u, *g;
+};
+struct TrainBufs {
+  std::vector<TrainLayer> L;
+  float* xL;
+  void* xf;
+  float *tgt, *tl, *row_lse, *logits32;
+  float2* part;
+  int64_t ldz;
+  void* dz;
+  float *dx, *dh, *dyf, *prod, *delta, *colpart;
+  void *dxb, *dhb, *dgb, *dub, *dob, *dqkvb;
+  size_t bytes;
+};
+
+// Carves the buffers from `ws` (or, with ws == nullptr, only counts bytes).
+TrainBufs carve_train(void* ws, const gpt2_dims* d, int B, int T) {
+  const size_t M = static_cast<size_t>(B) * T, D = d->d_model, F = d->d_ff, H = d->n_head, V = d->vocab;
+  size_t off = 0;
+  char* base = static_cast<char*>(ws);
+  auto take = [&](size_t bytes) -> void* {
+    void* p = base ? static_cast<void*>(base + off) : nullptr;
+    off += align256(bytes);
+    return p;
+  };
+  TrainBufs t;
+  t.L.resize(d->n_layer);
+  for (int l = 0; l < d->n_layer; ++l) {
+    TrainLayer& y = t.L[l];
+    y.x = static_cast<float*>(take(M * D * 4));
+    y.h = static_cast<float*>(take(M * D * 4));
+    y.lse = static_cast<float*>(take(static_cast<size_t>(B) * H * T * 4));
+    y.a = take(M * D * 2);
+    y.qkv = take(M * 3 * D * 2);
+    y.o = take(M * D * 2);
+    y.a2 = take(M * D * 2);
+    y.u = take(M * F * 2);
+    y.g = take(M * F * 2);
+  }
+  t.xL = static_cast<float*>(take(M * D * 4));
+  t.xf = take(M * D * 2);
+  t.tgt = static_cast<float*>(take(M * 4));
+  t.tl = static_cast<float*>(take(M * 4));
+  t.row_lse = static_cast<float*>(take(M * 4));
+  const bool fused = static_cast<int64_t>(M) > kMaxRowsGemm;
+  t.part = static_cast<float2*>(take((fused ? M * lse_max_partials(d->vocab) : M) * sizeof(float2)));
+  t.logits32 = fused ? nullptr : static_cast<float*>(take(M * ((V + 3) / 4 * 4) * 4));
+  t.ldz = (static_cast<int64_t>(V) + 7) / 8 * 8;
+  t.dz = take(M * t.ldz * 2);
+  t.dx = static_cast<float*>(take(M * D * 4));
+  t.dh = static_cast<float*>(take(M * D * 4));
+  t.dyf = static_cast<float*>(take(M * D * 4));
+  t.prod = static_cast<float*>(take(M * D * 4));
+  t.delta = static_cast<float*>(take(static_cast<size_t>(B) * H * T * 4));
+  const size_t widest = std::max<size_t>({3 * D, F, D});
+  t.colpart = static_cast<float*>(take(colsum_partial_bytes(static_cast<long long>(M), static_cast<int>(widest))));
+  t.dxb = take(M * D * 2);
+  t.dhb = take(M * D * 2);
+  t.dgb = take(M * F * 2);
+  t.dub = take(M * F * 2);
+  t.dob = take(M * D * 2);
+  t.dqkvb = take(M * 3 * D * 2);
+  t.bytes = off;
+  return t;
+}
+
+int check_grads(const gpt2_dims* d, const gpt2_model_grads* g) {
+  if (!g || !g->blocks) return GPT2_ERR_ARG;
+  const void* ps[4] = {g->wte, g->wpe, g->lnf_g, g->lnf_b};
+  for (const void* p : ps)
+    if (!p || !aligned16(p)) return GPT2_ERR_ARG;
+  for (int l = 0; l < d->n_layer; ++l) {
+    const gpt2_block_grads& b = g->blocks[l];
+    const float* bp[12] = {b.ln1_g, b.ln1_b, b.w_qkv, b.b_qkv, b.w_o, b.b_o,
+                           b.ln2_g, b.ln2_b, b.w_fc, b.b_fc, b.w_proj, b.b_proj};
+    for (const float* p : bp)
+      if (!p || !aligned16(p)) return GPT2_ERR_ARG;
+  }
+  return GPT2_OK;
+}
+
+// One tensor-core GEMM of the backward, profiled like the forward's.
+cudaError_t grad_gemm(const void* a, long long lda, bool a_mn, const void* w, long long ldw, bool w_kn, void* y,
+                      long long ldy, gpt2_dtype y_t, int64_t M, int N, int K, cudaStream_t s) {
+  ProfScope prof("gemm_grad_bf16_tcgen05", 2.0 * M * N * K,
+                 (static_cast<double>(M) * K + static_cast<double>(K) * N) * 2.0 + static_cast<double>(M) * N * esize(y_t),
+                 s);
+  return launch_gemm_grad(a, lda, a_mn, w, ldw, w_kn, y, ldy, y_t, static_cast<int>(M), N, K, s);
+}
+
+cudaError_t colsum(const void* in, bool in16, int64_t M, int N, float* partial, float* out, cudaStream_t s) {
+  ProfScope prof("colsum", static_cast<double>(M) * N, static_cast<double>(M) * N * (in16 ? 2.0 : 4.0), s);
+  return launch_colsum(in, in16, M, N, N, partial, out, s);
+}
+
+cudaError_t ln_bwd(const float* dy, const float* x, const void* gamma, const float* dres, float* dx, void* dx16,
+                   float* prod, int64_t M, int D, float eps, cudaStream_t s) {
+  ProfScope prof("layernorm_bwd", 12.0 * M * D, static_cast<double>(M) * D * (4.0 * 4 + (dres ? 4.0 : 0.0) + 2.0), s);
+  return launch_ln_bwd_16(dy, x, gamma, dres, dx, dx16, prod, M, D, eps, s);
+}
+
+// Forward with saved intermediates, then the mean shifted cross-entropy and
+// the gradient of every parameter (the order of the backward is the reverse
+// of the forward: llm.c notes 5.2-5.3; the tied lm_head and the embedding
+// both add to wte: "逐行拆GPT-2源码", GPT2LMHeadModel).
+int forward_backward(const gpt2_dims* d, const gpt2_model_weights* w, const int32_t* tokens, const int32_t* labels,
+                     const gpt2_model_grads* gr, float* mean_loss, int B, int T, TrainBufs& t, cudaStream_t s) {
+  const gpt2_dtype dt = d->dtype;
+  const int64_t M = static_cast<int64_t>(B) * T;
+  const int D = d->d_model, F = d->d_ff, H = d->n_head, V = d->vocab, L = d->n_layer;
+  const float eps = d->eps;
+  const bool exact = (d->flags & GPT2_GELU_EXACT) != 0;
+  // ---- forward
+  {
+    ProfScope prof("embed_layernorm", 8.0 * M * D, static_cast<double>(M) * D * 10.0, s);
+    GPT2_CUDA(launch_embed_ln(tokens, w->wte, w->wpe, w->blocks[0].ln1_g, w->blocks[0].ln1_b, t.L[0].x, t.L[0].a, B,
+                              T, D, V, eps, dt, s));
+  }
+  for (int l = 0; l < L; ++l) {
+    const gpt2_block_weights* bw = &w->blocks[l];
+    TrainLayer& y = t.L[l];
+    if (l > 0) GPT2_CUDA(layernorm(y.x, bw->ln1_g, bw->ln1_b, y.a, M, D, eps, GPT2_F32, dt, s));
+    GPT2_CUDA(linear(dt, y.a, bw->w_qkv, bw->b_qkv, nullptr, y.qkv, M, 3 * D, D, 3 * D, false, GPT2_EPI_BIAS, dt, s));
+    {
+      const double pairs = static_cast<double>(B) * H * T * (T + 1.0) / 2.0;
+      ProfScope prof("attn_causal_bf16_tc", 4.0 * 64.0 * pairs, static_cast<double>(M) * 4.0 * D * 2.0, s);
+      GPT2_CUDA(launch_attention_tc(dt, y.qkv, y.o, B, T, H, score_scale(d, l), s, y.lse));
+    }
+    GPT2_CUDA(linear(dt, y.o, bw->w_o, bw->b_o, y.x, y.h, M, D, D, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32, s));
+    GPT2_CUDA(layernorm(y.h, bw->ln2_g, bw->ln2_b, y.a2, M, D, eps, GPT2_F32, dt, s));
+    GPT2_CUDA(linear(dt, y.a2, bw->w_fc, bw->b_fc, nullptr, y.u, M, F, D, F, false, GPT2_EPI_BIAS, dt, s));
+    {
+      ProfScope prof("gelu", 8.0 * M * F, 4.0 * M * F, s);
+      GPT2_CUDA(launch_gelu_fwd_16(y.u, y.g, M * F, exact, s));
+    }
+    float* x_next = l + 1 < L ? t.L[l + 1].x : t.xL;
+    GPT2_CUDA(linear(dt, y.g, bw->w_proj, bw->b_proj, y.h, x_next, M, D, F, D, false, GPT2_EPI_BIAS_RESIDUAL, GPT2_F32,
+                     s));
+  }
+  GPT2_CUDA(layernorm(t.xL, w->lnf_g, w->lnf_b, t.xf, M, D, eps, GPT2_F32, dt, s));
+  // ---- loss: each row's log-sum-exp (kept for dz) and the mean
+  int n_part = 1;
+  if (t.logits32 == nullptr) {
+    ProfScope prof("gemm_lse_bf16_tcgen05", 2.0 * M * V * D, (static_cast<double>(M) + V) * D * 2.0, s);
+    GPT2_CUDA(launch_gemm_lse_16(dt, t.xf, w->wte, M, V, D, labels, T, t.part, t.tgt, &n_part, s));
+  } else {
+    const int64_t lv = (static_cast<int64_t>(V) + 3) / 4 * 4;
+    GPT2_CUDA(linear(dt, t.xf, w->wte, nullptr, nullptr, t.logits32, M, V, D, lv, true, GPT2_EPI_NONE, GPT2_F32, s));
+    GPT2_CUDA(launch_lse_from_logits(t.logits32, lv, M, V, labels, T, t.part, t.tgt, s));
+  }
+  {
+    ProfScope prof("loss_reduce", 4.0 * M * n_part, 8.0 * M * n_part + 12.0 * M, s);
+    GPT2_CUDA(launch_loss_rows(t.part, n_part, t.tgt, labels, B, T, V, t.row_lse, t.tl, mean_loss, s));
+  }
+  // ---- lm_head and LN_f
+  const float inv_n = 1.f / static_cast<float>(static_cast<double>(B) * (T - 1));
+  {
+    ProfScope prof("gemm_dlogits_bf16_tcgen05", 2.0 * M * V * D, static_cast<double>(M) * V * 2.0, s);
+    GPT2_CUDA(launch_gemm_dlogits(t.xf, w->wte, static_cast<int>(M), V, D, t.row_lse, labels, T, inv_n, t.dz, t.ldz,
+                                  s));
+  }
+  GPT2_CUDA(grad_gemm(t.dz, t.ldz, true, t.xf, D, true, gr->wte, D, GPT2_F32, V, D, static_cast<int>(M), s));
+  GPT2_CUDA(grad_gemm(t.dz, t.ldz, false, w->wte, D, true, t.dyf, D, GPT2_F32, M, D, V, s));
+  GPT2_CUDA(ln_bwd(t.dyf, t.xL, w->lnf_g, nullptr, t.dx, t.dxb, t.prod, M, D, eps, s));
+  GPT2_CUDA(colsum(t.prod, false, M, D, t.colpart, gr->lnf_g, s));
+  GPT2_CUDA(colsum(t.dyf, false, M, D, t.colpart, gr->lnf_b, s));
+  // ---- blocks, last first
+  const int Mi = static_cast<int>(M);
+  for (int l = L - 1; l >= 0; --l) {
+    const gpt2_block_weights* bw = &w->blocks[l];
+    const gpt2_block_grads* bg = &gr->blocks[l];
+    TrainLayer& y = t.L[l];
+    // x' = h + g W_proj + b_proj
+    GPT2_CUDA(grad_gemm(t.dxb, D, false, bw->w_proj, D, false, t.dgb, F, dt, M, F, D, s));
+    GPT2_CUDA(grad_gemm(y.g, F, true, t.dxb, D, true, bg->w_proj, D, GPT2_F32, F, D, Mi, s));
+    GPT2_CUDA(colsum(t.dx, false, M, D, t.colpart, bg->b_proj, s));
+    {
+      ProfScope prof("gelu_bwd", 20.0 * M * F, 6.0 * M * F, s);
+      GPT2_CUDA(launch_gelu_bwd_16(t.dgb, y.u, t.dub, M * F, exact, s));
+    }
+    // u = a2 W_fc + b_fc
+    GPT2_CUDA(grad_gemm(t.dub, F, false, bw->w_fc, F, false, t.dyf, D, GPT2_F32, M, D, F, s));
+    GPT2_CUDA(grad_gemm(y.a2, D, true, t.dub, F, true, bg->w_fc, F, GPT2_F32, D, F, Mi, s));
+    GPT2_CUDA(colsum(t.dub, true, M, F, t.colpart, bg->b_fc, s));
+    // a2 = LN_2(h), and the residual path: dh = dx' + LN_2'(h)^T da2
+    GPT2_CUDA(ln_bwd(t.dyf, y.h, bw->ln2_g, t.dx, t.dh, t.dhb, t.prod, M, D, eps, s));
+    GPT2_CUDA(colsum(t.prod, false, M, D, t.colpart, bg->ln2_g, s));
+    GPT2_CUDA(colsum(t.dyf, false, M, D, t.colpart, bg->ln2_b, s));
+    // h = x + o W_o + b_o
+    GPT2_CUDA(grad_gemm(t.dhb, D, false, bw->w_o, D, false, t.dob, D, dt, M, D, D, s));
+    GPT2_CUDA(grad_gemm(y.o, D, true, t.dhb, D, true, bg->w_o, D, GPT2_F32, D, D, Mi, s));
+    GPT2_CUDA(colsum(t.dh, false, M, D, t.colpart, bg->b_o, s));
+    // o = attention(qkv)
+    {
+      const double pairs = static_cast<double>(B) * H * T * (T + 1.0) / 2.0;
+      ProfScope prof("attn_causal_bwd_bf16_tc", 10.0 * 64.0 * pairs, static_cast<double>(M) * D * 2.0 * 8.0, s);
+      GPT2_CUDA(launch_attention_backward_tc(dt, y.qkv, y.o, y.lse, t.dob, t.dqkvb, t.delta, B, T, H,
+                                             score_scale(d, l), s));
+    }
+    // qkv = a W_qkv + b_qkv
+    GPT2_CUDA(grad_gemm(t.dqkvb, 3 * D, false, bw->w_qkv, 3 * D, false, t.dyf, D, GPT2_F32, M, D, 3 * D, s));
+    GPT2_CUDA(grad_gemm(y.a, D, true, t.dqkvb, 3 * D, true, bg->w_qkv, 3 * D, GPT2_F32, D, 3 * D, Mi, s));
+    GPT2_CUDA(colsum(t.dqkvb, true, M, 3 * D, t.colpart, bg->b_qkv, s));
+    // a = LN_1(x), and the residual path: dx = dh + LN_1'(x)^T da
+    GPT2_CUDA(ln_bwd(t.dyf, y.x, bw->ln1_g, t.dh, t.dx, t.dxb, t.prod, M, D, eps, s));
+    GPT2_CUDA(colsum(t.prod, false, M, D, t.colpart, bg->ln1_g, s));
+    GPT2_CUDA(colsum(t.dyf, false, M, D, t.colpart, bg->ln1_b, s));
+  }
+  // ---- the embedding: wte rows of the tokens used, wpe rows of the positions
+  {
+    ProfScope prof("embed_bwd", static_cast<double>(M) * D, static_cast<double>(M) * D * 8.0, s);
+    GPT2_CUDA(launch_embed_bwd(tokens, t.dx, gr->wte, gr->wpe, B, T, D, V, d->n_pos, s));
+  }
+  return GPT2_OK;
+}
+
 }  // namespace
 
 namespace gpt2 {
@@ -664,6 +889,46 @@ int gpt2_attention_causal_scaled(const void* qkv, void* out, int B, int T, int n
   if (B == 0 || T == 0) return GPT2_OK;
   if (!qkv || !out || !aligned16(qkv) || !aligned16(out)) return GPT2_ERR_ARG;
   return cuda_status(attention(dtype, qkv, out, B, T, n_head, score_scale, cs(stream)));
+}
+
+int gpt2_attention_causal_lse(const void* qkv, void* out, float* lse, int B, int T, int n_head, int head_dim,
+                              float score_scale, gpt2_dtype dtype, gpt2_stream_t stream) {
+  if (!valid_dtype(dtype) || B < 0 || T < 0 || n_head <= 0 || head_dim <= 0) return GPT2_ERR_ARG;
+  if (!(score_scale > 0.f) || !std::isfinite(score_scale)) return GPT2_ERR_ARG;
+  if (head_dim != 64 || !is16(dtype)) return GPT2_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * n_head > INT_MAX || T > 65535 * 64) return GPT2_ERR_UNSUPPORTED;
+  if (B == 0 || T == 0) return GPT2_OK;
+  if (!qkv || !out || !lse || !aligned16(qkv) || !aligned16(out)) return GPT2_ERR_ARG;
+  const double pairs = static_cast<double>(B) * n_head * T * (T + 1.0) / 2.0;
+  ProfScope prof(dtype == GPT2_BF16 ? "attn_causal_bf16_tc" : "attn_causal_f16_tc", 4.0 * 64.0 * pairs,
+                 static_cast<double>(B) * T * 4.0 * 64.0 * n_head * 2.0, cs(stream));
+  return cuda_status(launch_attention_tc(dtype, qkv, out, B, T, n_head, score_scale, cs(stream), lse));
+}
+
+size_t gpt2_attention_backward_workspace_bytes(int B, int T, int n_head) {
+  if (B < 0 || T < 0 || n_head <= 0) return 0;
+  return align256(static_cast<size_t>(B) * n_head * T * 4);
+}
+
+int gpt2_attention_causal_backward(const void* qkv, const void* out, const float* lse, const void* dout, void* dqkv,
+                                   int B, int T, int n_head, int head_dim, float score_scale, void* ws,
+                                   size_t ws_bytes, gpt2_dtype dtype, gpt2_stream_t stream) {
+  if (!valid_dtype(dtype) || B < 0 || T < 0 || n_head <= 0 || head_dim <= 0) return GPT2_ERR_ARG;
+  if (!(score_scale > 0.f) || !std::isfinite(score_scale)) return GPT2_ERR_ARG;
+  if (head_dim != 64 || !is16(dtype)) return GPT2_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * n_head * ((T + 127) / 128) > INT_MAX || static_cast<int64_t>(B) * T > INT_MAX)
+    return GPT2_ERR_UNSUPPORTED;
+  if (B == 0 || T == 0) return GPT2_OK;
+  const void* ps[5] = {qkv, out, lse, dout, dqkv};
+  for (const void* p : ps)
+    if (!p || !aligned16(p)) return GPT2_ERR_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return GPT2_ERR_ARG;
+  if (ws_bytes < gpt2_attention_backward_workspace_bytes(B, T, n_head)) return GPT2_ERR_WORKSPACE;
+  const double pairs = static_cast<double>(B) * n_head * T * (T + 1.0) / 2.0;
+  ProfScope prof(dtype == GPT2_BF16 ? "attn_causal_bwd_bf16_tc" : "attn_causal_bwd_f16_tc", 10.0 * 64.0 * pairs,
+                 static_cast<double>(B) * T * 64.0 * n_head * 2.0 * 8.0, cs(stream));
+  return cuda_status(launch_attention_backward_tc(dtype, qkv, out, lse, dout, dqkv, static_cast<float*>(ws), B, T,
+                                                  n_head, score_scale, cs(stream)));
 }
 
 size_t gpt2_mlp_workspace_bytes(int64_t M, int F, gpt2_dtype dtype) {
@@ -818,6 +1083,28 @@ int gpt2_forward_loss(const gpt2_dims* dims, const gpt2_model_weights* w, const 
   GPT2_CUDA(launch_loss_rows(part, n_part, tgt, labels, B, T, V, lse, token_loss ? token_loss : tl_scratch,
                              mean_loss, s));
   return GPT2_OK;
+}
+
+size_t gpt2_train_workspace_bytes(const gpt2_dims* dims, int B, int T) {
+  if (check_dims(dims, true) != GPT2_OK || dims->dtype != GPT2_BF16 || B < 0 || T < 0) return 0;
+  return carve_train(nullptr, dims, B, T).bytes;
+}
+
+int gpt2_forward_backward(const gpt2_dims* dims, const gpt2_model_weights* w, const int32_t* tokens,
+                          const int32_t* labels, const gpt2_model_grads* grads, float* mean_loss, int B, int T,
+                          void* ws, size_t ws_bytes, gpt2_stream_t stream) {
+  GPT2_TRY(check_model(dims, w));
+  if (dims->dtype != GPT2_BF16) return GPT2_ERR_UNSUPPORTED;
+  GPT2_TRY(check_grads(dims, grads));
+  if (B < 0 || T < 0 || static_cast<int64_t>(B) * T > INT_MAX) return GPT2_ERR_ARG;
+  if (T > dims->n_pos) return GPT2_ERR_ARG;
+  if (B == 0) return GPT2_OK;
+  if (T < 2 || !tokens || !mean_loss) return GPT2_ERR_ARG;
+  if (static_cast<int64_t>(B) * dims->n_head * ((T + 127) / 128) > INT_MAX) return GPT2_ERR_UNSUPPORTED;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return GPT2_ERR_ARG;
+  if (ws_bytes < gpt2_train_workspace_bytes(dims, B, T)) return GPT2_ERR_WORKSPACE;
+  TrainBufs t = carve_train(ws, dims, B, T);
+  return forward_backward(dims, w, tokens, labels ? labels : tokens, grads, mean_loss, B, T, t, cs(stream));
 }
 
 size_t gpt2_kv_cache_bytes(const gpt2_dims* dims, int B, int T_max) {

@@ -75,6 +75,19 @@ cudaError_t launch_gemm_lse_16(gpt2_dtype dt, const void* x, const void* w, int6
                                const int32_t* labels, int T, float2* part, float* tgt, int* n_part,
                                cudaStream_t stream);
 
+// The GEMM for the backward (bf16 operands, no epilogue; gemm_grad.cu):
+//   y[M, N] = op(A) op(W) with A [M, K] (pitch lda) or, with a_mn, [K, M];
+//   W [N, K] (pitch ldw) or, with w_kn, [K, N]; K any positive extent.
+//   y fp32, or bf16 when neither a_mn nor w_kn.
+cudaError_t launch_gemm_grad(const void* a, long long lda, bool a_mn, const void* w, long long ldw, bool w_kn,
+                             void* y, long long ldy, gpt2_dtype y_t, int M, int N, int K, cudaStream_t s);
+// The loss gradient with respect to the logits z = xf wte^T (bf16 [M, D] x
+// [V, D]), written as bf16 dz [M, lddz]: (exp(z - row_lse) - [v == label])
+// * inv_n at row r with label labels[r + 1]; zero in the last row of every
+// sequence of T rows.
+cudaError_t launch_gemm_dlogits(const void* xf, const void* wte, int M, int V, int D, const float* row_lse,
+                                const int32_t* labels, int T, float inv_n, void* dz, long long lddz, cudaStream_t s);
+
 // The same GEMM for M <= kMaxRowsGemm rows (operands swapped, K split over a
 // thread-block cluster); launch_gemm_16 hands such calls to it.  With
 // argmax_cand (epilogue NONE, fp32 y, which may then be null) it also writes
@@ -100,9 +113,17 @@ cudaError_t launch_gemm_f32(const float* x, const float* w, const float* bias, c
 
 // tcgen05 version (S and O in tensor memory), head_dim 64; dt GPT2_BF16 or
 // GPT2_F16.
-// Scores are q.k times score_scale (1/sqrt(64) for GPT-2).
+// Scores are q.k times score_scale (1/sqrt(64) for GPT-2).  With lse
+// (fp32 [B, n_head, T]) each row's log2 sum_j 2^(s_j log2(e)) is kept for
+// the backward.
 cudaError_t launch_attention_tc(gpt2_dtype dt, const void* qkv, void* out, int B, int T, int n_head, float score_scale,
-                                cudaStream_t stream);
+                                cudaStream_t stream, float* lse = nullptr);
+// Causal attention backward (16-bit paths, tcgen05): dqkv [B, T, 3D] from
+// qkv, the forward's output `out` and its lse (above), and dout [B, T, D];
+// delta is [B, n_head, T] fp32 scratch.
+cudaError_t launch_attention_backward_tc(gpt2_dtype dt, const void* qkv, const void* out, const float* lse,
+                                         const void* dout, void* dqkv, float* delta, int B, int T, int n_head,
+                                         float score_scale, cudaStream_t stream);
 cudaError_t launch_attention_f32(const float* qkv, float* out, int B, int T, int n_head, float score_scale,
                                  cudaStream_t stream);
 
@@ -139,6 +160,25 @@ cudaError_t launch_lse_from_logits(const float* logits, int64_t ld, int64_t M, i
                                    float2* part, float* tgt, cudaStream_t stream);
 cudaError_t launch_argmax_candidates(const float2* cand, int n_cand, int B, const int* valid, int32_t* next_tokens,
                                      int32_t* past_len, cudaStream_t stream);
+
+// 16-bit backward kernels (backward_16.cu; bf16).
+// out[N] = column sums of in[M, N] (row pitch ld; fp32 or, with in16, bf16),
+// in a fixed order; partial: colsum_partial_bytes(M, N) of scratch.
+size_t colsum_partial_bytes(long long M, int N);
+cudaError_t launch_colsum(const void* in, bool in16, long long M, int N, long long ld, float* partial, float* out,
+                          cudaStream_t s);
+// g = act(u) and du = dg * act'(u) over n (even) bf16 values; act gelu_new
+// or, with exact, x Phi(x).
+cudaError_t launch_gelu_fwd_16(const void* u, void* g, long long n, bool exact, cudaStream_t s);
+cudaError_t launch_gelu_bwd_16(const void* dg, const void* u, void* du, long long n, bool exact, cudaStream_t s);
+// LayerNorm backward (gamma bf16): dx = LN'(x)^T dy (+ dres), dx16 (nullable)
+// its bf16 copy, prod = dy * xhat.
+cudaError_t launch_ln_bwd_16(const float* dy, const float* x, const void* gamma, const float* dres, float* dx,
+                             void* dx16, float* prod, long long rows, int D, float eps, cudaStream_t s);
+// dwte[tokens[m]] += dx0[m] (each row in position order), dwpe[t] = sum_b
+// dx0[b, t] for t < T, 0 for T <= t < n_pos.
+cudaError_t launch_embed_bwd(const int32_t* tokens, const float* dx0, float* dwte, float* dwpe, int B, int T, int D,
+                             int V, int n_pos, cudaStream_t s);
 
 // Backward of one block on the fp32 path (backward_f32.cu).
 // dw[K, N] = x[M, K]^T dy[M, N].

@@ -205,6 +205,31 @@ int gpt2_attention_causal(const void *qkv, void *out, int B, int T, int n_head, 
 int gpt2_attention_causal_scaled(const void *qkv, void *out, int B, int T, int n_head, int head_dim,
                                  float score_scale, gpt2_dtype dtype, gpt2_stream_t stream);
 
+/* gpt2_attention_causal_scaled that also keeps, for the backward, each
+ * query row's log-sum-exp of its scaled scores: lse[b, h, t] (fp32
+ * [B, n_head, T]) = log2 sum_{j <= t} 2^(score_scale * log2(e) * q_t . k_j),
+ * so that p_tj = 2^(score_scale * log2(e) * q_t . k_j - lse[b, h, t]).
+ * 16-bit dtypes only (GPT2_ERR_UNSUPPORTED for GPT2_F32). */
+int gpt2_attention_causal_lse(const void *qkv, void *out, float *lse, int B, int T, int n_head, int head_dim,
+                              float score_scale, gpt2_dtype dtype, gpt2_stream_t stream);
+
+/* Backward of the causal attention (llm.c notes 5.3: the softmax gradient
+ * of the max-subtracted forward, no gradient at masked positions):
+ *   dv = p^T do, dp = do v^T, ds = p (dp - rowsum(do * o)),
+ *   dq = c ds k, dk = c ds^T q   (c = score_scale, per head)
+ * qkv [B, T, 3D] and out [B, T, D] are the forward's input and output, lse
+ * its row statistics (gpt2_attention_causal_lse), dout [B, T, D] the
+ * gradient of out; dqkv [B, T, 3D] receives the gradients of Q | K | V in
+ * the layout of qkv.  16-bit dtypes (all of qkv, out, dout, dqkv), fp32
+ * accumulation on the tensor cores; p and ds are rounded to the 16-bit type
+ * before they multiply.  The result does not depend on timing (no atomics).
+ * ws: device workspace of gpt2_attention_backward_workspace_bytes(B, T,
+ * n_head) bytes, 256-byte aligned. */
+size_t gpt2_attention_backward_workspace_bytes(int B, int T, int n_head);
+int gpt2_attention_causal_backward(const void *qkv, const void *out, const float *lse, const void *dout, void *dqkv,
+                                   int B, int T, int n_head, int head_dim, float score_scale, void *ws,
+                                   size_t ws_bytes, gpt2_dtype dtype, gpt2_stream_t stream);
+
 /* Workspace needed by gpt2_mlp for M rows (the [M, F] hidden activation). */
 size_t gpt2_mlp_workspace_bytes(int64_t M, int F, gpt2_dtype dtype);
 
@@ -309,6 +334,40 @@ size_t gpt2_block_backward_workspace_bytes(const gpt2_dims *dims, int B, int T);
 int gpt2_block_backward(const gpt2_dims *dims, const gpt2_block_weights *w, int layer, const float *x_in,
                         const float *dx_out, float *dx_in, const gpt2_block_grads *grads, int B, int T, void *ws,
                         size_t ws_bytes, gpt2_stream_t stream);
+
+/* Gradients of the whole model, fp32 device buffers of the weights' shapes
+ * (blocks: a HOST array of n_layer gpt2_block_grads). */
+typedef struct {
+  float *wte;   /* [V, D]: the tied lm_head and the embedding together */
+  float *wpe;   /* [n_pos, D]: rows >= T are set to zero */
+  float *lnf_g, *lnf_b;
+  const gpt2_block_grads *blocks;
+} gpt2_model_grads;
+
+/* Workspace of gpt2_forward_backward for a [B, T] batch (0 if the dims are
+ * invalid or not GPT2_BF16). */
+size_t gpt2_train_workspace_bytes(const gpt2_dims *dims, int B, int T);
+
+/* One training step's arithmetic: the forward of gpt2_forward_loss, keeping
+ * every block's intermediates (llm.c notes 5.2), the mean shifted
+ * cross-entropy into *mean_loss (device fp32), and the gradient of that
+ * loss with respect to every parameter into `grads` (written, not added;
+ * llm.c notes 5.3 for the LayerNorm and softmax gradients; "逐行拆GPT-2源码",
+ * GPT2LMHeadModel: wte receives the lm_head's and the embedding's
+ * gradient).  dL/dz at position t < T-1 is (softmax(z) - onehot(label of
+ * t+1)) / (B (T-1)), zero at the last position of each sequence.
+ *   dims->dtype must be GPT2_BF16 (else GPT2_ERR_UNSUPPORTED): bf16 operands
+ *   on the tensor cores with fp32 accumulation (the products of every
+ *   linear layer, of the lm_head and of the attention backward), fp32
+ *   LayerNorm, residual-stream and bias gradients; sums over rows in a fixed
+ *   order (results do not depend on timing).  tokens / labels as in
+ *   gpt2_forward_loss (labels NULL = tokens); T >= 2; ws of
+ *   gpt2_train_workspace_bytes(dims, B, T) bytes, 256-byte aligned (about
+ *   0.2 GB per layer at GPT-2 small width and B T = 8192, plus the
+ *   [B T, vocab] bf16 loss gradient). */
+int gpt2_forward_backward(const gpt2_dims *dims, const gpt2_model_weights *w, const int32_t *tokens,
+                          const int32_t *labels, const gpt2_model_grads *grads, float *mean_loss, int B, int T,
+                          void *ws, size_t ws_bytes, gpt2_stream_t stream);
 
 /* Workspace needed by gpt2_forward_loss for a [B, T] batch (0 if the dims
  * are invalid). */
