@@ -466,13 +466,15 @@ struct BwdActs {
   float *a, *qkv, *o, *h, *a2, *u, *g;        // forward: LN_1(x), c_attn, attention, h, LN_2(h), c_fc, act
   float *dg, *du, *da2, *dh, *dout, *dqkv, *da;  // backward
   float *prod, *lse, *delta;
+  float* colpart;  // column-sum partials
 };
 
 size_t bwd_ws_bytes(const gpt2_dims* d, int B, int T) {
   const size_t M = static_cast<size_t>(B) * T, D = d->d_model, F = d->d_ff, H = d->n_head;
   const size_t rows_d = align256(M * D * 4), rows_3d = align256(M * 3 * D * 4), rows_f = align256(M * F * 4);
   const size_t stats = align256(static_cast<size_t>(B) * H * T * 4);
-  return rows_d * 9 + rows_3d * 2 + rows_f * 4 + stats * 2;
+  return rows_d * 9 + rows_3d * 2 + rows_f * 4 + stats * 2 +
+         align256(colsum_partial_bytes(static_cast<long long>(M), static_cast<int>(std::max(3 * D, F))));
 }
 
 BwdActs carve_bwd(void* ws, const gpt2_dims* d, int B, int T) {
@@ -496,6 +498,8 @@ BwdActs carve_bwd(void* ws, const gpt2_dims* d, int B, int T) {
   A.prod = c.take<float>(M * D, 4);
   A.lse = c.take<float>(static_cast<size_t>(B) * H * T, 4);
   A.delta = c.take<float>(static_cast<size_t>(B) * H * T, 4);
+  A.colpart = c.take<float>(colsum_partial_bytes(static_cast<long long>(M), static_cast<int>(std::max(3 * D, F))) / 4,
+                            4);
   return A;
 }
 
@@ -528,28 +532,28 @@ int block_backward_f32(const gpt2_dims* d, const gpt2_block_weights* w, int laye
   // MLP
   GPT2_CUDA(linear(GPT2_F32, dy, w->w_proj, nullptr, nullptr, A.dg, M, F, D, F, true, GPT2_EPI_NONE, GPT2_F32, s));
   GPT2_CUDA(launch_gemm_at_f32(A.g, dy, gr->w_proj, M, F, D, s));
-  GPT2_CUDA(launch_colsum_f32(dy, gr->b_proj, M, D, s));
+  GPT2_CUDA(launch_colsum(dy, false, M, D, D, A.colpart, gr->b_proj, s));
   GPT2_CUDA(launch_gelu_backward_f32(A.dg, A.u, A.du, M * F, exact, s));
   GPT2_CUDA(linear(GPT2_F32, A.du, w->w_fc, nullptr, nullptr, A.da2, M, D, F, D, true, GPT2_EPI_NONE, GPT2_F32, s));
   GPT2_CUDA(launch_gemm_at_f32(A.a2, A.du, gr->w_fc, M, D, F, s));
-  GPT2_CUDA(launch_colsum_f32(A.du, gr->b_fc, M, F, s));
+  GPT2_CUDA(launch_colsum(A.du, false, M, F, F, A.colpart, gr->b_fc, s));
   // LN_2 and the residual path
   GPT2_CUDA(launch_ln_backward_f32(A.da2, A.h, f(w->ln2_g), dy, A.dh, A.prod, M, D, eps, s));
-  GPT2_CUDA(launch_colsum_f32(A.prod, gr->ln2_g, M, D, s));
-  GPT2_CUDA(launch_colsum_f32(A.da2, gr->ln2_b, M, D, s));
+  GPT2_CUDA(launch_colsum(A.prod, false, M, D, D, A.colpart, gr->ln2_g, s));
+  GPT2_CUDA(launch_colsum(A.da2, false, M, D, D, A.colpart, gr->ln2_b, s));
   // attention sublayer
   GPT2_CUDA(linear(GPT2_F32, A.dh, w->w_o, nullptr, nullptr, A.dout, M, D, D, D, true, GPT2_EPI_NONE, GPT2_F32, s));
   GPT2_CUDA(launch_gemm_at_f32(A.o, A.dh, gr->w_o, M, D, D, s));
-  GPT2_CUDA(launch_colsum_f32(A.dh, gr->b_o, M, D, s));
+  GPT2_CUDA(launch_colsum(A.dh, false, M, D, D, A.colpart, gr->b_o, s));
   GPT2_CUDA(launch_attention_backward_f32(A.qkv, A.dout, A.dqkv, A.lse, A.delta, B, T, H, sc, s));
   GPT2_CUDA(linear(GPT2_F32, A.dqkv, w->w_qkv, nullptr, nullptr, A.da, M, D, 3 * D, D, true, GPT2_EPI_NONE,
                    GPT2_F32, s));
   GPT2_CUDA(launch_gemm_at_f32(A.a, A.dqkv, gr->w_qkv, M, D, 3 * D, s));
-  GPT2_CUDA(launch_colsum_f32(A.dqkv, gr->b_qkv, M, 3 * D, s));
+  GPT2_CUDA(launch_colsum(A.dqkv, false, M, 3 * D, 3 * D, A.colpart, gr->b_qkv, s));
   // LN_1 and the residual path
   GPT2_CUDA(launch_ln_backward_f32(A.da, x, f(w->ln1_g), A.dh, dx, A.prod, M, D, eps, s));
-  GPT2_CUDA(launch_colsum_f32(A.prod, gr->ln1_g, M, D, s));
-  GPT2_CUDA(launch_colsum_f32(A.da, gr->ln1_b, M, D, s));
+  GPT2_CUDA(launch_colsum(A.prod, false, M, D, D, A.colpart, gr->ln1_g, s));
+  GPT2_CUDA(launch_colsum(A.da, false, M, D, D, A.colpart, gr->ln1_b, s));
   return GPT2_OK;
 }
 

@@ -27,17 +27,23 @@ __device__ __forceinline__ float warp_sum(float v) {
 template <typename T> __device__ __forceinline__ float ld_f(const T* p) { return to_f32<T>(*p); }
 
 // g = act(u): gelu_new (the hardware tanh, as the c_fc epilogue) or the
-// exact GELU; 16-bit in and out, two values per thread.
+// exact GELU; 16-bit in and out, eight values per thread.
 template <typename T16>
-__global__ void gelu_fwd_16(const T16* __restrict__ u, T16* __restrict__ g, long long n2, int exact) {
+__global__ void gelu_fwd_16(const T16* __restrict__ u, T16* __restrict__ g, long long n8, int exact) {
   griddep_wait();
   griddep_launch_dependents();
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n2) return;
-  const float2 x = Type16<T16>::unpack2(reinterpret_cast<const uint32_t*>(u)[i]);
-  const float a = exact ? gelu_exact(x.x) : gelu_new_fast(x.x);
-  const float b = exact ? gelu_exact(x.y) : gelu_new_fast(x.y);
-  reinterpret_cast<uint32_t*>(g)[i] = Type16<T16>::pack2(a, b);
+  if (i >= n8) return;
+  const uint4 in = reinterpret_cast<const uint4*>(u)[i];
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 x = Type16<T16>::unpack2(w[e]);
+    o[e] = exact ? Type16<T16>::pack2(gelu_exact(x.x), gelu_exact(x.y))
+                 : Type16<T16>::pack2(gelu_new_fast(x.x), gelu_new_fast(x.y));
+  }
+  reinterpret_cast<uint4*>(g)[i] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // du = dg * act'(u): d/du of 0.5 u (1 + tanh(k (u + 0.044715 u^3))), or of
@@ -52,15 +58,23 @@ __device__ __forceinline__ float gelu_grad(float x, int exact) {
   return 0.5f * (1.f + t) + 0.5f * x * (1.f - t * t) * k0 * fmaf(3.f * 0.044715f, x * x, 1.f);
 }
 template <typename T16>
-__global__ void gelu_bwd_16(const T16* __restrict__ dg, const T16* __restrict__ u, T16* __restrict__ du, long long n2,
+__global__ void gelu_bwd_16(const T16* __restrict__ dg, const T16* __restrict__ u, T16* __restrict__ du, long long n8,
                             int exact) {
   griddep_wait();
   griddep_launch_dependents();
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n2) return;
-  const float2 x = Type16<T16>::unpack2(reinterpret_cast<const uint32_t*>(u)[i]);
-  const float2 d = Type16<T16>::unpack2(reinterpret_cast<const uint32_t*>(dg)[i]);
-  reinterpret_cast<uint32_t*>(du)[i] = Type16<T16>::pack2(d.x * gelu_grad(x.x, exact), d.y * gelu_grad(x.y, exact));
+  if (i >= n8) return;
+  const uint4 xu = reinterpret_cast<const uint4*>(u)[i];
+  const uint4 xg = reinterpret_cast<const uint4*>(dg)[i];
+  const uint32_t wu[4] = {xu.x, xu.y, xu.z, xu.w}, wg[4] = {xg.x, xg.y, xg.z, xg.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 x = Type16<T16>::unpack2(wu[e]);
+    const float2 d = Type16<T16>::unpack2(wg[e]);
+    o[e] = Type16<T16>::pack2(d.x * gelu_grad(x.x, exact), d.y * gelu_grad(x.y, exact));
+  }
+  reinterpret_cast<uint4*>(du)[i] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // LayerNorm backward, one warp per row (the row is re-read from L1 between
@@ -109,10 +123,90 @@ __global__ void __launch_bounds__(256) ln_bwd_16(const float* __restrict__ dy, c
   }
 }
 
+// The same with the row held in registers (NV groups of four columns per
+// lane, 16-byte loads; groups past D/4 idle): x and dy are read once.
+template <typename T16, int NV>
+__global__ void __launch_bounds__(256) ln_bwd_16_reg(const float* __restrict__ dy, const float* __restrict__ x,
+                                                     const T16* __restrict__ gamma, const float* __restrict__ dres,
+                                                     float* __restrict__ dx, T16* __restrict__ dx16,
+                                                     float* __restrict__ prod, long long rows, int D, float eps) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const int nvec = D >> 2;
+  float4 xv[NV], gv[NV];
+  float gm[NV][4];
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int g = lane + 32 * i;
+    if (g < nvec) {
+      xv[i] = reinterpret_cast<const float4*>(x + r * D)[g];
+      gv[i] = reinterpret_cast<const float4*>(dy + r * D)[g];
+      const uint2 gw = reinterpret_cast<const uint2*>(gamma)[g];
+      const float2 g01 = Type16<T16>::unpack2(gw.x), g23 = Type16<T16>::unpack2(gw.y);
+      gm[i][0] = g01.x;
+      gm[i][1] = g01.y;
+      gm[i][2] = g23.x;
+      gm[i][3] = g23.y;
+    } else {
+      xv[i] = gv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      gm[i][0] = gm[i][1] = gm[i][2] = gm[i][3] = 0.f;
+    }
+    s += (xv[i].x + xv[i].y) + (xv[i].z + xv[i].w);
+  }
+  const float mean = warp_sum(s) / static_cast<float>(D);
+  float q = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    if (lane + 32 * i < nvec) {
+      const float a = xv[i].x - mean, b = xv[i].y - mean, c = xv[i].z - mean, d = xv[i].w - mean;
+      q = fmaf(a, a, fmaf(b, b, fmaf(c, c, fmaf(d, d, q))));
+    }
+  }
+  const float rstd = rsqrtf(warp_sum(q) / static_cast<float>(D) + eps);
+  float sg = 0.f, sgx = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const float xs[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w}, ds[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float g = ds[e] * gm[i][e];
+      sg += g;
+      sgx = fmaf(g, (xs[e] - mean) * rstd, sgx);
+    }
+  }
+  const float mg = warp_sum(sg) / static_cast<float>(D);
+  const float mgx = warp_sum(sgx) / static_cast<float>(D);
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int g = lane + 32 * i;
+    if (g >= nvec) continue;
+    const float xs[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w}, ds[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
+    float o[4], pr[4];
+    const float4 rr = dres ? reinterpret_cast<const float4*>(dres + r * D)[g] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float rs[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float xh = (xs[e] - mean) * rstd;
+      o[e] = rstd * (ds[e] * gm[i][e] - mg - xh * mgx) + rs[e];
+      pr[e] = ds[e] * xh;
+    }
+    reinterpret_cast<float4*>(dx + r * D)[g] = make_float4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<float4*>(prod + r * D)[g] = make_float4(pr[0], pr[1], pr[2], pr[3]);
+    if (dx16)
+      reinterpret_cast<uint2*>(dx16 + r * D)[g] =
+          make_uint2(Type16<T16>::pack2(o[0], o[1]), Type16<T16>::pack2(o[2], o[3]));
+  }
+}
+
 // Column sums, level 1: block (column tile of 64, row chunk of kChunk rows):
-// 4 groups of 64 threads sum rows group, group + 4, ... of the chunk, then
-// the 4 partials are added in order.  partial[chunk][col].
-constexpr int kChunk = 256;
+// 4 groups of 64 threads take rows group, group + 4, ... of the chunk (16
+// rows each, loaded together and added in a fixed tree), then the 4 group
+// sums are added in order.  partial[chunk][col].
+constexpr int kChunk = 64;
 template <typename T>
 __global__ void __launch_bounds__(256) colsum_partial(const T* __restrict__ in, long long M, int N, long long ld,
                                                       float* __restrict__ partial) {
@@ -121,12 +215,18 @@ __global__ void __launch_bounds__(256) colsum_partial(const T* __restrict__ in, 
   __shared__ float part[4][64];
   const int col = blockIdx.x * 64 + (threadIdx.x & 63);
   const int grp = threadIdx.x >> 6;
-  const long long r0 = static_cast<long long>(blockIdx.y) * kChunk;
-  float s = 0.f;
-  if (col < N) {
-    for (long long r = r0 + grp; r < r0 + kChunk && r < M; r += 4) s += ld_f(in + r * ld + col);
+  const long long r0 = static_cast<long long>(blockIdx.y) * kChunk + grp;
+  float v[kChunk / 4];
+#pragma unroll
+  for (int i = 0; i < kChunk / 4; ++i) {
+    const long long r = r0 + 4 * i;
+    v[i] = (col < N && r < M) ? ld_f(in + r * ld + col) : 0.f;
   }
-  part[grp][threadIdx.x & 63] = s;
+#pragma unroll
+  for (int w = kChunk / 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) v[i] += v[i + w];
+  part[grp][threadIdx.x & 63] = v[0];
   __syncthreads();
   if (grp == 0 && col < N)
     partial[static_cast<long long>(blockIdx.y) * N + col] = ((part[0][threadIdx.x] + part[1][threadIdx.x]) +
@@ -138,9 +238,13 @@ __global__ void colsum_final(const float* __restrict__ partial, int chunks, int 
   griddep_launch_dependents();
   const int col = blockIdx.x * blockDim.x + threadIdx.x;
   if (col >= N) return;
-  float s = 0.f;
-  for (int c = 0; c < chunks; ++c) s += partial[static_cast<long long>(c) * N + col];
-  out[col] = s;
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
+  int c = 0;
+  for (; c + 4 <= chunks; c += 4)
+#pragma unroll
+    for (int u = 0; u < 4; ++u) a[u] += partial[static_cast<long long>(c + u) * N + col];
+  for (; c < chunks; ++c) a[0] += partial[static_cast<long long>(c) * N + col];
+  out[col] = (a[0] + a[1]) + (a[2] + a[3]);
 }
 
 // dwte[token] += the gradient of every position that used the token: the
@@ -218,20 +322,35 @@ cudaError_t launch_colsum(const void* in, bool in16, long long M, int N, long lo
 
 cudaError_t launch_gelu_fwd_16(const void* u, void* g, long long n, bool exact, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  return launch_pdl(gelu_fwd_16<__nv_bfloat16>, dim3(blocks_for(n / 2, 256)), 256, 0, s, 0,
-                    static_cast<const __nv_bfloat16*>(u), static_cast<__nv_bfloat16*>(g), n / 2, exact ? 1 : 0);
+  return launch_pdl(gelu_fwd_16<__nv_bfloat16>, dim3(blocks_for(n / 8, 256)), 256, 0, s, 0,
+                    static_cast<const __nv_bfloat16*>(u), static_cast<__nv_bfloat16*>(g), n / 8, exact ? 1 : 0);
 }
 
 cudaError_t launch_gelu_bwd_16(const void* dg, const void* u, void* du, long long n, bool exact, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  return launch_pdl(gelu_bwd_16<__nv_bfloat16>, dim3(blocks_for(n / 2, 256)), 256, 0, s, 0,
+  return launch_pdl(gelu_bwd_16<__nv_bfloat16>, dim3(blocks_for(n / 8, 256)), 256, 0, s, 0,
                     static_cast<const __nv_bfloat16*>(dg), static_cast<const __nv_bfloat16*>(u),
-                    static_cast<__nv_bfloat16*>(du), n / 2, exact ? 1 : 0);
+                    static_cast<__nv_bfloat16*>(du), n / 8, exact ? 1 : 0);
+}
+
+template <int NV>
+cudaError_t ln_bwd_reg(const float* dy, const float* x, const void* gamma, const float* dres, float* dx, void* dx16,
+                       float* prod, long long rows, int D, float eps, cudaStream_t s) {
+  return launch_pdl(ln_bwd_16_reg<__nv_bfloat16, NV>, dim3(blocks_for(rows, 8)), 256, 0, s, 0, dy, x,
+                    static_cast<const __nv_bfloat16*>(gamma), dres, dx, static_cast<__nv_bfloat16*>(dx16), prod, rows,
+                    D, eps);
 }
 
 cudaError_t launch_ln_bwd_16(const float* dy, const float* x, const void* gamma, const float* dres, float* dx,
                              void* dx16, float* prod, long long rows, int D, float eps, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
+  // the row in registers up to 13 float4 groups per lane (D <= 1664)
+  const int nv = (D + 127) / 128;
+  if (nv <= 2) return ln_bwd_reg<2>(dy, x, gamma, dres, dx, dx16, prod, rows, D, eps, s);
+  if (nv <= 4) return ln_bwd_reg<4>(dy, x, gamma, dres, dx, dx16, prod, rows, D, eps, s);
+  if (nv <= 6) return ln_bwd_reg<6>(dy, x, gamma, dres, dx, dx16, prod, rows, D, eps, s);
+  if (nv <= 8) return ln_bwd_reg<8>(dy, x, gamma, dres, dx, dx16, prod, rows, D, eps, s);
+  if (nv <= 13) return ln_bwd_reg<13>(dy, x, gamma, dres, dx, dx16, prod, rows, D, eps, s);
   return launch_pdl(ln_bwd_16<__nv_bfloat16>, dim3(blocks_for(rows, 8)), 256, 0, s, 0, dy, x,
                     static_cast<const __nv_bfloat16*>(gamma), dres, dx, static_cast<__nv_bfloat16*>(dx16), prod, rows,
                     D, eps);

@@ -95,16 +95,6 @@ __global__ void __launch_bounds__(256) gemm_at_f32(const float* __restrict__ x, 
   }
 }
 
-// out[n] = sum over m of in[m, n], rows in order (one thread per column).
-__global__ void __launch_bounds__(256) colsum_f32(const float* __restrict__ in, float* __restrict__ out, int M,
-                                                  int N) {
-  const int n = blockIdx.x * 256 + threadIdx.x;
-  if (n >= N) return;
-  float s = 0.f;
-  for (int m = 0; m < M; ++m) s += in[static_cast<long long>(m) * N + n];
-  out[n] = s;
-}
-
 // One warp per row: dx = rstd (dxhat - mean(dxhat) - xhat mean(dxhat xhat))
 // (+ dres, the gradient arriving through the residual path, when given);
 // prod[row] = dy * xhat for the dgamma column sums.
@@ -309,11 +299,6 @@ cudaError_t launch_gemm_at_f32(const float* x, const float* dy, float* dw, int64
   return cudaGetLastError();
 }
 
-cudaError_t launch_colsum_f32(const float* in, float* out, int64_t M, int N, cudaStream_t stream) {
-  if (N == 0) return cudaSuccess;
-  colsum_f32<<<(N + 255) / 256, 256, 0, stream>>>(in, out, static_cast<int>(M), N);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_ln_backward_f32(const float* dy, const float* x, const float* gamma, const float* dres, float* dx,
                                    float* prod, int64_t rows, int D, float eps, cudaStream_t stream) {

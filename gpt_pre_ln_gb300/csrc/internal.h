@@ -167,8 +167,8 @@ cudaError_t launch_argmax_candidates(const float2* cand, int n_cand, int B, cons
 size_t colsum_partial_bytes(long long M, int N);
 cudaError_t launch_colsum(const void* in, bool in16, long long M, int N, long long ld, float* partial, float* out,
                           cudaStream_t s);
-// g = act(u) and du = dg * act'(u) over n (even) bf16 values; act gelu_new
-// or, with exact, x Phi(x).
+// g = act(u) and du = dg * act'(u) over n bf16 values (n a multiple of 8,
+// buffers 16-byte aligned); act gelu_new or, with exact, x Phi(x).
 cudaError_t launch_gelu_fwd_16(const void* u, void* g, long long n, bool exact, cudaStream_t s);
 cudaError_t launch_gelu_bwd_16(const void* dg, const void* u, void* du, long long n, bool exact, cudaStream_t s);
 // LayerNorm backward (gamma bf16): dx = LN'(x)^T dy (+ dres), dx16 (nullable)
@@ -184,8 +184,6 @@ cudaError_t launch_embed_bwd(const int32_t* tokens, const float* dx0, float* dwt
 // dw[K, N] = x[M, K]^T dy[M, N].
 cudaError_t launch_gemm_at_f32(const float* x, const float* dy, float* dw, int64_t M, int K, int N,
                                cudaStream_t stream);
-// out[N] = column sums of in[M, N], rows in order.
-cudaError_t launch_colsum_f32(const float* in, float* out, int64_t M, int N, cudaStream_t stream);
 // LayerNorm backward: dx = LN'(x)^T dy (+ dres when not null), prod = dy * xhat.
 cudaError_t launch_ln_backward_f32(const float* dy, const float* x, const float* gamma, const float* dres, float* dx,
                                    float* prod, int64_t rows, int D, float eps, cudaStream_t stream);
