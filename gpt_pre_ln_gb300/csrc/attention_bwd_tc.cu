@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(kv_empty(s), 1);
     }
     mbar_init(sdp_full, 1);
-    mbar_init(ds_ready, 128);
+    mbar_init(ds_ready, 4);  // one arrival per element-wise warp
     mbar_init(dq_done, 1);
     mbar_init(drain, 1);
     fence_barrier_init();
@@ -274,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(ds_ready);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_ready);
     }
     if (ok && n_kt > 0) {
       if (!__all_sync(0xffffffffu, mbar_wait(dq_done, static_cast<uint32_t>((n_kt - 1) & 1)))) {
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(qd_empty(s), 1);
     }
     mbar_init(sdp_full, 1);
-    mbar_init(pds_ready, 128);
+    mbar_init(pds_ready, 4);  // one arrival per element-wise warp
     mbar_init(dkv_done, 1);
     mbar_init(drain, 1);
     fence_barrier_init();
@@ -514,7 +515,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(pds_ready);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pds_ready);
     }
     if (ok && n_i > 0) {
       if (!__all_sync(0xffffffffu, mbar_wait(dkv_done, static_cast<uint32_t>((n_i - 1) & 1)))) {

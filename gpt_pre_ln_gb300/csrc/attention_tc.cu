@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
       mbar_init(v_empty(s), 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_ready, 128);
+    mbar_init(p_ready, 4);  // one arrival per softmax warp
     mbar_init(pv_done, 1);
     mbar_init(drain, 1);
     fence_barrier_init();
@@ -422,7 +422,8 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         l += ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y)) + ((ps[2].x + ps[2].y) + (ps[3].x + ps[3].y));
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(p_ready);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_ready);
       }
       if (!ok) break;
       // the item's last P.V has completed when pv_done reaches phase g - 1

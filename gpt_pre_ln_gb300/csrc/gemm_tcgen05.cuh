@@ -257,13 +257,20 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
     if (lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
   };
+  // one arrival per warp, once all its lanes have read, made by lane 31:
+  // lane 0 issues the warp's TMA stores, and an arrival (a release) from
+  // that lane waited for its stores in flight to reach memory (3-6k cycles
+  // per tile)
   auto arrive_empty = [&](int acc) {
     tc_fence_before();
-    const uint32_t tempty = acc ? tempty1 : tempty0;
-    if (CLUSTER_ARRIVE)
-      mbar_arrive_cluster(tempty);
-    else
-      mbar_arrive(tempty);
+    __syncwarp();
+    if (lane == 31) {
+      const uint32_t tempty = acc ? tempty1 : tempty0;
+      if (CLUSTER_ARRIVE)
+        mbar_arrive_cluster(tempty);
+      else
+        mbar_arrive(tempty);
+    }
   };
 
   // EPI_RES: the residual of a chunk (32 fp32 columns from col0) of this
@@ -458,7 +465,7 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
     }
     if constexpr (kBiasSmem) {
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc ? bias_empty1 : bias_empty0);  // this warp has read the tile's bias
+      if (lane == 31) mbar_arrive(acc ? bias_empty1 : bias_empty0);  // this warp has read the tile's bias (lane 0: see arrive_empty)
     }
     if constexpr (EPI == EPI_LSE) {
       // slice (n0 / BN) * 2 + half; lanes write consecutive rows
@@ -528,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), kEpiThreads);  // every epilogue thread, once per tile
+      mbar_init(tempty_bar(a), kEpiWarps);  // every epilogue warp, once per tile
       mbar_init(bias_full_bar(a), 1);
       mbar_init(bias_empty_bar(a), kEpiWarps);
     }
@@ -711,7 +718,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 2 * kEpiThreads);  // both CTAs' epilogue threads
+      mbar_init(tempty_bar(a), 2 * kEpiWarps);  // both CTAs' epilogue warps
       mbar_init(bias_full_bar(a), 1);
       mbar_init(bias_empty_bar(a), kEpiWarps);
     }
