@@ -75,7 +75,7 @@ using namespace gpt2;
 
 namespace {
 
-constexpr int kAbiVersion = 3;
+constexpr int kAbiVersion = 4;
 
 // ------------------------------------------------------------- profiler
 struct ProfRec {

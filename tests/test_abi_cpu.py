@@ -63,7 +63,7 @@ def test_struct_layout_matches_header(L):
 
 
 def test_status_strings(L):
-    assert G.gpt2_abi_version() == 3
+    assert G.gpt2_abi_version() == 4
     assert G.gpt2_status_string(0) == "ok"
     assert "workspace" in G.gpt2_status_string(3)
 

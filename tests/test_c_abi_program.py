@@ -55,7 +55,7 @@ def test_c_program_uses_the_abi(tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, r.stderr
     out = dict(line.split(" ", 1) for line in r.stdout.strip().splitlines())
-    assert out["abi"] == "3"
+    assert out["abi"] == "4"
     assert out["status3"] == "workspace too small"
     M = 8 * 1024
     assert int(out["ws"]) == 2 * M * 768 * 4 + 2 * M * 768 * 2 + M * 3 * 768 * 2 + M * 3072 * 2
