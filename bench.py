@@ -700,11 +700,14 @@ def _traffic_from_profile():
     it was taken on the current kernel source."""
     import hashlib
     summ = os.path.join(ROOT, "profiles", "gemm_bf16_tcgen05_gpt2_small_fwd.md")
-    src = os.path.join(ROOT, "gpt_pre_ln_gb300", "csrc", "gemm_tcgen05.cu")
+    srcs = [os.path.join(ROOT, "gpt_pre_ln_gb300", "csrc", f) for f in ("gemm_tcgen05.cuh", "gemm_tcgen05.cu")]
     if not os.path.exists(summ):
         return None
-    with open(src, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for src in srcs:
+        with open(src, "rb") as f:
+            h.update(f.read())
+    sha = h.hexdigest()[:16]
     for line in open(summ):
         if line.startswith("traffic_bytes_per_launch:"):
             parts = line.split()
@@ -915,9 +918,27 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--oracle-samples", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--only", choices=["decode", "train", "layernorm"],
+                    help="run one secondary entry alone and print its JSON (for profiling runs)")
     args = ap.parse_args()
     if args.oracle_samples:
         print(json.dumps(_oracle_samples()), flush=True)
+        return
+    if args.only:
+        import torch
+
+        import gpt_pre_ln_gb300 as G
+        from gpt_pre_ln_gb300 import build as _b
+        _b.build()
+        G.lib()
+        peaks = _peaks()
+        if args.only == "decode":
+            r = _decode_measure(G, torch, steps=args.steps)
+        elif args.only == "train":
+            r = _train_measure(G, torch, peaks, steps=args.steps)
+        else:
+            r = _layernorm_micro(G, torch, peaks, reps=args.steps)
+        print(json.dumps(r), flush=True)
         return
     if args.impl == "reference":
         run_reference(args)

@@ -575,7 +575,8 @@ struct TrainBufs {
   float2* part;
   int64_t ldz;
   void* dz;
-  float *dx, *dh, *dyf, *prod, *delta, *colpart;
+  float *dx, *dh, *dyf, *prod, *delta, *colpart, *splitk;
+  size_t splitk_bytes;
   void *dxb, *dhb, *dgb, *dub, *dob, *dqkvb;
   size_t bytes;
 };
@@ -621,6 +622,15 @@ TrainBufs carve_train(void* ws, const gpt2_dims* d, int B, int T) {
   t.delta = static_cast<float*>(take(static_cast<size_t>(B) * H * T * 4));
   const size_t widest = std::max<size_t>({3 * D, F, D});
   t.colpart = static_cast<float*>(take(colsum_partial_bytes(static_cast<long long>(M), static_cast<int>(widest))));
+  {
+    // fp32 partial slabs of the split-K weight-gradient products
+    const int Mi = static_cast<int>(M), Di = static_cast<int>(D), Fi = static_cast<int>(F);
+    size_t sk = 0;
+    const int shapes[5][2] = {{Di, 3 * Di}, {Di, Di}, {Di, Fi}, {Fi, Di}, {static_cast<int>(V), Di}};
+    for (const auto& sh : shapes) sk = std::max(sk, gemm_grad_scratch_bytes(sh[0], sh[1], Mi));
+    t.splitk_bytes = sk;
+    t.splitk = static_cast<float*>(take(sk));
+  }
   t.dxb = take(M * D * 2);
   t.dhb = take(M * D * 2);
   t.dgb = take(M * F * 2);
@@ -648,11 +658,13 @@ int check_grads(const gpt2_dims* d, const gpt2_model_grads* g) {
 
 // One tensor-core GEMM of the backward, profiled like the forward's.
 cudaError_t grad_gemm(const void* a, long long lda, bool a_mn, const void* w, long long ldw, bool w_kn, void* y,
-                      long long ldy, gpt2_dtype y_t, int64_t M, int N, int K, cudaStream_t s) {
+                      long long ldy, gpt2_dtype y_t, int64_t M, int N, int K, cudaStream_t s,
+                      float* scratch = nullptr, size_t scratch_bytes = 0) {
   ProfScope prof("gemm_grad_bf16_tcgen05", 2.0 * M * N * K,
                  (static_cast<double>(M) * K + static_cast<double>(K) * N) * 2.0 + static_cast<double>(M) * N * esize(y_t),
                  s);
-  return launch_gemm_grad(a, lda, a_mn, w, ldw, w_kn, y, ldy, y_t, static_cast<int>(M), N, K, s);
+  return launch_gemm_grad(a, lda, a_mn, w, ldw, w_kn, y, ldy, y_t, static_cast<int>(M), N, K, s, scratch,
+                          scratch_bytes);
 }
 
 cudaError_t colsum(const void* in, bool in16, int64_t M, int N, float* partial, float* out, cudaStream_t s) {
@@ -726,7 +738,7 @@ int forward_backward(const gpt2_dims* d, const gpt2_model_weights* w, const int3
     GPT2_CUDA(launch_gemm_dlogits(t.xf, w->wte, static_cast<int>(M), V, D, t.row_lse, labels, T, inv_n, t.dz, t.ldz,
                                   s));
   }
-  GPT2_CUDA(grad_gemm(t.dz, t.ldz, true, t.xf, D, true, gr->wte, D, GPT2_F32, V, D, static_cast<int>(M), s));
+  GPT2_CUDA(grad_gemm(t.dz, t.ldz, true, t.xf, D, true, gr->wte, D, GPT2_F32, V, D, static_cast<int>(M), s, t.splitk, t.splitk_bytes));
   GPT2_CUDA(grad_gemm(t.dz, t.ldz, false, w->wte, D, true, t.dyf, D, GPT2_F32, M, D, V, s));
   GPT2_CUDA(ln_bwd(t.dyf, t.xL, w->lnf_g, nullptr, t.dx, t.dxb, t.prod, M, D, eps, s));
   GPT2_CUDA(colsum(t.prod, false, M, D, t.colpart, gr->lnf_g, s));
@@ -739,7 +751,7 @@ int forward_backward(const gpt2_dims* d, const gpt2_model_weights* w, const int3
     TrainLayer& y = t.L[l];
     // x' = h + g W_proj + b_proj
     GPT2_CUDA(grad_gemm(t.dxb, D, false, bw->w_proj, D, false, t.dgb, F, dt, M, F, D, s));
-    GPT2_CUDA(grad_gemm(y.g, F, true, t.dxb, D, true, bg->w_proj, D, GPT2_F32, F, D, Mi, s));
+    GPT2_CUDA(grad_gemm(y.g, F, true, t.dxb, D, true, bg->w_proj, D, GPT2_F32, F, D, Mi, s, t.splitk, t.splitk_bytes));
     GPT2_CUDA(colsum(t.dx, false, M, D, t.colpart, bg->b_proj, s));
     {
       ProfScope prof("gelu_bwd", 20.0 * M * F, 6.0 * M * F, s);
@@ -747,7 +759,7 @@ int forward_backward(const gpt2_dims* d, const gpt2_model_weights* w, const int3
     }
     // u = a2 W_fc + b_fc
     GPT2_CUDA(grad_gemm(t.dub, F, false, bw->w_fc, F, false, t.dyf, D, GPT2_F32, M, D, F, s));
-    GPT2_CUDA(grad_gemm(y.a2, D, true, t.dub, F, true, bg->w_fc, F, GPT2_F32, D, F, Mi, s));
+    GPT2_CUDA(grad_gemm(y.a2, D, true, t.dub, F, true, bg->w_fc, F, GPT2_F32, D, F, Mi, s, t.splitk, t.splitk_bytes));
     GPT2_CUDA(colsum(t.dub, true, M, F, t.colpart, bg->b_fc, s));
     // a2 = LN_2(h), and the residual path: dh = dx' + LN_2'(h)^T da2
     GPT2_CUDA(ln_bwd(t.dyf, y.h, bw->ln2_g, t.dx, t.dh, t.dhb, t.prod, M, D, eps, s));
@@ -755,7 +767,7 @@ int forward_backward(const gpt2_dims* d, const gpt2_model_weights* w, const int3
     GPT2_CUDA(colsum(t.dyf, false, M, D, t.colpart, bg->ln2_b, s));
     // h = x + o W_o + b_o
     GPT2_CUDA(grad_gemm(t.dhb, D, false, bw->w_o, D, false, t.dob, D, dt, M, D, D, s));
-    GPT2_CUDA(grad_gemm(y.o, D, true, t.dhb, D, true, bg->w_o, D, GPT2_F32, D, D, Mi, s));
+    GPT2_CUDA(grad_gemm(y.o, D, true, t.dhb, D, true, bg->w_o, D, GPT2_F32, D, D, Mi, s, t.splitk, t.splitk_bytes));
     GPT2_CUDA(colsum(t.dh, false, M, D, t.colpart, bg->b_o, s));
     // o = attention(qkv)
     {
@@ -766,7 +778,7 @@ int forward_backward(const gpt2_dims* d, const gpt2_model_weights* w, const int3
     }
     // qkv = a W_qkv + b_qkv
     GPT2_CUDA(grad_gemm(t.dqkvb, 3 * D, false, bw->w_qkv, 3 * D, false, t.dyf, D, GPT2_F32, M, D, 3 * D, s));
-    GPT2_CUDA(grad_gemm(y.a, D, true, t.dqkvb, 3 * D, true, bg->w_qkv, 3 * D, GPT2_F32, D, 3 * D, Mi, s));
+    GPT2_CUDA(grad_gemm(y.a, D, true, t.dqkvb, 3 * D, true, bg->w_qkv, 3 * D, GPT2_F32, D, 3 * D, Mi, s, t.splitk, t.splitk_bytes));
     GPT2_CUDA(colsum(t.dqkvb, true, M, 3 * D, t.colpart, bg->b_qkv, s));
     // a = LN_1(x), and the residual path: dx = dh + LN_1'(x)^T da
     GPT2_CUDA(ln_bwd(t.dyf, y.x, bw->ln1_g, t.dh, t.dx, t.dxb, t.prod, M, D, eps, s));

@@ -186,6 +186,12 @@ struct EpiArgs {
   // sequence (labels, T as for EPI_LSE)
   const float* row_lse;
   float inv_n;
+  // split K (EPI_NONE with fp32 output only; M a multiple of 32, so that
+  // no 32-row store box crosses into the next slab): S > 1 splits the
+  // k-blocks of every tile into S ranges, tile (t, s) accumulating range s
+  // and storing its partial into rows s M .. s M + M - 1 of the output (S
+  // stacked [M, N] slabs, summed afterwards); 0 or 1: no split
+  int splits;
 };
 
 // EPI_LSE: one 32-column chunk of a row's logits into the running (m, s) of
@@ -238,7 +244,7 @@ __device__ __forceinline__ void lse_chunk(float (&v)[32], int col0, int N, int l
 //   MMAs), and transposes it through its staging area just before the
 //   chunk's output goes there: the loads overlap the MMAs, which never wait
 //   for them.
-template <int BN, int EPI, typename OutT, typename T16, bool CLUSTER_ARRIVE>
+template <int BN, int EPI, typename OutT, typename T16, bool CLUSTER_ARRIVE, bool SPLITK>
 __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const CUtensorMap* tmY, int warp, int lane,
                                               uint32_t stage_base, uint32_t bias_s, uint32_t bias_full0,
                                               uint32_t bias_full1, uint32_t bias_empty0, uint32_t bias_empty1,
@@ -287,12 +293,16 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
     }
   };
 
+  const int n_splits = SPLITK && a.splits > 1 ? a.splits : 1;
+  const int tiles_per_split = num_tiles / n_splits;
   int t_local = 0;
   for (int tile = tile_begin; tile < num_tiles; tile += tile_stride, ++t_local) {
     const int acc = t_local & 1;
     const uint32_t acc_par = (t_local >> 1) & 1;
-    const int m0 = (tile % m_units) * unit_rows + row_off;
-    const int n0 = (tile / m_units) * BN;
+    const int tt = SPLITK ? tile % tiles_per_split : tile;
+    const int row_shift = SPLITK ? (tile / tiles_per_split) * M : 0;  // the split's slab
+    const int m0 = (tt % m_units) * unit_rows + row_off;
+    const int n0 = (tt / m_units) * BN;
     const int row0 = m0 + quad * 32;  // first row of this warp
     const int valid_cols = N - n0 < BN ? N - n0 : BN;
     const int nch = (valid_cols + CW - 1) / CW;
@@ -459,7 +469,7 @@ __device__ __forceinline__ void epilogue_role(const EpiArgs<OutT, T16>& a, const
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0 && row0 < M) {  // (a box wholly below row M writes nothing)
-        tma_store_2d(tmY, stage_w, col0, row0);
+        tma_store_2d(tmY, stage_w, col0, row0 + row_shift);
         bulk_commit_group();
       }
     }
@@ -521,9 +531,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int M = ea.M, N = ea.N;
   const int m_tiles = (M + kBM - 1) / kBM;
   const int n_tiles = (N + BN - 1) / BN;
-  const int num_tiles = m_tiles * n_tiles;
+  // split K only in the weight-gradient instantiations (A MN-major)
+  constexpr bool kSplit = A_MN;
+  const int n_splits = kSplit && ea.splits > 1 ? ea.splits : 1;
+  const int tiles_per_split = m_tiles * n_tiles;
+  const int num_tiles = tiles_per_split * n_splits;
   const int tile0 = blockIdx.x, tile_step = gridDim.x;
   const int k_blocks = (K + kBK - 1) / kBK;  // k-blocks past K read zeros
+  // k-blocks [kb_lo, kb_hi) of a tile (its split's share)
+  auto kb_range = [&](int tile, int& kb_lo, int& kb_hi) {
+    if constexpr (kSplit) {
+      const int sp = tile / tiles_per_split;
+      kb_lo = sp * k_blocks / n_splits;
+      kb_hi = (sp + 1) * k_blocks / n_splits;
+    } else {
+      kb_lo = 0;
+      kb_hi = k_blocks;
+    }
+  };
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmA);
@@ -561,9 +586,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       long long issued = 0;
       bool ok = true;
       for (int tile = tile0; tile < num_tiles && ok; tile += tile_step) {
-        const int m0 = (tile % m_tiles) * kBM;
-        const int n0 = (tile / m_tiles) * BN;
-        for (int kb = 0; kb < k_blocks; ++kb) {
+        const int tt = kSplit ? tile % tiles_per_split : tile;
+        const int m0 = (tt % m_tiles) * kBM;
+        const int n0 = (tt / m_tiles) * BN;
+        int kb_lo, kb_hi;
+        kb_range(tile, kb_lo, kb_hi);
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1)) {
             record_error(err, kErrTimeout, kSiteGemmProducer);
             ok = false;
@@ -615,7 +643,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < k_blocks; ++kb) {
+        int kb_lo, kb_hi;
+        kb_range(tile, kb_lo, kb_hi);
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(full_bar(stage), phase)) {
             record_error(err, kErrTimeout, kSiteGemmMma);
             ok = false;
@@ -638,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               bdesc = sdesc_sw128(b_base + k * 32, 16, 1024);
             }
-            umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_bf16(d_tmem, adesc, bdesc, idesc, (kb != kb_lo || k != 0) ? 1u : 0u);
             any = true;
           }
           umma_commit(empty_bar(stage));
@@ -657,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    epilogue_role<BN, EPI, OutT, T16, false>(ea, &tmY, warp, lane, smem_u32(sOut), smem_u32(sBias), bias_full_bar(0),
+    epilogue_role<BN, EPI, OutT, T16, false, A_MN>(ea, &tmY, warp, lane, smem_u32(sOut), smem_u32(sBias), bias_full_bar(0),
                                          bias_full_bar(1), bias_empty_bar(0), bias_empty_bar(1), tmem_base,
                                          tfull_bar(0), tfull_bar(1),
                                          tempty_bar(0), tempty_bar(1), tile0, tile_step, num_tiles, m_tiles, kBM, 0);
@@ -705,8 +735,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int M = ea.M, N = ea.N;
   const int m_units = (M + 2 * kBM - 1) / (2 * kBM);
   const int n_tiles = (N + kPairBN - 1) / kPairBN;
-  const int num_tiles = m_units * n_tiles;
+  constexpr bool kSplit = A_MN;  // split K only for the weight gradients
+  const int n_splits = kSplit && ea.splits > 1 ? ea.splits : 1;
+  const int tiles_per_split = m_units * n_tiles;
+  const int num_tiles = tiles_per_split * n_splits;
   const int k_blocks = (K + kBK - 1) / kBK;  // k-blocks past K read zeros
+  auto kb_range = [&](int tile, int& kb_lo, int& kb_hi) {
+    if constexpr (kSplit) {
+      const int sp = tile / tiles_per_split;
+      kb_lo = sp * k_blocks / n_splits;
+      kb_hi = (sp + 1) * k_blocks / n_splits;
+    } else {
+      kb_lo = 0;
+      kb_hi = k_blocks;
+    }
+  };
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmA);
@@ -744,9 +787,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       long long issued = 0;
       bool ok = true;
       for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
-        const int m0 = (tile % m_units) * (2 * kBM) + static_cast<int>(rank) * kBM;
-        const int nb = (tile / m_units) * kPairBN + static_cast<int>(rank) * (kPairBN / 2);
-        for (int kb = 0; kb < k_blocks; ++kb) {
+        const int tt = kSplit ? tile % tiles_per_split : tile;
+        const int m0 = (tt % m_units) * (2 * kBM) + static_cast<int>(rank) * kBM;
+        const int nb = (tt / m_units) * kPairBN + static_cast<int>(rank) * (kPairBN / 2);
+        int kb_lo, kb_hi;
+        kb_range(tile, kb_lo, kb_hi);
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1)) {
             record_error(err, kErrTimeout, kSiteGemmProducer);
             ok = false;
@@ -799,7 +845,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kPairBN;
-        for (int kb = 0; kb < k_blocks; ++kb) {
+        int kb_lo, kb_hi;
+        kb_range(tile, kb_lo, kb_hi);
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(full_bar(stage), phase)) {
             record_error(err, kErrTimeout, kSiteGemmMma);
             ok = false;
@@ -818,7 +866,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             } else {
               bdesc = sdesc_sw128(b_base + k * 32, 16, 1024);
             }
-            umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb != kb_lo || k != 0) ? 1u : 0u);
             any = true;
           }
           umma_commit_pair_multicast(empty_bar(stage), kBoth);
@@ -836,7 +884,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    epilogue_role<kPairBN, EPI, OutT, T16, true>(ea, &tmY, warp, lane, smem_u32(sOut), smem_u32(sBias),
+    epilogue_role<kPairBN, EPI, OutT, T16, true, A_MN>(ea, &tmY, warp, lane, smem_u32(sOut), smem_u32(sBias),
                                             bias_full_bar(0), bias_full_bar(1), bias_empty_bar(0), bias_empty_bar(1),
                                             tmem_base, tfull_bar(0), tfull_bar(1),
                                             mapa_shared(tempty_bar(0), 0), mapa_shared(tempty_bar(1), 0), pair,
@@ -898,7 +946,8 @@ template <typename OutT, typename T16>
 bool make_out_map(CUtensorMap* map, const EpiArgs<OutT, T16>& ea) {
   constexpr int esz = static_cast<int>(sizeof(OutT));
   const uint64_t n16 = (static_cast<uint64_t>(ea.N) * esz + 15) / 16 * 16 / esz;
-  return encode_tma_2d(map, out_tma_type<OutT>(), ea.out, n16, static_cast<uint64_t>(ea.M),
+  const uint64_t slabs = ea.splits > 1 ? static_cast<uint64_t>(ea.splits) : 1;
+  return encode_tma_2d(map, out_tma_type<OutT>(), ea.out, n16, static_cast<uint64_t>(ea.M) * slabs,
                        static_cast<uint64_t>(ea.ldo) * esz, 128 / esz, 32);
 }
 
@@ -925,7 +974,7 @@ cudaError_t run_1sm(const Ops<T16>& op, const EpiArgs<OutT, T16>& ea, cudaStream
   const int m_tiles = (M + kBM - 1) / kBM;
   CUtensorMap ta, tb;
   if (!make_operand_maps<A_MN, B_MN>(&ta, &tb, op, M, N, BN)) return cudaErrorInvalidValue;
-  const int tiles = m_tiles * ((N + BN - 1) / BN);
+  const int tiles = m_tiles * ((N + BN - 1) / BN) * (ea.splits > 1 ? ea.splits : 1);
   const int ctas = tiles < num_sms() ? tiles : num_sms();
   CUtensorMap ty = ta;  // EPI_LSE stores no tile (a valid map, never used)
   if (EPI != EPI_LSE && !make_out_map(&ty, ea)) return cudaErrorInvalidValue;
@@ -963,7 +1012,7 @@ cudaError_t run_2sm(const Ops<T16>& op, const EpiArgs<OutT, T16>& ea, cudaStream
     max_pairs[dev] = n < num_sms() / 2 ? n : num_sms() / 2;
   }
   const int pairs_max = (dev >= 0 && dev < 64) ? max_pairs[dev] : num_sms() / 2;
-  const int tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kPairBN - 1) / kPairBN);
+  const int tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kPairBN - 1) / kPairBN) * (ea.splits > 1 ? ea.splits : 1);
   const int pairs = tiles < pairs_max ? tiles : pairs_max;
   CUtensorMap ty = ta;  // EPI_LSE stores no tile (a valid map, never used)
   if (EPI != EPI_LSE && !make_out_map(&ty, ea)) return cudaErrorInvalidValue;

@@ -79,8 +79,13 @@ cudaError_t launch_gemm_lse_16(gpt2_dtype dt, const void* x, const void* w, int6
 //   y[M, N] = op(A) op(W) with A [M, K] (pitch lda) or, with a_mn, [K, M];
 //   W [N, K] (pitch ldw) or, with w_kn, [K, N]; K any positive extent.
 //   y fp32, or bf16 when neither a_mn nor w_kn.
+//   With a_mn (weight gradients: few output tiles, K = the batch's rows) K
+//   may be split over the SMs into fp32 partial slabs in `scratch` (at least
+//   gemm_grad_scratch_bytes(M, N, K)), summed afterwards in a fixed order.
 cudaError_t launch_gemm_grad(const void* a, long long lda, bool a_mn, const void* w, long long ldw, bool w_kn,
-                             void* y, long long ldy, gpt2_dtype y_t, int M, int N, int K, cudaStream_t s);
+                             void* y, long long ldy, gpt2_dtype y_t, int M, int N, int K, cudaStream_t s,
+                             float* scratch = nullptr, size_t scratch_bytes = 0);
+size_t gemm_grad_scratch_bytes(int M, int N, int K);
 // The loss gradient with respect to the logits z = xf wte^T (bf16 [M, D] x
 // [V, D]), written as bf16 dz [M, lddz]: (exp(z - row_lse) - [v == label])
 // * inv_n at row r with label labels[r + 1]; zero in the last row of every
