@@ -575,7 +575,7 @@ struct TrainBufs {
   float2* part;
   int64_t ldz;
   void* dz;
-  float *dx, *dh, *dyf, *prod, *delta, *colpart, *splitk;
+  float *dx, *dh, *dyf, *delta, *colpart, *splitk;
   size_t splitk_bytes;
   void *dxb, *dhb, *dgb, *dub, *dob, *dqkvb;
   size_t bytes;
@@ -618,10 +618,13 @@ TrainBufs carve_train(void* ws, const gpt2_dims* d, int B, int T) {
   t.dx = static_cast<float*>(take(M * D * 4));
   t.dh = static_cast<float*>(take(M * D * 4));
   t.dyf = static_cast<float*>(take(M * D * 4));
-  t.prod = static_cast<float*>(take(M * D * 4));
   t.delta = static_cast<float*>(take(static_cast<size_t>(B) * H * T * 4));
   const size_t widest = std::max<size_t>({3 * D, F, D});
-  t.colpart = static_cast<float*>(take(colsum_partial_bytes(static_cast<long long>(M), static_cast<int>(widest))));
+  // column-sum partials: the generic sums (bias of qkv) and those of the
+  // LayerNorm and GELU backward kernels
+  const long long Ml = static_cast<long long>(M);
+  t.colpart = static_cast<float*>(take(std::max(colsum_partial_bytes(Ml, static_cast<int>(widest)),
+                                                ln_bwd_scratch_bytes(Ml, static_cast<int>(D)))));
   {
     // fp32 partial slabs of the split-K weight-gradient products
     const int Mi = static_cast<int>(M), Di = static_cast<int>(D), Fi = static_cast<int>(F);
@@ -672,10 +675,14 @@ cudaError_t colsum(const void* in, bool in16, int64_t M, int N, float* partial, 
   return launch_colsum(in, in16, M, N, N, partial, out, s);
 }
 
+// LayerNorm backward with the column sums of dy * xhat (dgamma), dy (dbeta)
+// and, when dbias is given, of dx (the bias gradient of the residual branch
+// whose output is the LayerNorm's input).
 cudaError_t ln_bwd(const float* dy, const float* x, const void* gamma, const float* dres, float* dx, void* dx16,
-                   float* prod, int64_t M, int D, float eps, cudaStream_t s) {
-  ProfScope prof("layernorm_bwd", 12.0 * M * D, static_cast<double>(M) * D * (4.0 * 4 + (dres ? 4.0 : 0.0) + 2.0), s);
-  return launch_ln_bwd_16(dy, x, gamma, dres, dx, dx16, prod, M, D, eps, s);
+                   float* dgamma, float* dbeta, float* dbias, float* scratch, int64_t M, int D, float eps,
+                   cudaStream_t s) {
+  ProfScope prof("layernorm_bwd", 15.0 * M * D, static_cast<double>(M) * D * (4.0 * 3 + (dres ? 4.0 : 0.0) + 2.0), s);
+  return launch_ln_bwd_sums_16(dy, x, gamma, dres, dx, dx16, dgamma, dbeta, dbias, M, D, eps, scratch, s);
 }
 
 // Forward with saved intermediates, then the mean shifted cross-entropy and
@@ -740,9 +747,9 @@ int forward_backward(const gpt2_dims* d, const gpt2_model_weights* w, const int3
   }
   GPT2_CUDA(grad_gemm(t.dz, t.ldz, true, t.xf, D, true, gr->wte, D, GPT2_F32, V, D, static_cast<int>(M), s, t.splitk, t.splitk_bytes));
   GPT2_CUDA(grad_gemm(t.dz, t.ldz, false, w->wte, D, true, t.dyf, D, GPT2_F32, M, D, V, s));
-  GPT2_CUDA(ln_bwd(t.dyf, t.xL, w->lnf_g, nullptr, t.dx, t.dxb, t.prod, M, D, eps, s));
-  GPT2_CUDA(colsum(t.prod, false, M, D, t.colpart, gr->lnf_g, s));
-  GPT2_CUDA(colsum(t.dyf, false, M, D, t.colpart, gr->lnf_b, s));
+  // (the sums of dx: the bias gradient of the last block's MLP c_proj)
+  GPT2_CUDA(ln_bwd(t.dyf, t.xL, w->lnf_g, nullptr, t.dx, t.dxb, gr->lnf_g, gr->lnf_b, gr->blocks[L - 1].b_proj,
+                   t.colpart, M, D, eps, s));
   // ---- blocks, last first
   const int Mi = static_cast<int>(M);
   for (int l = L - 1; l >= 0; --l) {
@@ -752,23 +759,19 @@ int forward_backward(const gpt2_dims* d, const gpt2_model_weights* w, const int3
     // x' = h + g W_proj + b_proj
     GPT2_CUDA(grad_gemm(t.dxb, D, false, bw->w_proj, D, false, t.dgb, F, dt, M, F, D, s));
     GPT2_CUDA(grad_gemm(y.g, F, true, t.dxb, D, true, bg->w_proj, D, GPT2_F32, F, D, Mi, s, t.splitk, t.splitk_bytes));
-    GPT2_CUDA(colsum(t.dx, false, M, D, t.colpart, bg->b_proj, s));
     {
-      ProfScope prof("gelu_bwd", 20.0 * M * F, 6.0 * M * F, s);
-      GPT2_CUDA(launch_gelu_bwd_16(t.dgb, y.u, t.dub, M * F, exact, s));
+      ProfScope prof("gelu_bwd", 21.0 * M * F, 6.0 * M * F, s);
+      GPT2_CUDA(launch_gelu_bwd_sums_16(t.dgb, y.u, t.dub, M, F, exact, bg->b_fc, t.colpart, s));
     }
     // u = a2 W_fc + b_fc
     GPT2_CUDA(grad_gemm(t.dub, F, false, bw->w_fc, F, false, t.dyf, D, GPT2_F32, M, D, F, s));
     GPT2_CUDA(grad_gemm(y.a2, D, true, t.dub, F, true, bg->w_fc, F, GPT2_F32, D, F, Mi, s, t.splitk, t.splitk_bytes));
-    GPT2_CUDA(colsum(t.dub, true, M, F, t.colpart, bg->b_fc, s));
     // a2 = LN_2(h), and the residual path: dh = dx' + LN_2'(h)^T da2
-    GPT2_CUDA(ln_bwd(t.dyf, y.h, bw->ln2_g, t.dx, t.dh, t.dhb, t.prod, M, D, eps, s));
-    GPT2_CUDA(colsum(t.prod, false, M, D, t.colpart, bg->ln2_g, s));
-    GPT2_CUDA(colsum(t.dyf, false, M, D, t.colpart, bg->ln2_b, s));
+    GPT2_CUDA(ln_bwd(t.dyf, y.h, bw->ln2_g, t.dx, t.dh, t.dhb, bg->ln2_g, bg->ln2_b, bg->b_o, t.colpart, M, D, eps,
+                     s));
     // h = x + o W_o + b_o
     GPT2_CUDA(grad_gemm(t.dhb, D, false, bw->w_o, D, false, t.dob, D, dt, M, D, D, s));
     GPT2_CUDA(grad_gemm(y.o, D, true, t.dhb, D, true, bg->w_o, D, GPT2_F32, D, D, Mi, s, t.splitk, t.splitk_bytes));
-    GPT2_CUDA(colsum(t.dh, false, M, D, t.colpart, bg->b_o, s));
     // o = attention(qkv)
     {
       const double pairs = static_cast<double>(B) * H * T * (T + 1.0) / 2.0;
@@ -781,9 +784,9 @@ int forward_backward(const gpt2_dims* d, const gpt2_model_weights* w, const int3
     GPT2_CUDA(grad_gemm(y.a, D, true, t.dqkvb, 3 * D, true, bg->w_qkv, 3 * D, GPT2_F32, D, 3 * D, Mi, s, t.splitk, t.splitk_bytes));
     GPT2_CUDA(colsum(t.dqkvb, true, M, 3 * D, t.colpart, bg->b_qkv, s));
     // a = LN_1(x), and the residual path: dx = dh + LN_1'(x)^T da
-    GPT2_CUDA(ln_bwd(t.dyf, y.x, bw->ln1_g, t.dh, t.dx, t.dxb, t.prod, M, D, eps, s));
-    GPT2_CUDA(colsum(t.prod, false, M, D, t.colpart, bg->ln1_g, s));
-    GPT2_CUDA(colsum(t.dyf, false, M, D, t.colpart, bg->ln1_b, s));
+    // (the sums of dx: the bias gradient of the previous block's MLP c_proj)
+    GPT2_CUDA(ln_bwd(t.dyf, y.x, bw->ln1_g, t.dh, t.dx, t.dxb, bg->ln1_g, bg->ln1_b,
+                     l > 0 ? gr->blocks[l - 1].b_proj : nullptr, t.colpart, M, D, eps, s));
   }
   // ---- the embedding: wte rows of the tokens used, wpe rows of the positions
   {

@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -304,6 +305,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (!ok && lane == 0) record_error(err, kErrTimeout, kSiteAttnBwd);
   }
 
+  // every warp arrives converged (the producer and MMA roles ran on one lane):
+  // a CTA barrier reached by a diverged warp need not hold the others, and
+  // the tensor memory is freed only after the epilogue's last read
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -367,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -550,6 +556,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (!ok && lane == 0) record_error(err, kErrTimeout, kSiteAttnBwd);
   }
 
+  // every warp arrives converged (the producer and MMA roles ran on one lane):
+  // a CTA barrier reached by a diverged warp need not hold the others, and
+  // the tensor memory is freed only after the epilogue's last read
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

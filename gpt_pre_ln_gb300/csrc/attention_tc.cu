@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -461,6 +462,10 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     if (!ok && lane == 0) record_error(err, kErrTimeout, kSiteAttnSoftmax);
   }
 
+  // every warp arrives converged (the producer and MMA roles ran on one lane):
+  // a CTA barrier reached by a diverged warp need not hold the others, and
+  // the tensor memory is freed only after the epilogue's last read
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -46,39 +46,22 @@ __global__ void gelu_fwd_16(const T16* __restrict__ u, T16* __restrict__ g, long
   reinterpret_cast<uint4*>(g)[i] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// du = dg * act'(u): d/du of 0.5 u (1 + tanh(k (u + 0.044715 u^3))), or of
-// u Phi(u) = Phi(u) + u phi(u).
+// act'(u): d/du of 0.5 u (1 + tanh(k (u + 0.044715 u^3))), or of u Phi(u)
+// = Phi(u) + u phi(u).
 __device__ __forceinline__ float gelu_grad(float x, int exact) {
   if (exact) {
     const float Phi = 0.5f * (1.f + erff(x * 0.7071067811865476f));
     return Phi + x * 0.3989422804014327f * expf(-0.5f * x * x);
   }
-  const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
-  const float t = tanhf(k0 * fmaf(0.044715f * x, x * x, x));
+  // tanh(v) = 1 - 2 / (1 + e^(2v)) on the hardware exp2 and reciprocal
+  // (absolute error about 1e-7; saturates for large |v|)
+  const float k0 = 0.7978845608028654f;         // sqrt(2/pi)
+  const float two_log2e = 2.8853900817779268f;  // 2 / ln(2)
+  const float t = fmaf(-2.f, rcp_approx(1.f + ex2_approx(two_log2e * k0 * fmaf(0.044715f * x, x * x, x))), 1.f);
   return 0.5f * (1.f + t) + 0.5f * x * (1.f - t * t) * k0 * fmaf(3.f * 0.044715f, x * x, 1.f);
 }
-template <typename T16>
-__global__ void gelu_bwd_16(const T16* __restrict__ dg, const T16* __restrict__ u, T16* __restrict__ du, long long n8,
-                            int exact) {
-  griddep_wait();
-  griddep_launch_dependents();
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n8) return;
-  const uint4 xu = reinterpret_cast<const uint4*>(u)[i];
-  const uint4 xg = reinterpret_cast<const uint4*>(dg)[i];
-  const uint32_t wu[4] = {xu.x, xu.y, xu.z, xu.w}, wg[4] = {xg.x, xg.y, xg.z, xg.w};
-  uint32_t o[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float2 x = Type16<T16>::unpack2(wu[e]);
-    const float2 d = Type16<T16>::unpack2(wg[e]);
-    o[e] = Type16<T16>::pack2(d.x * gelu_grad(x.x, exact), d.y * gelu_grad(x.y, exact));
-  }
-  reinterpret_cast<uint4*>(du)[i] = make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-// LayerNorm backward, one warp per row (the row is re-read from L1 between
-// passes): with xhat = (x - mean) rstd and g = dy * gamma,
+// LayerNorm backward for rows too wide for registers, one warp per row (the
+// row is re-read from L1 between passes): with xhat = (x - mean) rstd and g = dy * gamma,
 //   dx = rstd (g - mean(g) - xhat mean(g xhat)) (+ dres),
 //   prod = dy * xhat (its column sums are dgamma; those of dy are dbeta).
 // dx fp32; dx16 (nullable) the same rounded to 16 bits for the next GEMM.
@@ -123,18 +106,126 @@ __global__ void __launch_bounds__(256) ln_bwd_16(const float* __restrict__ dy, c
   }
 }
 
-// The same with the row held in registers (NV groups of four columns per
-// lane, 16-byte loads; groups past D/4 idle): x and dy are read once.
-template <typename T16, int NV>
-__global__ void __launch_bounds__(256) ln_bwd_16_reg(const float* __restrict__ dy, const float* __restrict__ x,
-                                                     const T16* __restrict__ gamma, const float* __restrict__ dres,
-                                                     float* __restrict__ dx, T16* __restrict__ dx16,
-                                                     float* __restrict__ prod, long long rows, int D, float eps) {
+// Column sums, level 1: a block of 8 warps sums a chunk of kChunk rows over
+// 32 x VEC columns (VEC columns of 16 bytes per lane: warp loads are whole
+// 512-byte row segments); warp w takes rows w, w + 8, ... of the chunk (all
+// its loads in flight together, added in a fixed tree), then the 8 warp sums
+// are added in warp order.  partial[chunk][col].
+constexpr int kChunk = 64;
+template <typename T, int VEC>
+__global__ void __launch_bounds__(256) colsum_partial(const T* __restrict__ in, long long M, int N, long long ld,
+                                                      float* __restrict__ partial) {
   griddep_wait();
   griddep_launch_dependents();
-  const long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
+  __shared__ float red[8][32 * VEC];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c0 = (blockIdx.x * 32 + lane) * VEC;
+  const long long r0 = static_cast<long long>(blockIdx.y) * kChunk + warp;
+  constexpr int R = kChunk / 8;
+  float v[R][VEC];
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const long long r = r0 + 8 * i;
+    const T* src = in + r * ld + c0;
+    if (r < M && c0 + VEC <= N) {
+      if constexpr (VEC == 1) {
+        v[i][0] = ld_f(src);
+      } else if constexpr (sizeof(T) == 4) {
+        const float4 q = *reinterpret_cast<const float4*>(src);
+        v[i][0] = q.x;
+        v[i][1] = q.y;
+        v[i][2] = q.z;
+        v[i][3] = q.w;
+      } else {
+        const uint4 q = *reinterpret_cast<const uint4*>(src);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = Type16<T>::unpack2(w[e]);
+          v[i][2 * e] = f.x;
+          v[i][2 * e + 1] = f.y;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) v[i][e] = (r < M && c0 + e < N) ? ld_f(src + e) : 0.f;
+    }
+  }
+#pragma unroll
+  for (int w = R / 2; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i)
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) v[i][e] += v[i + w][e];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) red[warp][lane * VEC + e] = v[0][e];
+  __syncthreads();
+  for (int t = threadIdx.x; t < 32 * VEC; t += 256) {
+    const int col = blockIdx.x * 32 * VEC + t;
+    float s = red[0][t];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) s += red[w][t];
+    if (col < N) partial[static_cast<long long>(blockIdx.y) * N + col] = s;
+  }
+}
+
+// Level 2: column c of partial [rows, N] summed over the rows in a fixed
+// order (warp w of 32 takes rows w, w + 32, ..., four running sums by row
+// index mod 4, then the 32 warp sums in warp order).  The result goes to
+// out_q[c - q seg] for q = c / seg (three outputs at most; a null output is
+// skipped).
+__global__ void __launch_bounds__(1024) colsum_final(const float* __restrict__ partial, int rows, int N, int seg,
+                                                     float* __restrict__ out0, float* __restrict__ out1,
+                                                     float* __restrict__ out2) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ float red[32][33];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col = blockIdx.x * 32 + lane;
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
+  if (col < N) {
+    const float* p = partial + col;
+    int r = warp;
+    for (; r + 96 < rows; r += 128) {
+      a[0] += p[static_cast<long long>(r) * N];
+      a[1] += p[static_cast<long long>(r + 32) * N];
+      a[2] += p[static_cast<long long>(r + 64) * N];
+      a[3] += p[static_cast<long long>(r + 96) * N];
+    }
+    for (; r < rows; r += 32) a[0] += p[static_cast<long long>(r) * N];
+  }
+  red[warp][lane] = (a[0] + a[1]) + (a[2] + a[3]);
+  __syncthreads();
+  if (warp == 0 && col < N) {
+    float s = red[0][lane];
+    for (int w = 1; w < 32; ++w) s += red[w][lane];
+    const int q = col / seg;
+    float* o = q == 0 ? out0 : (q == 1 ? out1 : out2);
+    if (o) o[col - q * seg] = s;
+  }
+}
+
+// LayerNorm backward with its column sums: one warp per row with the row in
+// registers (NV groups of four columns per lane, 16-byte loads; x and dy are
+// read once), 16 rows per block, and no per-row product written out.  The
+// block adds up, over its rows and in warp order, dy * xhat (the gamma
+// gradient), dy (beta) and dx (the bias gradient of the residual branch that
+// produced the LayerNorm's input), through a shared [16][D] buffer one
+// quantity at a time: partial[block][q][D].
+constexpr int kLnColsWarps = 16;
+template <typename T16, int NV>
+__global__ void __launch_bounds__(kLnColsWarps * 32) ln_bwd_cols(const float* __restrict__ dy,
+                                                                const float* __restrict__ x,
+                                                                const T16* __restrict__ gamma,
+                                                                const float* __restrict__ dres, float* __restrict__ dx,
+                                                                T16* __restrict__ dx16, float* __restrict__ partial,
+                                                                long long rows, int D, float eps) {
+  griddep_wait();
+  griddep_launch_dependents();
+  extern __shared__ float red[];  // [kLnColsWarps][D]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long r = static_cast<long long>(blockIdx.x) * kLnColsWarps + warp;
+  const bool valid = r < rows;
   const int nvec = D >> 2;
   float4 xv[NV], gv[NV];
   float gm[NV][4];
@@ -142,7 +233,7 @@ __global__ void __launch_bounds__(256) ln_bwd_16_reg(const float* __restrict__ d
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int g = lane + 32 * i;
-    if (g < nvec) {
+    if (valid && g < nvec) {
       xv[i] = reinterpret_cast<const float4*>(x + r * D)[g];
       gv[i] = reinterpret_cast<const float4*>(dy + r * D)[g];
       const uint2 gw = reinterpret_cast<const uint2*>(gamma)[g];
@@ -180,71 +271,98 @@ __global__ void __launch_bounds__(256) ln_bwd_16_reg(const float* __restrict__ d
   }
   const float mg = warp_sum(sg) / static_cast<float>(D);
   const float mgx = warp_sum(sgx) / static_cast<float>(D);
+  // xv becomes dy * xhat, gm becomes dx (zero in rows past the end)
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int g = lane + 32 * i;
-    if (g >= nvec) continue;
-    const float xs[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w}, ds[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
-    float o[4], pr[4];
-    const float4 rr = dres ? reinterpret_cast<const float4*>(dres + r * D)[g] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float xs[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+    const float ds[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
+    const float4 rr = (valid && dres && g < nvec) ? reinterpret_cast<const float4*>(dres + r * D)[g]
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
     const float rs[4] = {rr.x, rr.y, rr.z, rr.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float xh = (xs[e] - mean) * rstd;
-      o[e] = rstd * (ds[e] * gm[i][e] - mg - xh * mgx) + rs[e];
-      pr[e] = ds[e] * xh;
+      gm[i][e] = valid ? rstd * (ds[e] * gm[i][e] - mg - xh * mgx) + rs[e] : 0.f;
+      xs[e] = ds[e] * xh;
     }
-    reinterpret_cast<float4*>(dx + r * D)[g] = make_float4(o[0], o[1], o[2], o[3]);
-    reinterpret_cast<float4*>(prod + r * D)[g] = make_float4(pr[0], pr[1], pr[2], pr[3]);
-    if (dx16)
-      reinterpret_cast<uint2*>(dx16 + r * D)[g] =
-          make_uint2(Type16<T16>::pack2(o[0], o[1]), Type16<T16>::pack2(o[2], o[3]));
+    xv[i] = make_float4(xs[0], xs[1], xs[2], xs[3]);
+    if (valid && g < nvec) {
+      reinterpret_cast<float4*>(dx + r * D)[g] = make_float4(gm[i][0], gm[i][1], gm[i][2], gm[i][3]);
+      if (dx16)
+        reinterpret_cast<uint2*>(dx16 + r * D)[g] =
+            make_uint2(Type16<T16>::pack2(gm[i][0], gm[i][1]), Type16<T16>::pack2(gm[i][2], gm[i][3]));
+    }
+  }
+  float* out = partial + static_cast<long long>(blockIdx.x) * 3 * D;
+#pragma unroll
+  for (int qn = 0; qn < 3; ++qn) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int g = lane + 32 * i;
+      if (g < nvec) {
+        const float4 v = qn == 0 ? xv[i] : (qn == 1 ? gv[i] : make_float4(gm[i][0], gm[i][1], gm[i][2], gm[i][3]));
+        reinterpret_cast<float4*>(red + warp * D)[g] = v;
+      }
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < D; c += kLnColsWarps * 32) {
+      float t = red[c];
+#pragma unroll
+      for (int w = 1; w < kLnColsWarps; ++w) t += red[w * D + c];
+      out[qn * D + c] = t;
+    }
+    __syncthreads();
   }
 }
 
-// Column sums, level 1: block (column tile of 64, row chunk of kChunk rows):
-// 4 groups of 64 threads take rows group, group + 4, ... of the chunk (16
-// rows each, loaded together and added in a fixed tree), then the 4 group
-// sums are added in order.  partial[chunk][col].
-constexpr int kChunk = 64;
-template <typename T>
-__global__ void __launch_bounds__(256) colsum_partial(const T* __restrict__ in, long long M, int N, long long ld,
-                                                      float* __restrict__ partial) {
+// du = dg * act'(u) with the column sums of du (the c_fc bias gradient):
+// block = 8 warps over a chunk of kChunk rows and 256 columns (8 per lane,
+// 16-byte loads); warp w takes rows w, w + 8, ...; the 8 warp sums are added
+// in warp order.  partial[chunk][col].  F a multiple of 8.
+template <typename T16>
+__global__ void __launch_bounds__(256) gelu_bwd_cols(const T16* __restrict__ dg, const T16* __restrict__ u,
+                                                     T16* __restrict__ du, long long M, int F, int exact,
+                                                     float* __restrict__ partial) {
   griddep_wait();
   griddep_launch_dependents();
-  __shared__ float part[4][64];
-  const int col = blockIdx.x * 64 + (threadIdx.x & 63);
-  const int grp = threadIdx.x >> 6;
-  const long long r0 = static_cast<long long>(blockIdx.y) * kChunk + grp;
-  float v[kChunk / 4];
+  __shared__ float red[8][256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c0 = blockIdx.x * 256 + lane * 8;
+  const long long r0 = static_cast<long long>(blockIdx.y) * kChunk + warp;
+  float acc[8];
 #pragma unroll
-  for (int i = 0; i < kChunk / 4; ++i) {
-    const long long r = r0 + 4 * i;
-    v[i] = (col < N && r < M) ? ld_f(in + r * ld + col) : 0.f;
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  if (c0 < F) {
+#pragma unroll 4
+    for (int i = 0; i < kChunk / 8; ++i) {
+      const long long r = r0 + 8 * i;
+      if (r >= M) break;
+      const long long off = (r * F + c0) / 8;
+      const uint4 xu = reinterpret_cast<const uint4*>(u)[off];
+      const uint4 xg = reinterpret_cast<const uint4*>(dg)[off];
+      const uint32_t wu[4] = {xu.x, xu.y, xu.z, xu.w}, wg[4] = {xg.x, xg.y, xg.z, xg.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 xx = Type16<T16>::unpack2(wu[e]);
+        const float2 d = Type16<T16>::unpack2(wg[e]);
+        const float a = d.x * gelu_grad(xx.x, exact), b = d.y * gelu_grad(xx.y, exact);
+        acc[2 * e] += a;
+        acc[2 * e + 1] += b;
+        o[e] = Type16<T16>::pack2(a, b);
+      }
+      reinterpret_cast<uint4*>(du)[off] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
   }
 #pragma unroll
-  for (int w = kChunk / 8; w >= 1; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) v[i] += v[i + w];
-  part[grp][threadIdx.x & 63] = v[0];
+  for (int e = 0; e < 8; ++e) red[warp][lane * 8 + e] = acc[e];
   __syncthreads();
-  if (grp == 0 && col < N)
-    partial[static_cast<long long>(blockIdx.y) * N + col] = ((part[0][threadIdx.x] + part[1][threadIdx.x]) +
-                                                             part[2][threadIdx.x]) + part[3][threadIdx.x];
-}
-// level 2: out[col] = sum of the chunks' partials in chunk order.
-__global__ void colsum_final(const float* __restrict__ partial, int chunks, int N, float* __restrict__ out) {
-  griddep_wait();
-  griddep_launch_dependents();
-  const int col = blockIdx.x * blockDim.x + threadIdx.x;
-  if (col >= N) return;
-  float a[4] = {0.f, 0.f, 0.f, 0.f};
-  int c = 0;
-  for (; c + 4 <= chunks; c += 4)
+  const int col = blockIdx.x * 256 + threadIdx.x;
+  float s = red[0][threadIdx.x];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) a[u] += partial[static_cast<long long>(c + u) * N + col];
-  for (; c < chunks; ++c) a[0] += partial[static_cast<long long>(c) * N + col];
-  out[col] = (a[0] + a[1]) + (a[2] + a[3]);
+  for (int w = 1; w < 8; ++w) s += red[w][threadIdx.x];
+  if (col < F) partial[static_cast<long long>(blockIdx.y) * F + col] = s;
 }
 
 // dwte[token] += the gradient of every position that used the token: the
@@ -305,19 +423,35 @@ unsigned blocks_for(long long n, int per) { return static_cast<unsigned>((n + pe
 
 size_t colsum_partial_bytes(long long M, int N) { return static_cast<size_t>((M + kChunk - 1) / kChunk) * N * 4; }
 
+namespace {
+
+cudaError_t colsum_finish(const float* partial, int rows, int N, int seg, float* o0, float* o1, float* o2,
+                          cudaStream_t s) {
+  return launch_pdl(colsum_final, dim3(blocks_for(N, 32)), 1024, 0, s, 0, partial, rows, N, seg, o0, o1, o2);
+}
+
+template <typename T>
+cudaError_t colsum_level1(const T* in, long long M, int N, long long ld, float* partial, cudaStream_t s) {
+  constexpr int VEC = 16 / sizeof(T);
+  const unsigned chunks = static_cast<unsigned>((M + kChunk - 1) / kChunk);
+  const bool vec_ok = (reinterpret_cast<uintptr_t>(in) & 15u) == 0 && ld % VEC == 0;
+  if (vec_ok)
+    return launch_pdl(colsum_partial<T, VEC>, dim3(blocks_for(N, 32 * VEC), chunks), 256, 0, s, 0, in, M, N, ld,
+                      partial);
+  return launch_pdl(colsum_partial<T, 1>, dim3(blocks_for(N, 32), chunks), 256, 0, s, 0, in, M, N, ld, partial);
+}
+
+}  // namespace
+
 cudaError_t launch_colsum(const void* in, bool in16, long long M, int N, long long ld, float* partial, float* out,
                           cudaStream_t s) {
   if (N == 0) return cudaSuccess;
   const int chunks = static_cast<int>((M + kChunk - 1) / kChunk);
   if (chunks == 0) return cudaMemsetAsync(out, 0, static_cast<size_t>(N) * 4, s);
-  const dim3 grid((N + 63) / 64, chunks);
-  cudaError_t e = in16 ? launch_pdl(colsum_partial<__nv_bfloat16>, grid, 256, 0, s, 0,
-                                    static_cast<const __nv_bfloat16*>(in), M, N, ld, partial)
-                       : launch_pdl(colsum_partial<float>, grid, 256, 0, s, 0, static_cast<const float*>(in), M, N,
-                                    ld, partial);
+  cudaError_t e = in16 ? colsum_level1(static_cast<const __nv_bfloat16*>(in), M, N, ld, partial, s)
+                       : colsum_level1(static_cast<const float*>(in), M, N, ld, partial, s);
   if (e != cudaSuccess) return e;
-  return launch_pdl(colsum_final, dim3(blocks_for(N, 256)), 256, 0, s, 0, static_cast<const float*>(partial),
-                    chunks, N, out);
+  return colsum_finish(partial, chunks, N, N, out, nullptr, nullptr, s);
 }
 
 cudaError_t launch_gelu_fwd_16(const void* u, void* g, long long n, bool exact, cudaStream_t s) {
@@ -326,34 +460,80 @@ cudaError_t launch_gelu_fwd_16(const void* u, void* g, long long n, bool exact, 
                     static_cast<const __nv_bfloat16*>(u), static_cast<__nv_bfloat16*>(g), n / 8, exact ? 1 : 0);
 }
 
-cudaError_t launch_gelu_bwd_16(const void* dg, const void* u, void* du, long long n, bool exact, cudaStream_t s) {
-  if (n == 0) return cudaSuccess;
-  return launch_pdl(gelu_bwd_16<__nv_bfloat16>, dim3(blocks_for(n / 8, 256)), 256, 0, s, 0,
-                    static_cast<const __nv_bfloat16*>(dg), static_cast<const __nv_bfloat16*>(u),
-                    static_cast<__nv_bfloat16*>(du), n / 8, exact ? 1 : 0);
+cudaError_t launch_gelu_bwd_sums_16(const void* dg, const void* u, void* du, long long M, int F, bool exact,
+                                    float* dbias, float* scratch, cudaStream_t s) {
+  if (F == 0) return cudaSuccess;
+  const int chunks = static_cast<int>((M + kChunk - 1) / kChunk);
+  if (chunks == 0) return cudaMemsetAsync(dbias, 0, static_cast<size_t>(F) * 4, s);
+  cudaError_t e = launch_pdl(gelu_bwd_cols<__nv_bfloat16>, dim3(blocks_for(F, 256), chunks), 256, 0, s, 0,
+                             static_cast<const __nv_bfloat16*>(dg), static_cast<const __nv_bfloat16*>(u),
+                             static_cast<__nv_bfloat16*>(du), M, F, exact ? 1 : 0, scratch);
+  if (e != cudaSuccess) return e;
+  return colsum_finish(scratch, chunks, F, F, dbias, nullptr, nullptr, s);
 }
+
+namespace {
+
+// the row in registers up to 13 float4 groups per lane (D <= 1664)
+constexpr int kLnRegMaxD = 13 * 128;
 
 template <int NV>
-cudaError_t ln_bwd_reg(const float* dy, const float* x, const void* gamma, const float* dres, float* dx, void* dx16,
-                       float* prod, long long rows, int D, float eps, cudaStream_t s) {
-  return launch_pdl(ln_bwd_16_reg<__nv_bfloat16, NV>, dim3(blocks_for(rows, 8)), 256, 0, s, 0, dy, x,
-                    static_cast<const __nv_bfloat16*>(gamma), dres, dx, static_cast<__nv_bfloat16*>(dx16), prod, rows,
-                    D, eps);
+cudaError_t ln_bwd_cols_launch(const float* dy, const float* x, const void* gamma, const float* dres, float* dx,
+                               void* dx16, float* partial, long long rows, int D, float eps, cudaStream_t s) {
+  auto kern = ln_bwd_cols<__nv_bfloat16, NV>;
+  const int smem = kLnColsWarps * D * 4;
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (smem > 48 * 1024 && dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kLnColsWarps * kLnRegMaxD * 4);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  return launch_pdl(kern, dim3(blocks_for(rows, kLnColsWarps)), kLnColsWarps * 32, smem, s, 0, dy, x,
+                    static_cast<const __nv_bfloat16*>(gamma), dres, dx, static_cast<__nv_bfloat16*>(dx16), partial,
+                    rows, D, eps);
 }
 
-cudaError_t launch_ln_bwd_16(const float* dy, const float* x, const void* gamma, const float* dres, float* dx,
-                             void* dx16, float* prod, long long rows, int D, float eps, cudaStream_t s) {
-  if (rows == 0) return cudaSuccess;
-  // the row in registers up to 13 float4 groups per lane (D <= 1664)
+}  // namespace
+
+size_t ln_bwd_scratch_bytes(long long M, int D) {
+  if (D <= kLnRegMaxD) return static_cast<size_t>((M + kLnColsWarps - 1) / kLnColsWarps) * 3 * D * 4;
+  // wide rows: the per-row product dy * xhat, then the generic column sums
+  return static_cast<size_t>(M) * D * 4 + colsum_partial_bytes(M, D);
+}
+
+cudaError_t launch_ln_bwd_sums_16(const float* dy, const float* x, const void* gamma, const float* dres, float* dx,
+                                  void* dx16, float* dgamma, float* dbeta, float* dbias, long long rows, int D,
+                                  float eps, float* scratch, cudaStream_t s) {
+  if (rows == 0) {
+    cudaError_t e = cudaMemsetAsync(dgamma, 0, static_cast<size_t>(D) * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dbeta, 0, static_cast<size_t>(D) * 4, s);
+    if (e == cudaSuccess && dbias) e = cudaMemsetAsync(dbias, 0, static_cast<size_t>(D) * 4, s);
+    return e;
+  }
   const int nv = (D + 127) / 128;
-  if (nv <= 2) return ln_bwd_reg<2>(dy, x, gamma, dres, dx, dx16, prod, rows, D, eps, s);
-  if (nv <= 4) return ln_bwd_reg<4>(dy, x, gamma, dres, dx, dx16, prod, rows, D, eps, s);
-  if (nv <= 6) return ln_bwd_reg<6>(dy, x, gamma, dres, dx, dx16, prod, rows, D, eps, s);
-  if (nv <= 8) return ln_bwd_reg<8>(dy, x, gamma, dres, dx, dx16, prod, rows, D, eps, s);
-  if (nv <= 13) return ln_bwd_reg<13>(dy, x, gamma, dres, dx, dx16, prod, rows, D, eps, s);
-  return launch_pdl(ln_bwd_16<__nv_bfloat16>, dim3(blocks_for(rows, 8)), 256, 0, s, 0, dy, x,
-                    static_cast<const __nv_bfloat16*>(gamma), dres, dx, static_cast<__nv_bfloat16*>(dx16), prod, rows,
-                    D, eps);
+  cudaError_t e = cudaSuccess;
+  if (nv <= 2) e = ln_bwd_cols_launch<2>(dy, x, gamma, dres, dx, dx16, scratch, rows, D, eps, s);
+  else if (nv <= 4) e = ln_bwd_cols_launch<4>(dy, x, gamma, dres, dx, dx16, scratch, rows, D, eps, s);
+  else if (nv <= 6) e = ln_bwd_cols_launch<6>(dy, x, gamma, dres, dx, dx16, scratch, rows, D, eps, s);
+  else if (nv <= 8) e = ln_bwd_cols_launch<8>(dy, x, gamma, dres, dx, dx16, scratch, rows, D, eps, s);
+  else if (nv <= 13) e = ln_bwd_cols_launch<13>(dy, x, gamma, dres, dx, dx16, scratch, rows, D, eps, s);
+  else {
+    float* prod = scratch;
+    float* part = scratch + rows * D;
+    e = launch_pdl(ln_bwd_16<__nv_bfloat16>, dim3(blocks_for(rows, 8)), 256, 0, s, 0, dy, x,
+                   static_cast<const __nv_bfloat16*>(gamma), dres, dx, static_cast<__nv_bfloat16*>(dx16), prod, rows,
+                   D, eps);
+    if (e == cudaSuccess) e = launch_colsum(prod, false, rows, D, D, part, dgamma, s);
+    if (e == cudaSuccess) e = launch_colsum(dy, false, rows, D, D, part, dbeta, s);
+    if (e == cudaSuccess && dbias) e = launch_colsum(dx, false, rows, D, D, part, dbias, s);
+    return e;
+  }
+  if (e != cudaSuccess) return e;
+  const int blocks = static_cast<int>((rows + kLnColsWarps - 1) / kLnColsWarps);
+  return colsum_finish(scratch, blocks, 3 * D, D, dgamma, dbeta, dbias, s);
 }
 
 cudaError_t launch_embed_bwd(const int32_t* tokens, const float* dx0, float* dwte, float* dwpe, int B, int T, int D,

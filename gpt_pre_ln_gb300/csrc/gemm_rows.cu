@@ -239,6 +239,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
     tmem_relinquish();
   }
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -573,6 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
     tmem_relinquish();
   }
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -693,6 +694,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          tempty_bar(0), tempty_bar(1), tile0, tile_step, num_tiles, m_tiles, kBM, 0);
   }
 
+  // every warp arrives converged (the producer and MMA roles ran on one lane):
+  // a CTA barrier reached by a diverged warp need not hold the others, and
+  // the tensor memory is freed only after the epilogue's last read
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -891,6 +896,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                             num_pairs, num_tiles, m_units, 2 * kBM, static_cast<int>(rank) * kBM);
   }
 
+  __syncwarp();
   tc_fence_before();
   // neither CTA leaves while the pair's MMAs may still read its shared memory
   // or write its tensor memory

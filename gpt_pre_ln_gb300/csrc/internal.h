@@ -172,14 +172,21 @@ cudaError_t launch_argmax_candidates(const float2* cand, int n_cand, int B, cons
 size_t colsum_partial_bytes(long long M, int N);
 cudaError_t launch_colsum(const void* in, bool in16, long long M, int N, long long ld, float* partial, float* out,
                           cudaStream_t s);
-// g = act(u) and du = dg * act'(u) over n bf16 values (n a multiple of 8,
-// buffers 16-byte aligned); act gelu_new or, with exact, x Phi(x).
+// g = act(u) over n bf16 values (n a multiple of 8, buffers 16-byte
+// aligned); act gelu_new or, with exact, x Phi(x).
 cudaError_t launch_gelu_fwd_16(const void* u, void* g, long long n, bool exact, cudaStream_t s);
-cudaError_t launch_gelu_bwd_16(const void* dg, const void* u, void* du, long long n, bool exact, cudaStream_t s);
+// du = dg * act'(u) over [M, F] bf16 (F a multiple of 8, buffers 16-byte
+// aligned) and dbias = the column sums of du; scratch:
+// colsum_partial_bytes(M, F).
+cudaError_t launch_gelu_bwd_sums_16(const void* dg, const void* u, void* du, long long M, int F, bool exact,
+                                    float* dbias, float* scratch, cudaStream_t s);
 // LayerNorm backward (gamma bf16): dx = LN'(x)^T dy (+ dres), dx16 (nullable)
-// its bf16 copy, prod = dy * xhat.
-cudaError_t launch_ln_bwd_16(const float* dy, const float* x, const void* gamma, const float* dres, float* dx,
-                             void* dx16, float* prod, long long rows, int D, float eps, cudaStream_t s);
+// its bf16 copy, and the column sums dgamma = sum dy * xhat, dbeta = sum dy,
+// dbias (nullable) = sum dx; scratch: ln_bwd_scratch_bytes(rows, D).
+size_t ln_bwd_scratch_bytes(long long M, int D);
+cudaError_t launch_ln_bwd_sums_16(const float* dy, const float* x, const void* gamma, const float* dres, float* dx,
+                                  void* dx16, float* dgamma, float* dbeta, float* dbias, long long rows, int D,
+                                  float eps, float* scratch, cudaStream_t s);
 // dwte[tokens[m]] += dx0[m] (each row in position order), dwpe[t] = sum_b
 // dx0[b, t] for t < T, 0 for T <= t < n_pos.
 cudaError_t launch_embed_bwd(const int32_t* tokens, const float* dx0, float* dwte, float* dwpe, int B, int T, int D,
