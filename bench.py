@@ -726,6 +726,9 @@ def run_ours(args):
     from gpt_pre_ln_gb300 import build as _b
 
     torch.cuda.set_device(local)
+    # a stream of our own: the library replays repeated identical calls as
+    # CUDA graphs, and the legacy default stream cannot be captured
+    torch.cuda.set_stream(torch.cuda.Stream())
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
@@ -931,6 +934,7 @@ def main():
         from gpt_pre_ln_gb300 import build as _b
         _b.build()
         G.lib()
+        torch.cuda.set_stream(torch.cuda.Stream())  # (see run_ours)
         peaks = _peaks()
         if args.only == "decode":
             r = _decode_measure(G, torch, steps=args.steps)

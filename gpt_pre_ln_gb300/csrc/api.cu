@@ -184,6 +184,125 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? GPT2_OK : GPT2_ERR_CU
   } while (0)
 #define GPT2_CUDA(expr) GPT2_TRY(cuda_status(expr))
 
+// ------------------------------------------------------------ launch graphs
+// The multi-kernel entry points (forward, loss, training step, prefill,
+// decode step) launch 60-260 kernels per call.  A call whose arguments
+// (every pointer, size and the stream) equal those of an earlier call
+// replays a CUDA graph captured from that earlier sequence of launches: the
+// same kernels with the same parameters, launched as one graph (whose
+// per-kernel launch cost on the device is lower; programmatic launch
+// between the kernels is kept as graph edges).  The first call with a key
+// runs eagerly (it also performs the one-time per-device set-up: kernel
+// attributes, occupancy queries); the second is captured and replayed;
+// later ones replay.  Calls on the legacy default stream, calls made while
+// the stream is itself being captured (the caller's own graph), and calls
+// while the launch profiler is on run eagerly.  A capture or instantiation
+// that fails leaves that key eager.  At most kMaxGraphs keys are kept (least
+// recently used evicted).
+struct GraphEntry {
+  std::vector<uint64_t> key;
+  cudaGraphExec_t exec = nullptr;
+  int state = 0;  // 1: seen once (eager), 2: graph ready, -1: eager for good
+  uint64_t last_use = 0;
+};
+struct GraphCache {
+  std::mutex mu;
+  std::vector<GraphEntry> entries;
+  uint64_t tick = 0;
+};
+GraphCache g_graphs;
+constexpr size_t kMaxGraphs = 16;
+
+struct KeyBuilder {
+  std::vector<uint64_t> w;
+  KeyBuilder& add(uint64_t v) {
+    w.push_back(v);
+    return *this;
+  }
+  KeyBuilder& ptr(const void* p) { return add(reinterpret_cast<uint64_t>(p)); }
+  KeyBuilder& dims(const gpt2_dims* d) {
+    uint32_t eps_bits;
+    std::memcpy(&eps_bits, &d->eps, 4);
+    return add(d->n_layer).add(d->d_model).add(d->n_head).add(d->d_ff).add(d->vocab).add(d->n_pos).add(eps_bits)
+        .add(d->dtype).add(d->flags);
+  }
+  KeyBuilder& model(const gpt2_model_weights* m, int n_layer) {
+    ptr(m->wte).ptr(m->wpe).ptr(m->lnf_g).ptr(m->lnf_b);
+    for (int l = 0; l < n_layer; ++l) {
+      const gpt2_block_weights& b = m->blocks[l];
+      ptr(b.ln1_g).ptr(b.ln1_b).ptr(b.w_qkv).ptr(b.b_qkv).ptr(b.w_o).ptr(b.b_o);
+      ptr(b.ln2_g).ptr(b.ln2_b).ptr(b.w_fc).ptr(b.b_fc).ptr(b.w_proj).ptr(b.b_proj);
+    }
+    return *this;
+  }
+};
+
+template <typename Body>
+int run_graphed(KeyBuilder& kb, cudaStream_t s, Body&& body) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (s == nullptr || s == cudaStreamLegacy || s == cudaStreamPerThread || g_prof.on ||
+      cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+    return body(s);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  kb.add(static_cast<uint64_t>(dev)).ptr(s);
+  GraphEntry* e = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_graphs.mu);
+    for (GraphEntry& x : g_graphs.entries)
+      if (x.key == kb.w) e = &x;
+    if (e && e->state == 2) {
+      e->last_use = ++g_graphs.tick;
+      return cuda_status(cudaGraphLaunch(e->exec, s));
+    }
+    if (!e) {
+      if (g_graphs.entries.size() >= kMaxGraphs) {
+        auto lru = std::min_element(g_graphs.entries.begin(), g_graphs.entries.end(),
+                                    [](const GraphEntry& a, const GraphEntry& b) { return a.last_use < b.last_use; });
+        if (lru->exec) cudaGraphExecDestroy(lru->exec);
+        g_graphs.entries.erase(lru);
+      }
+      GraphEntry n;
+      n.key = kb.w;
+      n.state = 1;
+      n.last_use = ++g_graphs.tick;
+      g_graphs.entries.push_back(std::move(n));
+      return body(s);  // first call: eager
+    }
+    if (e->state != 1) return body(s);
+    e->state = -1;  // until the capture below succeeds
+  }
+  // second call with this key: capture its launches, then replay
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  bool ok = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
+  if (ok) {
+    const int rc = body(s);
+    ok = cudaStreamEndCapture(s, &graph) == cudaSuccess && rc == GPT2_OK && graph != nullptr;
+  }
+  if (ok) ok = cudaGraphInstantiate(&exec, graph, 0) == cudaSuccess;
+  if (graph) cudaGraphDestroy(graph);
+  if (!ok) {
+    if (exec) cudaGraphExecDestroy(exec);
+    cudaGetLastError();  // a failed capture leaves no work behind: run the calls eagerly
+    return body(s);
+  }
+  std::lock_guard<std::mutex> lk(g_graphs.mu);
+  GraphEntry* x = nullptr;
+  for (GraphEntry& y : g_graphs.entries)
+    if (y.key == kb.w) x = &y;
+  if (!x) {  // evicted meanwhile: replay once and drop
+    const int rc = cuda_status(cudaGraphLaunch(exec, s));
+    cudaGraphExecDestroy(exec);
+    return rc;
+  }
+  if (x->exec) cudaGraphExecDestroy(x->exec);
+  x->exec = exec;
+  x->state = 2;
+  x->last_use = ++g_graphs.tick;
+  return cuda_status(cudaGraphLaunch(exec, s));
+}
+
 // One linear layer on the path of dims.dtype (no argument checks).
 cudaError_t linear(gpt2_dtype dt, const void* x, const void* w, const void* bias, const float* res, void* y,
                    int64_t M, int N, int K, int64_t ldy, bool w_out_in, int epi, gpt2_dtype y_t, cudaStream_t s) {
@@ -1047,11 +1166,14 @@ int gpt2_forward_logits(const gpt2_dims* dims, const gpt2_model_weights* w, cons
   const int64_t M = static_cast<int64_t>(B) * T;
   const gpt2_dtype dt = dims->dtype;
   Acts A = carve_acts(ws, dims, M);
-  cudaStream_t s = cs(stream);
-  GPT2_TRY(forward_to_lnf(dims, w, tokens, B, T, A, s));
-  GPT2_CUDA(linear(dt, A.a, w->wte, nullptr, nullptr, logits, M, dims->vocab, dims->d_model, ld, true, GPT2_EPI_NONE,
-                   logits_t, s));
-  return GPT2_OK;
+  KeyBuilder kb;
+  kb.add(1).dims(dims).model(w, dims->n_layer).ptr(tokens).ptr(logits).add(ld).add(logits_t).add(B).add(T).ptr(ws);
+  return run_graphed(kb, cs(stream), [&](cudaStream_t s) -> int {
+    GPT2_TRY(forward_to_lnf(dims, w, tokens, B, T, A, s));
+    GPT2_CUDA(linear(dt, A.a, w->wte, nullptr, nullptr, logits, M, dims->vocab, dims->d_model, ld, true,
+                     GPT2_EPI_NONE, logits_t, s));
+    return GPT2_OK;
+  });
 }
 
 
@@ -1077,31 +1199,35 @@ int gpt2_forward_loss(const gpt2_dims* dims, const gpt2_model_weights* w, const 
   const int D = dims->d_model, V = dims->vocab;
   if (!labels) labels = tokens;
   Acts A = carve_acts(ws, dims, M);
-  Carve c(static_cast<char*>(ws) + acts_bytes(dims, M));
-  float* tgt = c.take<float>(M, 4);
-  float* tl_scratch = c.take<float>(M, 4);
-  cudaStream_t s = cs(stream);
-  GPT2_TRY(forward_to_lnf(dims, w, tokens, B, T, A, s));
-  float2* part;
-  int n_part = 1;
-  if (loss_fused(dims, M)) {
-    part = c.take<float2>(M * lse_max_partials(V), sizeof(float2));
-    const double e = static_cast<double>(esize(dt));
-    ProfScope prof(dt == GPT2_BF16 ? "gemm_lse_bf16_tcgen05" : "gemm_lse_f16_tcgen05", 2.0 * M * V * D,
-                   (static_cast<double>(M) + V) * D * e, s);
-    GPT2_CUDA(launch_gemm_lse_16(dt, A.a, w->wte, M, V, D, labels, T, part, tgt, &n_part, s));
-  } else {
-    part = c.take<float2>(M, sizeof(float2));
-    float* logits = c.take<float>(M * loss_ld(dims), 4);
-    GPT2_CUDA(linear(dt, A.a, w->wte, nullptr, nullptr, logits, M, V, D, loss_ld(dims), true, GPT2_EPI_NONE,
-                     GPT2_F32, s));
-    ProfScope prof("lse_from_logits", 3.0 * M * V, 4.0 * M * V, s);
-    GPT2_CUDA(launch_lse_from_logits(logits, loss_ld(dims), M, V, labels, T, part, tgt, s));
-  }
-  ProfScope prof("loss_reduce", 4.0 * M * n_part, 8.0 * M * n_part + 12.0 * M, s);
-  GPT2_CUDA(launch_loss_rows(part, n_part, tgt, labels, B, T, V, lse, token_loss ? token_loss : tl_scratch,
-                             mean_loss, s));
-  return GPT2_OK;
+  KeyBuilder kb;
+  kb.add(2).dims(dims).model(w, dims->n_layer).ptr(tokens).ptr(labels).ptr(token_loss).ptr(lse).ptr(mean_loss).add(B)
+      .add(T).ptr(ws);
+  return run_graphed(kb, cs(stream), [&](cudaStream_t s) -> int {
+    Carve c(static_cast<char*>(ws) + acts_bytes(dims, M));
+    float* tgt = c.take<float>(M, 4);
+    float* tl_scratch = c.take<float>(M, 4);
+    GPT2_TRY(forward_to_lnf(dims, w, tokens, B, T, A, s));
+    float2* part;
+    int n_part = 1;
+    if (loss_fused(dims, M)) {
+      part = c.take<float2>(M * lse_max_partials(V), sizeof(float2));
+      const double e = static_cast<double>(esize(dt));
+      ProfScope prof(dt == GPT2_BF16 ? "gemm_lse_bf16_tcgen05" : "gemm_lse_f16_tcgen05", 2.0 * M * V * D,
+                     (static_cast<double>(M) + V) * D * e, s);
+      GPT2_CUDA(launch_gemm_lse_16(dt, A.a, w->wte, M, V, D, labels, T, part, tgt, &n_part, s));
+    } else {
+      part = c.take<float2>(M, sizeof(float2));
+      float* logits = c.take<float>(M * loss_ld(dims), 4);
+      GPT2_CUDA(linear(dt, A.a, w->wte, nullptr, nullptr, logits, M, V, D, loss_ld(dims), true, GPT2_EPI_NONE,
+                       GPT2_F32, s));
+      ProfScope prof("lse_from_logits", 3.0 * M * V, 4.0 * M * V, s);
+      GPT2_CUDA(launch_lse_from_logits(logits, loss_ld(dims), M, V, labels, T, part, tgt, s));
+    }
+    ProfScope prof("loss_reduce", 4.0 * M * n_part, 8.0 * M * n_part + 12.0 * M, s);
+    GPT2_CUDA(launch_loss_rows(part, n_part, tgt, labels, B, T, V, lse, token_loss ? token_loss : tl_scratch,
+                               mean_loss, s));
+    return GPT2_OK;
+  });
 }
 
 size_t gpt2_train_workspace_bytes(const gpt2_dims* dims, int B, int T) {
@@ -1123,7 +1249,17 @@ int gpt2_forward_backward(const gpt2_dims* dims, const gpt2_model_weights* w, co
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return GPT2_ERR_ARG;
   if (ws_bytes < gpt2_train_workspace_bytes(dims, B, T)) return GPT2_ERR_WORKSPACE;
   TrainBufs t = carve_train(ws, dims, B, T);
-  return forward_backward(dims, w, tokens, labels ? labels : tokens, grads, mean_loss, B, T, t, cs(stream));
+  KeyBuilder kb;
+  kb.add(3).dims(dims).model(w, dims->n_layer).ptr(tokens).ptr(labels).ptr(mean_loss).add(B).add(T).ptr(ws);
+  kb.ptr(grads->wte).ptr(grads->wpe).ptr(grads->lnf_g).ptr(grads->lnf_b);
+  for (int l = 0; l < dims->n_layer; ++l) {
+    const gpt2_block_grads& g = grads->blocks[l];
+    kb.ptr(g.ln1_g).ptr(g.ln1_b).ptr(g.w_qkv).ptr(g.b_qkv).ptr(g.w_o).ptr(g.b_o);
+    kb.ptr(g.ln2_g).ptr(g.ln2_b).ptr(g.w_fc).ptr(g.b_fc).ptr(g.w_proj).ptr(g.b_proj);
+  }
+  return run_graphed(kb, cs(stream), [&](cudaStream_t s) -> int {
+    return forward_backward(dims, w, tokens, labels ? labels : tokens, grads, mean_loss, B, T, t, s);
+  });
 }
 
 size_t gpt2_kv_cache_bytes(const gpt2_dims* dims, int B, int T_max) {
@@ -1150,29 +1286,32 @@ int gpt2_decode_step(const gpt2_dims* dims, const gpt2_model_weights* w, void* k
   if (logits_opt && ld % 4 != 0) return GPT2_ERR_UNSUPPORTED;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return GPT2_ERR_ARG;
   if (ws_bytes < decode_ws_bytes(dims, B)) return GPT2_ERR_WORKSPACE;
-  cudaStream_t s = cs(stream);
   char* base = static_cast<char*>(ws);
-  int* valid = reinterpret_cast<int*>(base);
-  DecodeGroup G;
-  G.d = dims;
-  G.w = w;
-  G.kv_cache = kv_cache;
-  G.B_cache = B;
-  G.T_max = T_max;
-  G.b0 = 0;
-  G.nb = B;
-  G.past_len = past_len;
-  G.tokens = tokens;
-  G.next_tokens = next_tokens;
-  G.logits = logits_opt;
-  G.ld = ld;
-  G.valid = valid;
-  G.carve(base + align256(static_cast<size_t>(B) * 4));
-  G.s = s;
-  GPT2_CUDA(G.embed());
-  for (int l = 0; l < dims->n_layer; ++l) GPT2_CUDA(G.layer(l));
-  GPT2_CUDA(G.head());
-  return GPT2_OK;
+  KeyBuilder kb;
+  kb.add(5).dims(dims).model(w, dims->n_layer).ptr(kv_cache).add(B).add(T_max).ptr(past_len).ptr(tokens)
+      .ptr(next_tokens).ptr(logits_opt).add(ld).ptr(ws);
+  return run_graphed(kb, cs(stream), [&](cudaStream_t s) -> int {
+    DecodeGroup G;
+    G.d = dims;
+    G.w = w;
+    G.kv_cache = kv_cache;
+    G.B_cache = B;
+    G.T_max = T_max;
+    G.b0 = 0;
+    G.nb = B;
+    G.past_len = past_len;
+    G.tokens = tokens;
+    G.next_tokens = next_tokens;
+    G.logits = logits_opt;
+    G.ld = ld;
+    G.valid = reinterpret_cast<int*>(base);
+    G.carve(base + align256(static_cast<size_t>(B) * 4));
+    G.s = s;
+    GPT2_CUDA(G.embed());
+    for (int l = 0; l < dims->n_layer; ++l) GPT2_CUDA(G.layer(l));
+    GPT2_CUDA(G.head());
+    return GPT2_OK;
+  });
 }
 
 size_t gpt2_prefill_workspace_bytes(const gpt2_dims* dims, int B, int T) {
