@@ -65,25 +65,51 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
 __device__ __forceinline__ uint64_t kmaj(uint32_t base, int kk) { return sdesc_sw128(base + kk * 32, 16, 1024); }
 __device__ __forceinline__ uint64_t mnmaj(uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, 8192, 1024); }
 
-// delta[b, h, t] = sum_d dout[b, t, h*64 + d] * out[b, t, h*64 + d]: one
-// warp per (b, t, h), two values per lane.
+// delta[b, h, t] = sum_d dout[b, t, h*64 + d] * out[b, t, h*64 + d]: eight
+// lanes per (b, t, h) row of 64 values (16-byte loads, the 8 products added
+// in a fixed tree, then the lanes by xor shuffles), kDeltaRows rows per
+// group of lanes with all their loads in flight together.
+constexpr int kDeltaRows = 4;
 template <typename T16>
-__global__ void attn_bwd_delta(const T16* __restrict__ out, const T16* __restrict__ dout, float* __restrict__ delta,
-                               int B, int T, int H) {
+__global__ void __launch_bounds__(256) attn_bwd_delta(const T16* __restrict__ out, const T16* __restrict__ dout,
+                                                      float* __restrict__ delta, int B, int T, int H) {
   griddep_wait();
   griddep_launch_dependents();
-  const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (w >= static_cast<long long>(B) * T * H) return;
-  const int h = static_cast<int>(w % H);
-  const long long bt = w / H;
-  const long long off = bt * H * kHd + h * kHd + lane * 2;
-  const float2 o = Type16<T16>::unpack2(*reinterpret_cast<const uint32_t*>(out + off));
-  const float2 g = Type16<T16>::unpack2(*reinterpret_cast<const uint32_t*>(dout + off));
-  const float s = warp_sum(fmaf(o.x, g.x, o.y * g.y));
-  if (lane == 0) {
-    const long long b = bt / T, t = bt % T;
-    delta[(b * H + h) * T + t] = s;
+  const long long n = static_cast<long long>(B) * T * H;
+  const long long grp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3;
+  const long long n_grp = (static_cast<long long>(gridDim.x) * blockDim.x) >> 3;
+  const int g = threadIdx.x & 7;
+  uint4 o[kDeltaRows], d[kDeltaRows];
+#pragma unroll
+  for (int i = 0; i < kDeltaRows; ++i) {
+    const long long w = grp + i * n_grp;  // (b t) H + h
+    if (w < n) {
+      o[i] = *reinterpret_cast<const uint4*>(out + w * kHd + g * 8);
+      d[i] = *reinterpret_cast<const uint4*>(dout + w * kHd + g * 8);
+    } else {
+      o[i] = d[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kDeltaRows; ++i) {
+    const uint32_t ow[4] = {o[i].x, o[i].y, o[i].z, o[i].w}, dw[4] = {d[i].x, d[i].y, d[i].z, d[i].w};
+    float p[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 a = Type16<T16>::unpack2(ow[e]), b = Type16<T16>::unpack2(dw[e]);
+      p[e] = fmaf(a.x, b.x, a.y * b.y);
+    }
+    float sum = (p[0] + p[1]) + (p[2] + p[3]);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    const long long w = grp + i * n_grp;
+    if (g == 0 && w < n) {
+      const int h = static_cast<int>(w % H);
+      const long long bt = w / H;
+      const long long b = bt / T, t = bt % T;
+      delta[(b * H + h) * T + t] = sum;
+    }
   }
 }
 
@@ -594,8 +620,9 @@ cudaError_t launch_bwd(const void* qkv, const void* out, const float* lse, const
   cudaError_t e = smem_once(attn_bwd_dq<T16>, conf_q);
   if (e == cudaSuccess) e = smem_once(attn_bwd_dkv<T16>, conf_kv);
   if (e != cudaSuccess) return e;
-  const long long warps = static_cast<long long>(rows) * H;
-  e = launch_pdl(attn_bwd_delta<T16>, dim3(static_cast<unsigned>((warps + 7) / 8)), 256, 0, s, 0,
+  const long long items = static_cast<long long>(rows) * H;  // rows of 64 values, 8 lanes and kDeltaRows rows each
+  const long long groups = (items + kDeltaRows - 1) / kDeltaRows;
+  e = launch_pdl(attn_bwd_delta<T16>, dim3(static_cast<unsigned>((groups * 8 + 255) / 256)), 256, 0, s, 0,
                  static_cast<const T16*>(out), static_cast<const T16*>(dout), delta, B, T, H);
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f * score_scale;
