@@ -170,10 +170,11 @@ __global__ void __launch_bounds__(256) colsum_partial(const T* __restrict__ in, 
 }
 
 // Level 2: column c of partial [rows, N] summed over the rows in a fixed
-// order (warp w of 32 takes rows w, w + 32, ..., four running sums by row
-// index mod 4, then the 32 warp sums in warp order).  The result goes to
-// out_q[c - q seg] for q = c / seg (three outputs at most; a null output is
-// skipped).
+// order: warp w of 32 takes rows w, w + 32, ... in batches of 16 (then 4,
+// then single rows) whose loads are all in flight together and whose values
+// are added in a fixed tree; then the 32 warp sums in warp order.  The
+// result goes to out_q[c - q seg] for q = c / seg (three outputs at most; a
+// null output is skipped).
 __global__ void __launch_bounds__(1024) colsum_final(const float* __restrict__ partial, int rows, int N, int seg,
                                                      float* __restrict__ out0, float* __restrict__ out1,
                                                      float* __restrict__ out2) {
@@ -182,19 +183,29 @@ __global__ void __launch_bounds__(1024) colsum_final(const float* __restrict__ p
   __shared__ float red[32][33];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int col = blockIdx.x * 32 + lane;
-  float a[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc = 0.f;
   if (col < N) {
     const float* p = partial + col;
     int r = warp;
-    for (; r + 96 < rows; r += 128) {
-      a[0] += p[static_cast<long long>(r) * N];
-      a[1] += p[static_cast<long long>(r + 32) * N];
-      a[2] += p[static_cast<long long>(r + 64) * N];
-      a[3] += p[static_cast<long long>(r + 96) * N];
+    for (; r + 15 * 32 < rows; r += 16 * 32) {
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = p[static_cast<long long>(r + 32 * i) * N];
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) v[i] += v[i + w];
+      acc += v[0];
     }
-    for (; r < rows; r += 32) a[0] += p[static_cast<long long>(r) * N];
+    for (; r + 3 * 32 < rows; r += 4 * 32) {
+      float v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = p[static_cast<long long>(r + 32 * i) * N];
+      acc += (v[0] + v[2]) + (v[1] + v[3]);
+    }
+    for (; r < rows; r += 32) acc += p[static_cast<long long>(r) * N];
   }
-  red[warp][lane] = (a[0] + a[1]) + (a[2] + a[3]);
+  red[warp][lane] = acc;
   __syncthreads();
   if (warp == 0 && col < N) {
     float s = red[0][lane];

@@ -34,6 +34,7 @@ cudaError_t run_plain(const Ops<T16>& op, void* y, long long ldy, int M, int N, 
 // split S ways: S minimising ceil(tiles S / units) / S over 1..6, each split
 // keeping at least four k-blocks; no split once the tiles fill a round (the
 // partial slabs would cost more traffic than the last round saves).
+constexpr int kMaxSplits = 6;
 int pick_splits(int M, int N, int K) {
   const int v = pick_grad_variant(M, N);
   const long long tiles = v == 0 ? static_cast<long long>((M + 255) / 256) * ((N + 255) / 256)
@@ -43,7 +44,7 @@ int pick_splits(int M, int N, int K) {
   int best = 1;
   if (tiles >= units) return best;
   double best_cost = 1.0;
-  for (int S = 2; S <= 6 && kb / S >= 4; ++S) {
+  for (int S = 2; S <= kMaxSplits && kb / S >= 4; ++S) {
     const double cost = static_cast<double>((tiles * S + units - 1) / units) / S;
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
@@ -63,13 +64,22 @@ __global__ void splitk_reduce(const float* __restrict__ part, int S, int M, int 
   if (i >= n4) return;
   const long long e = i * 4;
   const int r = static_cast<int>(e / N), c = static_cast<int>(e % N);
-  float4 a = reinterpret_cast<const float4*>(part)[i];
-  for (int sp = 1; sp < S; ++sp) {
-    const float4 b = reinterpret_cast<const float4*>(part + static_cast<long long>(sp) * M * N)[i];
-    a.x += b.x;
-    a.y += b.y;
-    a.z += b.z;
-    a.w += b.w;
+  // every slab's load in flight together (S <= kMaxSplits), then the sum
+  // in slab order
+  float4 v[kMaxSplits];
+#pragma unroll
+  for (int sp = 0; sp < kMaxSplits; ++sp)
+    v[sp] = sp < S ? reinterpret_cast<const float4*>(part + static_cast<long long>(sp) * M * N)[i]
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 a = v[0];
+#pragma unroll
+  for (int sp = 1; sp < kMaxSplits; ++sp) {
+    if (sp < S) {
+      a.x += v[sp].x;
+      a.y += v[sp].y;
+      a.z += v[sp].z;
+      a.w += v[sp].w;
+    }
   }
   *reinterpret_cast<float4*>(out + r * ldo + c) = a;
 }
