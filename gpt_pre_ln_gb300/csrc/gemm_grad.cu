@@ -25,7 +25,12 @@ cudaError_t run_plain(const Ops<T16>& op, void* y, long long ldy, int M, int N, 
   EpiArgs<OutT, T16> ea{nullptr, nullptr, static_cast<OutT*>(y), ldy, M, N, device_error_word()};
   ea.splits = splits;
   const int v = pick_grad_variant(M, N);
-  if (v == 0) return run_2sm<A_MN, B_MN, EPI_NONE, OutT, T16>(op, ea, s);
+  if (v == 0) return run_2sm<kPairBN, A_MN, B_MN, EPI_NONE, OutT, T16>(op, ea, s);
+  // the D-wide input gradients over a long K (dX of c_fc and c_attn, and
+  // dxf over the vocabulary): the 192-wide pair tile
+  if constexpr (!A_MN && sizeof(OutT) == 4) {
+    if (use_pair192(M, N, op.K)) return run_2sm<192, A_MN, B_MN, EPI_NONE, OutT, T16>(op, ea, s);
+  }
   return run_1sm<192, A_MN, B_MN, EPI_NONE, OutT, T16>(op, ea, s);
 }
 
@@ -129,7 +134,7 @@ cudaError_t launch_gemm_dlogits(const void* xf, const void* wte, int M, int V, i
   ea.row_lse = row_lse;
   ea.inv_n = inv_n;
   const Ops<T16> op{static_cast<const T16*>(xf), D, static_cast<const T16*>(wte), D, D};
-  if (pick_grad_variant(M, V) == 0) return run_2sm<false, false, EPI_DZ, T16, T16>(op, ea, s);
+  if (pick_grad_variant(M, V) == 0) return run_2sm<kPairBN, false, false, EPI_DZ, T16, T16>(op, ea, s);
   return run_1sm<192, false, false, EPI_DZ, T16, T16>(op, ea, s);
 }
 

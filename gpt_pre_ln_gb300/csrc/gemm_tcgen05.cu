@@ -42,7 +42,7 @@ cudaError_t launch(const void* x, const void* w, const void* bias, const float* 
     return launch_gemm_rows_16(Type16<T16>::kFormat == 0 ? GPT2_F16 : GPT2_BF16, x, w, bias, residual, y, M, N, K,
                                ldy, w_out_in, epilogue, y_t, stream);
   const int m = static_cast<int>(M);
-  const int v = pick_variant(m, N);
+  const int v = pick_variant(m, N, K, epilogue == GPT2_EPI_BIAS_RESIDUAL);
   const T16* X = static_cast<const T16*>(x);
   const T16* W = static_cast<const T16*>(w);
   const T16* Bv = static_cast<const T16*>(bias);
@@ -55,7 +55,7 @@ cudaError_t launch_lse(const void* x, const void* w, int64_t M, int N, int K, co
                        float2* part, float* tgt, int* n_part, cudaStream_t stream) {
   const int m = static_cast<int>(M);
   const int v = pick_variant(m, N);
-  const int bn = v == 0 ? kPairBN : v;
+  const int bn = variant_bn(v);
   *n_part = 2 * ((N + bn - 1) / bn);
   EpiArgs<float, T16> ea{nullptr, nullptr, nullptr, 0, m, N, device_error_word(), labels, T, part, tgt};
   const Ops<T16> op{static_cast<const T16*>(x), K, static_cast<const T16*>(w), K, K};

@@ -707,14 +707,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------ CTA pair
+// Pair tiles of 256 x PBN: PBN = 256 for wide outputs, 192 for the D-wide
+// ones (N = 768: 128 tiles for 76 pairs, two rounds of 1.68 tiles, where
+// the 256-wide tile leaves 96 tiles and the same two rounds of a longer
+// tile).  Each CTA holds 128 rows of the tile and stages PBN / 2 columns of
+// B per k-block; with B MN-major those are whole 64-column swizzle atoms
+// (128 columns, of which the MMA reads PBN / 2).
 constexpr int kPairBN = 256;
 
-template <bool A_MN, bool B_MN, int EPI, typename OutT, typename T16>
+template <int PBN, bool A_MN, bool B_MN, int EPI, typename OutT, typename T16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
              const __grid_constant__ CUtensorMap tmY, const EpiArgs<OutT, T16> ea, int K) {
-  using Cfg = GemmCfg<kPairBN, kPairBN / 2>;
+  static_assert(PBN == 256 || PBN == 192, "pair tile width");
+  using Cfg = GemmCfg<PBN, 128>;
   constexpr int STAGES = Cfg::STAGES;
+  constexpr int kBAtoms = (PBN / 2 + 63) / 64;  // MN-major B: 64-column boxes per CTA
+  constexpr int kBLoadBytes = B_MN ? kBAtoms * 64 * kBK * 2 : (PBN / 2) * kBK * 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -739,7 +748,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int num_pairs = gridDim.x >> 1;
   const int M = ea.M, N = ea.N;
   const int m_units = (M + 2 * kBM - 1) / (2 * kBM);
-  const int n_tiles = (N + kPairBN - 1) / kPairBN;
+  const int n_tiles = (N + PBN - 1) / PBN;
   constexpr bool kSplit = A_MN;  // split K only for the weight gradients
   const int n_splits = kSplit && ea.splits > 1 ? ea.splits : 1;
   const int tiles_per_split = m_units * n_tiles;
@@ -794,7 +803,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
         const int tt = kSplit ? tile % tiles_per_split : tile;
         const int m0 = (tt % m_units) * (2 * kBM) + static_cast<int>(rank) * kBM;
-        const int nb = (tt / m_units) * kPairBN + static_cast<int>(rank) * (kPairBN / 2);
+        const int nb = (tt / m_units) * PBN + static_cast<int>(rank) * (PBN / 2);
         int kb_lo, kb_hi;
         kb_range(tile, kb_lo, kb_hi);
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
@@ -804,7 +813,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t fb = mapa_shared(full_bar(stage), 0);  // the even CTA's barrier
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::STAGE_BYTES);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * (Cfg::A_BYTES + kBLoadBytes));
           const uint32_t a_dst = smem_u32(sA + stage * Cfg::A_BYTES);
           if constexpr (A_MN) {
             tma_load_2d_pair(a_dst, &tmA, fb, m0, kb * kBK);
@@ -815,7 +824,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t b_dst = smem_u32(sB + stage * Cfg::B_BYTES);
           if constexpr (B_MN) {
 #pragma unroll
-            for (int j = 0; j < kPairBN / 128; ++j)
+            for (int j = 0; j < kBAtoms; ++j)
               tma_load_2d_pair(b_dst + j * (kBK * 128), &tmB, fb, nb + j * 64, kb * kBK);
           } else {
             tma_load_2d_pair(b_dst, &tmB, fb, kb * kBK, nb);
@@ -833,7 +842,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ------------------------------------------------ pair MMA issuer
-      constexpr uint32_t idesc = idesc_f16kind_f32(2 * kBM, kPairBN, A_MN, B_MN, Type16<T16>::kFormat);
+      constexpr uint32_t idesc = idesc_f16kind_f32(2 * kBM, PBN, A_MN, B_MN, Type16<T16>::kFormat);
       constexpr uint16_t kBoth = 0x3;
       int stage = 0;
       uint32_t phase = 0;
@@ -849,7 +858,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * kPairBN;
+        const uint32_t d_tmem = tmem_base + acc * PBN;
         int kb_lo, kb_hi;
         kb_range(tile, kb_lo, kb_hi);
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
@@ -889,7 +898,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    epilogue_role<kPairBN, EPI, OutT, T16, true, A_MN>(ea, &tmY, warp, lane, smem_u32(sOut), smem_u32(sBias),
+    epilogue_role<PBN, EPI, OutT, T16, true, A_MN>(ea, &tmY, warp, lane, smem_u32(sOut), smem_u32(sBias),
                                             bias_full_bar(0), bias_full_bar(1), bias_empty_bar(0), bias_empty_bar(1),
                                             tmem_base, tfull_bar(0), tfull_bar(1),
                                             mapa_shared(tempty_bar(0), 0), mapa_shared(tempty_bar(1), 0), pair,
@@ -987,16 +996,16 @@ cudaError_t run_1sm(const Ops<T16>& op, const EpiArgs<OutT, T16>& ea, cudaStream
   return launch_pdl(kern, ctas, kThreads, Cfg::SMEM_BYTES, stream, 0, ta, tb, ty, ea, op.K);
 }
 
-template <bool A_MN, bool B_MN, int EPI, typename OutT, typename T16>
+template <int PBN, bool A_MN, bool B_MN, int EPI, typename OutT, typename T16>
 cudaError_t run_2sm(const Ops<T16>& op, const EpiArgs<OutT, T16>& ea, cudaStream_t stream) {
-  using Cfg = GemmCfg<kPairBN, kPairBN / 2>;
-  auto kern = gemm_2sm<A_MN, B_MN, EPI, OutT, T16>;
+  using Cfg = GemmCfg<PBN, 128>;
+  auto kern = gemm_2sm<PBN, A_MN, B_MN, EPI, OutT, T16>;
   static int configured[64] = {0};
   cudaError_t e = set_smem_once(kern, Cfg::SMEM_BYTES, configured);
   if (e != cudaSuccess) return e;
   const int M = ea.M, N = ea.N;
   CUtensorMap ta, tb;
-  if (!make_operand_maps<A_MN, B_MN>(&ta, &tb, op, M, N, kPairBN / 2)) return cudaErrorInvalidValue;
+  if (!make_operand_maps<A_MN, B_MN>(&ta, &tb, op, M, N, PBN / 2)) return cudaErrorInvalidValue;
   // pairs that can be resident at once (a pair needs two SMs of one GPC)
   static int max_pairs[64] = {0};
   int dev = 0;
@@ -1018,26 +1027,41 @@ cudaError_t run_2sm(const Ops<T16>& op, const EpiArgs<OutT, T16>& ea, cudaStream
     max_pairs[dev] = n < num_sms() / 2 ? n : num_sms() / 2;
   }
   const int pairs_max = (dev >= 0 && dev < 64) ? max_pairs[dev] : num_sms() / 2;
-  const int tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kPairBN - 1) / kPairBN) * (ea.splits > 1 ? ea.splits : 1);
+  const int tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + PBN - 1) / PBN) * (ea.splits > 1 ? ea.splits : 1);
   const int pairs = tiles < pairs_max ? tiles : pairs_max;
   CUtensorMap ty = ta;  // EPI_LSE stores no tile (a valid map, never used)
   if (EPI != EPI_LSE && !make_out_map(&ty, ea)) return cudaErrorInvalidValue;
   return launch_pdl(kern, 2 * pairs, kThreads, Cfg::SMEM_BYTES, stream, 0, ta, tb, ty, ea, op.K);
 }
 
-// Kernel variant for an M x N problem: 0 = CTA pair (256 x 256 tiles),
-// otherwise the tile width of the single-CTA kernel.  Measured on the GPT-2
-// shapes: the pair wins wherever the output is wide (c_attn, c_fc, lm_head:
-// its per-SM operand traffic is lower); for D-wide outputs (N <= 1024) its
-// 256-wide tiles leave too few tiles for 76 pairs and the single-CTA kernel
-// with the tile width that needs the fewest rounds wins.
-int pick_variant(int M, int N) {
+// The 256 x 192 pair tile for a D-wide output (N <= 1024) with a long K:
+// these products are bound by the operand stream from L2 (M = 8192,
+// N = 768, K = 3072: ~500 MB from L2 per launch with 128 x 192 tiles), and
+// the pair reads a fifth less per output; at K = 768 the pair's start-up
+// costs more than that saves (measured: 37.6 against 38.9 us at K = 3072,
+// 16.2 against 14.4 us at K = 768).
+bool use_pair192(int M, int N, int K) { return M >= 2 * kBM && N > 128 && N <= 1024 && K >= 2048; }
+
+// Kernel variant for an M x N problem: 0 = CTA pair with 256 x 256 tiles,
+// 1 = CTA pair with 256 x 192 tiles, otherwise the tile width of the
+// single-CTA kernel.  Measured on the GPT-2 shapes: the pair wins wherever
+// the output is wide (c_attn, c_fc, lm_head: its per-SM operand traffic is
+// lower); for D-wide outputs (N <= 1024) its 256-wide tiles leave too few
+// tiles for 76 pairs: the 192-wide pair tile where use_pair192 says so (and
+// the caller offers it: the residual epilogue), else the single-CTA tile
+// width that needs the fewest rounds.
+constexpr int kVariantPair192 = 1;
+int variant_bn(int v) { return v == 0 ? 256 : v == kVariantPair192 ? 192 : v; }
+int pick_variant(int M, int N, int K = 0, bool pair192 = false) {
 #ifdef GPT2_GEMM_FORCE_BN
   (void)M;
   (void)N;
+  (void)K;
+  (void)pair192;
   return GPT2_GEMM_FORCE_BN;
 #else
   if (M >= 2 * kBM && N > 1024) return 0;
+  if (pair192 && use_pair192(M, N, K)) return kVariantPair192;
   const int sms = num_sms();
   int best = 192;
   long long best_cost = -1;
@@ -1058,8 +1082,13 @@ int pick_variant(int M, int N) {
 
 template <bool A_MN, bool B_MN, int EPI, typename OutT, typename T16>
 cudaError_t run_variant(int v, const Ops<T16>& op, const EpiArgs<OutT, T16>& ea, cudaStream_t s) {
+  if constexpr (EPI == EPI_RES) {
+    if (v == kVariantPair192) return run_2sm<192, A_MN, B_MN, EPI, OutT, T16>(op, ea, s);
+  } else {
+    if (v == kVariantPair192) v = 192;
+  }
   switch (v) {
-    case 0: return run_2sm<A_MN, B_MN, EPI, OutT, T16>(op, ea, s);
+    case 0: return run_2sm<kPairBN, A_MN, B_MN, EPI, OutT, T16>(op, ea, s);
     case 128: return run_1sm<128, A_MN, B_MN, EPI, OutT, T16>(op, ea, s);
     case 192: return run_1sm<192, A_MN, B_MN, EPI, OutT, T16>(op, ea, s);
     default: return run_1sm<256, A_MN, B_MN, EPI, OutT, T16>(op, ea, s);

@@ -79,6 +79,7 @@ LINEAR_CASES = [
     (257, 768, 3072, G.W_IN_OUT),     # mlp c_proj (K = 4D)
     (1, 256, 64, G.W_IN_OUT),         # single row, single k-block
     (300, 1000, 768, G.W_OUT_IN),     # lm_head style, ragged N
+    (520, 1000, 768, G.W_IN_OUT),     # ragged N in the last 192-wide pair tile, W read N-major
     (130, 50257, 768, G.W_OUT_IN),    # full vocabulary
     # few rows (one token per sequence of a decode step): the swapped-operand
     # kernel with K split over a thread-block cluster
