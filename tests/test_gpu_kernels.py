@@ -80,6 +80,7 @@ LINEAR_CASES = [
     (1, 256, 64, G.W_IN_OUT),         # single row, single k-block
     (300, 1000, 768, G.W_OUT_IN),     # lm_head style, ragged N
     (520, 1000, 768, G.W_IN_OUT),     # ragged N in the last 192-wide pair tile, W read N-major
+    (300, 3072, 768, G.W_IN_OUT),     # c_fc shape over two 256-row pair units (the second ragged)
     (130, 50257, 768, G.W_OUT_IN),    # full vocabulary
     # few rows (one token per sequence of a decode step): the swapped-operand
     # kernel with K split over a thread-block cluster

@@ -115,6 +115,17 @@ def test_train_step_switches_and_ragged():
     _compare(dims, params, tokens, gd, loss, flags)
 
 
+@pytest.mark.parametrize("d_model,n_head", [(1024, 16), (1600, 25)])
+def test_train_step_wide_rows(d_model, n_head):
+    """The GPT-2 medium and XL widths (the LayerNorm backward holds 8 and 13
+    groups of four columns per lane), one layer, a ragged row count."""
+    dims = synth.Dims(n_layer=1, d_model=d_model, n_head=n_head, d_ff=4 * d_model, vocab=600, n_pos=96)
+    params, d = synth.draw_model(dims, "bf16", 905 + n_head)
+    tokens = synth.draw_tokens(d, 3, 83, dims.vocab)
+    loss, gd = _train_step(dims, params, tokens)
+    _compare(dims, params, tokens, gd, loss)
+
+
 def test_train_step_is_deterministic():
     dims = synth.Dims(n_layer=2, d_model=128, n_head=2, d_ff=512, vocab=1000, n_pos=300)
     params, d = synth.draw_model(dims, "bf16", 904)
