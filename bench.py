@@ -61,6 +61,43 @@ WORKLOAD = "gpt2_small_fwd_b8_t1024"
 METRIC = "tokens/s GPT-2 small fwd B=8 T=1024 bf16; % tensor-core peak; decode % HBM BW"
 
 
+def _gpu_numa_cpus(dev):
+    """The host CPUs of the NUMA node the GPU hangs off (from its PCI
+    function's sysfs entry), or None where that is not known."""
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        bus = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{bus}/numa_node") as f:
+            node = int(f.read().strip())
+        if node < 0:
+            return None
+        cpus = set()
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            for part in f.read().strip().split(","):
+                lo, _, hi = part.partition("-")
+                cpus.update(range(int(lo), int(hi or lo) + 1))
+        cpus &= os.sched_getaffinity(0)
+        return cpus or None
+    except (OSError, ValueError, AttributeError):
+        return None
+
+
+def _pinned_near_gpu(dev, make):
+    """Runs make() (which allocates and fills pinned host buffers) on the CPUs
+    of the GPU's NUMA node, so that the pages land in the memory next to the
+    GPU's host link, then restores the thread's CPU set."""
+    cpus = _gpu_numa_cpus(dev)
+    if not cpus:
+        return make()
+    old = os.sched_getaffinity(0)
+    os.sched_setaffinity(0, cpus)
+    try:
+        return make()
+    finally:
+        os.sched_setaffinity(0, old)
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -826,8 +863,12 @@ def run_ours(args):
     # Every step copies its token ids host -> device and its full bf16 logits
     # device -> host (pinned memory).  The copy-out of step i runs on a second
     # stream while step i+1 computes (two device and two host logits buffers).
-    h_tok = torch.from_numpy(tokens_np.copy()).pin_memory()
-    h_log = [torch.empty(B, T, ld, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    def make_host():
+        ht = torch.from_numpy(tokens_np.copy()).pin_memory()
+        hl = [torch.zeros(B, T, ld, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        return ht, hl
+
+    h_tok, h_log = _pinned_near_gpu(torch.cuda.current_device(), make_host)
     d_log = [logits, torch.empty_like(logits)]
     copy_stream = torch.cuda.Stream()
     fwd_done = [torch.cuda.Event() for _ in range(2)]

@@ -129,20 +129,6 @@ __device__ __forceinline__ float mlp_act(float x, bool exact) {
   return OUT16 ? gelu_new_fast(x) : gelu_new_accurate(x);
 }
 
-// The same over a chunk of N values, with one branch for the whole chunk
-// (`exact` is uniform across the warp) so that the default path keeps its
-// straight-line code.
-template <bool OUT16, int N>
-__device__ __forceinline__ void mlp_act_chunk(float (&v)[N], bool exact) {
-  if (exact) {
-#pragma unroll
-    for (int i = 0; i < N; ++i) v[i] = gelu_exact(v[i]);
-  } else {
-#pragma unroll
-    for (int i = 0; i < N; ++i) v[i] = OUT16 ? gelu_new_fast(v[i]) : gelu_new_accurate(v[i]);
-  }
-}
-
 // Two fp32 FMAs in one instruction (sm_100 family): d = a * b + c for each
 // half of the pair, rounded to nearest: the same results as two fmaf calls.
 __device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
@@ -177,6 +163,36 @@ __device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
       : "=f"(d.x), "=f"(d.y)
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
+}
+
+// gelu_new_fast on a pair, with the paired fp32 instructions: the same
+// operations in the same order, so the same results as two scalar calls.
+__device__ __forceinline__ float2 gelu_new_fast2(float2 x) {
+  const float2 u = mul_f32x2(make_float2(0.7978845608028654f, 0.7978845608028654f),
+                             fma_f32x2(mul_f32x2(make_float2(0.044715f, 0.044715f), x), mul_f32x2(x, x), x));
+  const float2 hx = mul_f32x2(make_float2(0.5f, 0.5f), x);
+  return fma_f32x2(hx, make_float2(tanh_hw(u.x), tanh_hw(u.y)), hx);
+}
+
+// The activation over a chunk of N values (N even), with one branch for the
+// whole chunk (`exact` is uniform across the warp) so that the default path
+// keeps its straight-line code.
+template <bool OUT16, int N>
+__device__ __forceinline__ void mlp_act_chunk(float (&v)[N], bool exact) {
+  if (exact) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = gelu_exact(v[i]);
+  } else if constexpr (OUT16) {
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+      const float2 g = gelu_new_fast2(make_float2(v[i], v[i + 1]));
+      v[i] = g.x;
+      v[i + 1] = g.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = gelu_new_accurate(v[i]);
+  }
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -155,9 +155,9 @@ __device__ __forceinline__ void apply_bias_act_smem(float (&v)[OutTraits<OutT>::
     const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float2 f = Type16<T16>::unpack2(w[e]);
-      v[q * 8 + 2 * e] += f.x;
-      v[q * 8 + 2 * e + 1] += f.y;
+      const float2 f = add_f32x2(make_float2(v[q * 8 + 2 * e], v[q * 8 + 2 * e + 1]), Type16<T16>::unpack2(w[e]));
+      v[q * 8 + 2 * e] = f.x;
+      v[q * 8 + 2 * e + 1] = f.y;
     }
   }
   if constexpr (EPI == EPI_GELU) mlp_act_chunk<sizeof(OutT) == 2>(v, gelu_exact_on);
