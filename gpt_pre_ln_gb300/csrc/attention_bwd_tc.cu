@@ -286,15 +286,18 @@ __global__ void __launch_bounds__(kThreads, 2)
           tmem_ld_32x32b_x32(tS + c * 32, rs);
           tmem_ld_32x32b_x32(tDP + c * 32, rp);
           tmem_ld_wait();
+          // p = 2^(s c log2(e) - lse), ds = p (dp - delta) c on paired fp32
+          // instructions (the same operations as scalar code)
+          const float2 sl2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(-lse2, -lse2);
+          const float2 nd2 = make_float2(-dl, -dl), sc2 = make_float2(score_scale, score_scale);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            float ds[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float p = ex2_approx(fmaf(__uint_as_float(rs[2 * i + e]), scale_log2, -lse2));
-              ds[e] = p * (__uint_as_float(rp[2 * i + e]) - dl) * score_scale;
-            }
-            pk[i] = pack_masked<T16>(ds[0], ds[1], d < 0 || 2 * i <= lane, d < 0 || 2 * i + 1 <= lane);
+            const float2 x = fma_f32x2(make_float2(__uint_as_float(rs[2 * i]), __uint_as_float(rs[2 * i + 1])), sl2, nl2);
+            const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            const float2 ds = mul_f32x2(
+                mul_f32x2(pp, add_f32x2(make_float2(__uint_as_float(rp[2 * i]), __uint_as_float(rp[2 * i + 1])), nd2)),
+                sc2);
+            pk[i] = pack_masked<T16>(ds.x, ds.y, d < 0 || 2 * i <= lane, d < 0 || 2 * i + 1 <= lane);
           }
         }
         tmem_st_32x32b_x16(tS + c * 16, pk);  // over S columns already read
@@ -497,10 +500,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int q0 = (qi0 + i) * 64;
       const int sl = i & 1;
       {
-        // this tile's 64 row statistics into the slot (rows past T: zero)
+        // this tile's 64 row statistics, negated, into the slot (rows past
+        // T: zero)
         const int qq = q0 + (t & 63);
         const float v = qq < T ? (t < 64 ? lse[stat0 + qq] : delta[stat0 + qq]) : 0.f;
-        (t < 64 ? s_lse : s_dl)[sl * 64 + (t & 63)] = v;
+        (t < 64 ? s_lse : s_dl)[sl * 64 + (t & 63)] = -v;
       }
       named_bar_sync(1, 128);
       if (!ok) continue;
@@ -525,21 +529,24 @@ __global__ void __launch_bounds__(kThreads, 2)
           tmem_ld_32x32b_x32(tS + c * 32, rs);
           tmem_ld_32x32b_x32(tDP + c * 32, rp);
           tmem_ld_wait();
-          const float* ls = s_lse + sl * 64 + c * 32;
-          const float* dls = s_dl + sl * 64 + c * 32;
+          const float2* nls = reinterpret_cast<const float2*>(s_lse + sl * 64 + c * 32);  // -lse
+          const float2* nds = reinterpret_cast<const float2*>(s_dl + sl * 64 + c * 32);   // -delta
+          const float2 sl2 = make_float2(scale_log2, scale_log2), sc2 = make_float2(score_scale, score_scale);
+          // p and ds on paired fp32 instructions (the same operations as
+          // scalar code)
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            float p[2], ds[2];
             bool vis[2];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int qi = 2 * e + u;
-              vis[u] = (d > 0 || lane <= qi) && qc0 + qi < T;
-              p[u] = ex2_approx(fmaf(__uint_as_float(rs[qi]), scale_log2, -ls[qi]));
-              ds[u] = p[u] * (__uint_as_float(rp[qi]) - dls[qi]) * score_scale;
-            }
-            pk[e] = pack_masked<T16>(p[0], p[1], vis[0], vis[1]);
-            dk[e] = pack_masked<T16>(ds[0], ds[1], vis[0], vis[1]);
+            for (int u = 0; u < 2; ++u) vis[u] = (d > 0 || lane <= 2 * e + u) && qc0 + 2 * e + u < T;
+            const float2 x =
+                fma_f32x2(make_float2(__uint_as_float(rs[2 * e]), __uint_as_float(rs[2 * e + 1])), sl2, nls[e]);
+            const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            const float2 ds = mul_f32x2(
+                mul_f32x2(p, add_f32x2(make_float2(__uint_as_float(rp[2 * e]), __uint_as_float(rp[2 * e + 1])), nds[e])),
+                sc2);
+            pk[e] = pack_masked<T16>(p.x, p.y, vis[0], vis[1]);
+            dk[e] = pack_masked<T16>(ds.x, ds.y, vis[0], vis[1]);
           }
         }
         tmem_st_32x32b_x16(tS + c * 16, pk);   // P^T over S^T columns already read
