@@ -340,60 +340,21 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
           break;
         }
         tc_fence_after();
-        // pass 1: row maximum of the raw scores (8 independent partial
-        // maxima, three-input max; the scale is positive, so it is applied
-        // once to the maximum); chunks wholly above the diagonal skipped
-        float pm[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) pm[e] = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kTk / 32; ++c) {
-          const int d = attn_chunk_offset(j, c, qt, quad);
-          if (d > 0) continue;
-          uint32_t raw[32];
-          tmem_ld_32x32b_x32(tS + c * 32, raw);
-          tmem_ld_wait();
-          if (d == 0) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i <= lane) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(raw[i]));
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pm[i & 7] = max3f(pm[i & 7], __uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]));
-          }
-        }
-        const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                               fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * scale;
-        const bool raise = mx > m_run + kRescaleLog2;
-        // tcgen05.ld / tcgen05.st are warp-collective: the whole warp takes
-        // the rescale branch if any of its rows needs it (alpha = 1 for the
-        // others)
-        if (j > 0 && __any_sync(0xffffffffu, raise)) {
-          // O and l were accumulated against m_run: bring them to mx
-          const float alpha = raise ? ex2_approx(m_run - mx) : 1.f;
-          l *= alpha;
-#pragma unroll
-          for (int c = 0; c < kHd / 32; ++c) {
-            uint32_t raw[32];
-            tmem_ld_32x32b_x32(tO + c * 32, raw);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) raw[i] = __float_as_uint(__uint_as_float(raw[i]) * alpha);
-            tmem_st_32x32b_x32(tO + c * 32, raw);
-          }
-        }
-        if (raise) m_run = mx;
-        // pass 2: P = exp2(s * scale - m_run) as 16-bit values, 16 columns
-        // per 32-key chunk, written over S columns this thread has already
-        // read (chunk c's P lands in columns 16c .. 16c + 15 < 32c + 32);
-        // paired fp32 arithmetic, 4 independent pair sums; masked chunks
-        // are written as zeros
+        // One pass per 32-key chunk, each score read once from tensor
+        // memory: the chunk's row maximum (masked on the diagonal; the scale
+        // is positive, so it is applied once to the maximum), then
+        // P = exp2(s * scale - m_run) as 16-bit values written over S
+        // columns this thread has already read (chunk c's P lands in columns
+        // 16c .. 16c + 15 < 32c + 32), paired fp32 arithmetic, 4 independent
+        // pair sums; chunks wholly above the diagonal are written as zeros.
+        // m_run is raised only when a chunk's maximum exceeds it by more
+        // than 8 (log2 units); then O (from earlier tiles of the item), l,
+        // this tile's sums so far and the P already written for chunk 0 are
+        // brought to the new maximum first.
         float2 ps[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) ps[e] = make_float2(0.f, 0.f);
         const float2 scale2 = make_float2(scale, scale);
-        const float2 neg_m2 = make_float2(-m_run, -m_run);
 #pragma unroll
         for (int c = 0; c < kTk / 32; ++c) {
           const int d = attn_chunk_offset(j, c, qt, quad);
@@ -405,6 +366,55 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             uint32_t raw[32];
             tmem_ld_32x32b_x32(tS + c * 32, raw);
             tmem_ld_wait();
+            float pm[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pm[e] = -INFINITY;
+            if (d == 0) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i <= lane) pm[i & 3] = fmaxf(pm[i & 3], __uint_as_float(raw[i]));
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                pm[i & 3] = max3f(pm[i & 3], __uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]));
+            }
+            const float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])) * scale;
+            const bool raise = mx > m_run + kRescaleLog2;
+            // tcgen05.ld / tcgen05.st are warp-collective: the whole warp
+            // takes the rescale branch if any of its rows needs it (alpha = 1
+            // for the others; alpha = 0 for a row's first keys, m_run = -inf)
+            if (__any_sync(0xffffffffu, raise)) {
+              const float alpha = raise ? ex2_approx(m_run - mx) : 1.f;
+              const float2 alpha2 = make_float2(alpha, alpha);
+              l *= alpha;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) ps[e] = mul_f32x2(ps[e], alpha2);
+              if (j > 0) {  // (the item's first P.V overwrites O)
+#pragma unroll 1
+                for (int h = 0; h < kHd / 16; ++h) {  // 16 columns at a time (the scores stay in registers)
+                  uint32_t o[16];
+                  tmem_ld_32x32b_x16(tO + h * 16, o);
+                  tmem_ld_wait();
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                  tmem_st_32x32b_x16(tO + h * 16, o);
+                }
+              }
+              if (c > 0) {  // chunk 0's P, written against the old maximum
+                uint32_t p0[16];
+                tmem_st_wait();
+                tmem_ld_32x32b_x16(tP, p0);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  const float2 q = Type16<T16>::unpack2(p0[i]);
+                  p0[i] = Type16<T16>::pack2(q.x * alpha, q.y * alpha);
+                }
+                tmem_st_32x32b_x16(tP, p0);
+              }
+              if (raise) m_run = mx;
+            }
+            const float2 neg_m2 = make_float2(-m_run, -m_run);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const float2 x = fma_f32x2(make_float2(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])),

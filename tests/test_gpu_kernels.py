@@ -240,6 +240,42 @@ def test_attention_causality_on_gpu():
     assert not torch.equal(out1[:, i + 1:], out2[:, i + 1:])
 
 
+@pytest.mark.parametrize("growth", [0.05, 0.5])
+def test_attention_rising_scores(growth):
+    """Keys whose scale grows along the sequence, so that a row's running
+    maximum keeps rising by more than the kernel's rescale threshold (8 in
+    log2 units) from chunk to chunk and tile to tile: every rescale path (the
+    accumulated output, the sums, and the probabilities already written for
+    the tile's first chunk) runs; the output and the row log-sum-exps stay
+    within the bounds of the plain case."""
+    B, T, H = 2, 400, 3
+    D = 64 * H
+    r = rng(1300 + int(growth * 100))
+    qkv = r.standard_normal((B, T, 3 * D))
+    qkv[:, :, D:2 * D] *= (1.0 + growth * np.arange(T))[None, :, None] / 4.0
+    qkv = bf16(qkv)
+    out = torch.full((B, T, D), float("nan"), device="cuda", dtype=torch.bfloat16)
+    lse = torch.full((B, H, T), float("nan"), device="cuda")
+    G.gpt2_attention_causal_lse(to_t(qkv, "bf16"), out, lse, B, T, H, 64, 0.125, G.BF16)
+    torch.cuda.synchronize()
+    ref = O.causal_attention(qkv, H)
+    q, k, v = O.split_qkv_heads(qkv, H)
+    pav = O.merge_heads(O.causal_probs(q, k) @ np.abs(v))
+    assert_close_elementwise(to_np(out), ref, 2.0 ** -8 * np.abs(ref) + 2.0 ** -8 * pav + 1e-6, f"growth {growth}")
+    s_ = (q @ np.swapaxes(k, -1, -2)) / 8.0
+    s_ = np.where(np.tril(np.ones((T, T), bool)), s_, -np.inf)
+    ref_lse = O.logsumexp(s_) / np.log(2.0)
+    # each score is an fp32 sum of 64 exact products: |error| <= 64 u sum |q_d k_d| / 8
+    # (u = 2^-24), in log2 units; the log-sum-exp moves by at most the largest
+    # of its scores' errors (plus fp32 rounding of its own, 1e-4)
+    sabs = (np.abs(q) @ np.swapaxes(np.abs(k), -1, -2)) / 8.0
+    sabs = np.where(np.tril(np.ones((T, T), bool)), sabs, 0.0)
+    bound = 1e-4 + 2.0 * 64 * 2.0 ** -24 * sabs.max(-1) / np.log(2.0)
+    assert np.all(np.abs(to_np(lse) - ref_lse) <= bound)
+    # the scores of the last rows span far more than the threshold
+    assert (s_[:, :, -1, :].max(-1) - s_[:, :, -1, :64].max(-1)).max() / np.log(2.0) > 8.0
+
+
 # ------------------------------------------------------------------------ MLP
 @pytest.mark.parametrize("with_res", [True, False])
 def test_mlp_bf16(with_res):
